@@ -1,0 +1,312 @@
+"""Pins for the fp64 oracle: facts that the pages and the mathematics fix, checked
+against routines other than the ones the oracle itself calls.
+
+Each test names the passage it pins. A plausible slip in the oracle (a dropped
+(R0 R0^T)^-1, a transposed factor, a wrong Monarch index, a missing bias, an off-by-one
+in Newton-Schulz) fails at least one of them.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as WL
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _orth(rng, rows, cols):
+    q, _ = np.linalg.qr(rng.standard_normal((rows, cols)))
+    return q
+
+
+def _top_left_projector(W, p):
+    """Projector onto W's top-p left singular subspace, via eigh of W W^T
+    (a different LAPACK route from the oracle's SVD)."""
+    w, v = np.linalg.eigh(W @ W.T)
+    top = v[:, np.argsort(w)[::-1][:p]]
+    return top @ top.T
+
+
+def _small_case(seed=0, n=40, d=24, m=36, k=5, r=4, batch=3):
+    rng = _rng(seed)
+    W = rng.standard_normal((d, m)) * (np.arange(1, d + 1) ** -0.5)[:, None]
+    b = rng.standard_normal(m) * 0.1
+    X = rng.standard_normal((batch, n, d)) * np.linspace(3.0, 0.3, d)[None, None, :]
+    return W, b, X, k, r
+
+
+# -------------------------------------------------------------------- static fit
+
+def test_tsvd_is_frobenius_optimal_rank_k():
+    """Appendix B (truncated SVD is the best rank-k approximation in Frobenius norm):
+    ||W - W_hat||_F^2 equals the sum of the trailing eigenvalues of W^T W."""
+    W, _, _, k, _ = _small_case()
+    U, V = O.tsvd_factors(W, k)
+    What = O.lowrank_dense(U, V)
+    lam = np.sort(np.linalg.eigvalsh(W.T @ W))[::-1]
+    assert np.linalg.matrix_rank(What) == k
+    assert np.isclose(np.linalg.norm(W - What) ** 2, lam[k:].sum(), rtol=1e-10)
+    # W_hat is the projection of W onto its top-k left singular subspace
+    assert np.allclose(What, _top_left_projector(W, k) @ W, atol=1e-11)
+    # even split of the singular values: U^T U == V V^T (both diag(S_k))
+    assert np.allclose(U.T @ U, V @ V.T, atol=1e-11)
+
+
+def _planted_monarch(rng, nb, bi, bo):
+    """Dense matrix built entry by entry from W[(a,i),(c,j)] = B1[a][i,c] B2[c][a,j]."""
+    B1 = rng.standard_normal((nb, bi, nb))
+    B2 = rng.standard_normal((nb, nb, bo))
+    W = np.zeros((nb * bi, nb * bo))
+    for a in range(nb):
+        for i in range(bi):
+            for c in range(nb):
+                for j in range(bo):
+                    W[a * bi + i, c * bo + j] = B1[a][i, c] * B2[c][a, j]
+    return W, B1, B2
+
+
+def test_monarch_dense_matches_index_form():
+    """Appendix B / blog structured-methods section: block-diagonal . stride permutation .
+    block-diagonal equals the per-block rank-1 index form."""
+    rng = _rng(1)
+    W, B1, B2 = _planted_monarch(rng, 4, 3, 5)
+    assert np.allclose(O.monarch_dense(B1, B2), W, atol=1e-13)
+
+
+def test_monarch_fit_recovers_planted_monarch():
+    rng = _rng(2)
+    W, _, _ = _planted_monarch(rng, 4, 4, 4)
+    B1, B2 = O.monarch_factors(W, 4)
+    assert np.linalg.norm(W - O.monarch_dense(B1, B2)) < 1e-12 * np.linalg.norm(W)
+
+
+def test_monarch_fit_is_blockwise_optimal():
+    """The fit's error equals the sum over blocks of the non-leading eigenvalues of each
+    block's Gram matrix (best rank-1 per block)."""
+    rng = _rng(3)
+    nb, bi, bo = 4, 4, 6
+    W = rng.standard_normal((nb * bi, nb * bo))
+    B1, B2 = O.monarch_factors(W, nb)
+    err = np.linalg.norm(W - O.monarch_dense(B1, B2)) ** 2
+    tail = 0.0
+    for a in range(nb):
+        for c in range(nb):
+            blk = W[a * bi:(a + 1) * bi, c * bo:(c + 1) * bo]
+            lam = np.sort(np.linalg.eigvalsh(blk @ blk.T))[::-1]
+            tail += lam[1:].sum()
+    assert np.isclose(err, tail, rtol=1e-10)
+
+
+# -------------------------------------------------------------------- residual / R0 / P
+
+def test_residual_split_is_exact():
+    """Blog residual-split section: X W = X W_hat + X W_res."""
+    W, _, X, k, r = _small_case()
+    prep = O.prepare(W, np.zeros(W.shape[1]), "lowrank", k, r)
+    XU = X @ prep["F1"]
+    lhs = XU @ prep["F2"] + X @ prep["W_res"]
+    assert np.allclose(lhs, X @ W, atol=1e-12)
+
+
+def test_r0_is_next_singular_block_for_lowrank():
+    """2.3 / blog one-step section: for a low-rank W_hat the residual's top-r right singular
+    vectors span W's right singular vectors k+1..k+r."""
+    W, _, _, k, r = _small_case()
+    prep = O.prepare(W, np.zeros(W.shape[1]), "lowrank", k, r)
+    w, v = np.linalg.eigh(W.T @ W)
+    v = v[:, np.argsort(w)[::-1]]
+    span = v[:, k:k + r]
+    R0 = prep["R0"]
+    assert np.allclose(R0 @ R0.T, np.eye(r), atol=1e-12)
+    assert np.allclose(span @ span.T, R0.T @ R0, atol=1e-9)
+
+
+def test_projection_inverts_r0_gram():
+    """The L-update with R fixed: if W_res = A R0 for any full-row-rank R0 (not
+    orthonormal), then P = A exactly. A dropped (R0 R0^T)^-1 fails here."""
+    rng = _rng(4)
+    A = rng.standard_normal((10, 3))
+    R0 = rng.standard_normal((3, 14)) * 3.0
+    assert np.allclose(O.projection(A @ R0, R0), A, atol=1e-12)
+
+
+# -------------------------------------------------------------------- the online step
+
+@pytest.mark.parametrize("ridge", [0.0, 0.7])
+def test_r_is_least_squares_solution(ridge):
+    """Blog rank-r objective section: with L fixed, R minimises ||X W_res - L R||_F^2
+    (+ ridge ||R||_F^2, 2.2). Brute force: LAPACK lstsq on the stacked system."""
+    W, b, X, k, r = _small_case(seed=5)
+    prep = O.prepare(W, b, "lowrank", k, r)
+    _, inter = O.forward(X, prep, ridge=ridge, keep=True)
+    for s in range(X.shape[0]):
+        L = X[s] @ prep["P"]
+        target = X[s] @ prep["W_res"]
+        A = np.vstack([L, np.sqrt(ridge) * np.eye(r)])
+        rhs = np.vstack([target, np.zeros((r, W.shape[1]))])
+        R_ls = np.linalg.lstsq(A, rhs, rcond=None)[0]
+        assert np.allclose(inter["R"][s], R_ls, atol=1e-10)
+
+
+def test_normal_equations_hold():
+    """Residual of the R-update is orthogonal to range(L): L^T (X W_res - L R) = 0."""
+    for name in ("c1",):
+        cfg = WL.get_config(name)
+        W, b = WL.make_weights(cfg)
+        X = WL.make_inputs(cfg)
+        prep = O.prepare(W, b, cfg.kind, cfg.k, cfg.r)
+        _, inter = O.forward(X, prep, keep=True)
+        for s in range(X.shape[0]):
+            L, R = inter["L"][s], inter["R"][s]
+            e = X[s] @ prep["W_res"] - L @ R
+            scale = np.linalg.norm(L) * np.linalg.norm(X[s] @ prep["W_res"])
+            assert np.linalg.norm(L.T @ e) <= 1e-10 * scale
+
+
+def test_output_is_static_plus_bias_plus_correction():
+    """Y = X W_hat + b + L R with the bias added exactly once (W_hat taken from the factors)."""
+    W, b, X, k, r = _small_case(seed=6)
+    prep = O.prepare(W, b, "lowrank", k, r)
+    Y, inter = O.forward(X, prep, keep=True)
+    for s in range(X.shape[0]):
+        corr = inter["L"][s] @ inter["R"][s]
+        assert np.allclose(Y[s] - (X[s] @ prep["F1"]) @ prep["F2"] - corr, b[None, :], atol=1e-12)
+
+
+def test_exact_when_residual_rank_at_most_r():
+    """If rank(W_res) <= r and R0 spans its row space, L R = X W_res, so Y = X W + b."""
+    rng = _rng(7)
+    d, m, k, r = 20, 30, 4, 3
+    W = _orth(rng, d, k + r) @ np.diag(np.linspace(5, 1, k + r)) @ _orth(rng, m, k + r).T
+    b = rng.standard_normal(m)
+    X = rng.standard_normal((2, 25, d))
+    prep = O.prepare(W, b, "lowrank", k, r)
+    Y = O.forward(X, prep)
+    assert np.allclose(Y, X @ W + b, atol=1e-10)
+    # non-orthonormal R0 spanning the same rows gives the same output
+    M = rng.standard_normal((r, r)) + 3 * np.eye(r)
+    prep2 = O.prepare(W, b, "lowrank", k, r, R0=M @ prep["R0"])
+    assert np.allclose(O.forward(X, prep2), X @ W + b, atol=1e-9)
+
+
+def test_proposition1_isotropic_input():
+    """Proposition 1 (2.3, Appendix C): with X^T X = c I, one-step DyRA equals the static
+    rank-(k+r) truncated SVD and R equals R0."""
+    rng = _rng(8)
+    n, d, m, k, r = 64, 24, 40, 5, 6
+    W = rng.standard_normal((d, m)) * (np.arange(1, d + 1) ** -0.7)[:, None]
+    c = 2.5
+    X = (np.sqrt(c) * _orth(rng, n, d))[None]
+    prep = O.prepare(W, np.zeros(m), "lowrank", k, r)
+    Y, inter = O.forward(X, prep, keep=True)
+    assert np.allclose(inter["R"][0], prep["R0"], atol=1e-9)
+    assert np.allclose(Y[0], X[0] @ (_top_left_projector(W, k + r) @ W), atol=1e-9)
+
+
+def test_lr_error_above_eckart_young_bound_and_als_monotone():
+    """E.3: ALS error is bounded below by the optimal rank-r error of X W_res (SVD of the
+    residual product) and does not increase with more ALS iterations."""
+    W, _, X, k, r = _small_case(seed=9, n=50)
+    prep = O.prepare(W, np.zeros(W.shape[1]), "lowrank", k, r)
+    Xs = X[0]
+    target = Xs @ prep["W_res"]
+    lam = np.sort(np.linalg.eigvalsh(target.T @ target))[::-1]
+    bound = np.sqrt(max(lam[r:].sum(), 0.0))
+    errs = []
+    for t in (1, 1.5, 2, 3, 5, 40):
+        L, R = O.als_factors(Xs, prep["W_res"], prep["R0"], t)
+        errs.append(np.linalg.norm(target - L @ R))
+    _, inter = O.forward(X[:1], prep, keep=True)
+    assert np.isclose(np.linalg.norm(target - inter["L"][0] @ inter["R"][0]), errs[0], rtol=1e-10)
+    assert all(e >= bound * (1 - 1e-12) for e in errs)
+    assert all(errs[i + 1] <= errs[i] * (1 + 1e-12) for i in range(len(errs) - 1))
+    assert errs[-1] <= bound * (1 + 1e-3)
+
+
+def test_gauge_invariance_of_r0():
+    """Rotating or sign-flipping R0's rows leaves L R (hence Y) unchanged."""
+    rng = _rng(10)
+    W, b, X, k, r = _small_case(seed=10)
+    prep = O.prepare(W, b, "lowrank", k, r)
+    Q = _orth(rng, r, r)
+    Q[:, 0] *= -1
+    prep2 = O.prepare(W, b, "lowrank", k, r, R0=Q @ prep["R0"])
+    assert np.allclose(O.forward(X, prep), O.forward(X, prep2), atol=1e-10)
+
+
+def test_zero_sample_falls_back_to_static_branch():
+    """Degenerate case: an all-zero sample gives L = 0 and G = 0 (not SPD); its output is
+    the bias (static branch of a zero input)."""
+    W, b, X, k, r = _small_case(seed=11)
+    X = X.copy()
+    X[1] = 0.0
+    prep = O.prepare(W, b, "lowrank", k, r)
+    Y, inter = O.forward(X, prep, keep=True)
+    assert inter["ok"] == [True, False, True]
+    assert np.allclose(Y[1], b[None, :], atol=0)
+
+
+def test_rows_subset_matches_full_forward():
+    W, b, X, k, r = _small_case(seed=12)
+    prep = O.prepare(W, b, "lowrank", k, r)
+    Y = O.forward(X, prep)
+    rows = [np.array([0, 7, 39]), np.array([3]), np.array([5, 6])]
+    Ys = O.forward(X, prep, rows=rows)
+    for s in range(3):
+        assert np.allclose(Ys[s], Y[s][rows[s]], atol=1e-12)
+
+
+# -------------------------------------------------------------------- Newton-Schulz
+
+def test_newton_schulz_closed_form():
+    """With X0 = alpha I, I - G_hat X_t = (I - alpha G_hat)^(2^t) exactly, so on G_hat's
+    eigenvalues mu: x_t(mu) = (1 - (1 - alpha mu)^(2^t)) / mu."""
+    rng = _rng(13)
+    A = rng.standard_normal((40, 12)) * np.linspace(3, 0.5, 12)[None, :]
+    G = A.T @ A
+    dinv = 1 / np.sqrt(np.diag(G))
+    Gh = G * dinv[:, None] * dinv[None, :]
+    mu, V = np.linalg.eigh(Gh)
+    alpha = 1.0 / np.max(np.abs(Gh).sum(axis=1))
+    for t in (1, 2, 5, 8):
+        x = (1 - (1 - alpha * mu) ** (2 ** t)) / mu
+        expect = (V * x[None, :]) @ V.T * dinv[:, None] * dinv[None, :]
+        assert np.allclose(O.newton_schulz_inverse(G, t), expect, rtol=1e-9, atol=1e-12)
+
+
+def test_newton_schulz_converges_to_inverse():
+    rng = _rng(14)
+    A = rng.standard_normal((300, 32))
+    G = A.T @ A
+    assert np.allclose(O.newton_schulz_inverse(G, 30), np.linalg.inv(G), rtol=1e-11, atol=1e-14)
+    B = rng.standard_normal((32, 7))
+    R, ok = O.solve_right_factor(G, B, "newton_schulz", 30)
+    assert ok and np.allclose(R, np.linalg.solve(G, B), rtol=1e-10, atol=1e-12)
+
+
+# -------------------------------------------------------------------- metric and workloads
+
+def test_approximation_error_metric():
+    rng = _rng(15)
+    X = rng.standard_normal((2, 5, 4))
+    W = rng.standard_normal((4, 3))
+    b = rng.standard_normal(3)
+    assert O.approximation_error(X @ W + b, X, W, b) < 1e-15
+    assert np.isclose(O.approximation_error(b + 0 * (X @ W), X, W, b), 1.0)
+
+
+def test_c1_dyra_beats_static_truncation():
+    """c1 end to end: the correction lowers the output error below the static rank-k fit,
+    and Proposition 1's comparison point (static rank k+r) is beaten on anisotropic X."""
+    cfg = WL.get_config("c1")
+    W, b = WL.make_weights(cfg)
+    X = WL.make_inputs(cfg)
+    prep = O.prepare(W, b, cfg.kind, cfg.k, cfg.r)
+    Y = O.forward(X, prep)
+    e_dyra = O.approximation_error(Y, X, W, b)
+    e_static = O.approximation_error(X @ prep["W_hat"] + b, X, W, b)
+    U2, V2 = O.tsvd_factors(W, cfg.k + cfg.r)
+    e_static_kr = O.approximation_error(X @ (U2 @ V2) + b, X, W, b)
+    assert e_dyra < e_static_kr < e_static

@@ -1,0 +1,205 @@
+/*
+ * dyra.h -- C ABI of the B300 (sm_103a) DyRA linear layer.
+ *
+ * The layer approximates Y = X W + b by
+ *
+ *     Y ~= X W_hat + b + L R,        L = X P,   R = (L^T L + lambda I)^-1 (L^T X) W_res
+ *
+ * W_hat is a static structured approximation of W (truncated-SVD low rank U V, or
+ * Monarch), W_res = W - W_hat, P = W_res R0^T (R0 R0^T)^-1 is fixed offline, and R is
+ * recomputed for every sample by one alternating-least-squares step.
+ *
+ * Sources: "DyRA: Dynamic Residual Approximation for Efficient Matrix Multiplication in
+ * DNNs" -- section-by-section summary page: 2.2 (dynamic residual approximation, ridge),
+ * 2.3 (one-step ALS, Proposition 1, cost), 2.4 (fused kernels, Cholesky for small r and
+ * Newton-Schulz for larger r), Appendix B (truncated SVD, Monarch); and the blog digest
+ * "DyRA：用输入相关的残差修正加速大模型的矩阵乘法": residual-split equations
+ * (W = W_hat + W_res, XW = X W_hat + X W_res), the rank-r objective
+ * min ||X W_res - L R||_F^2 with the ALS order of operations, the one-step form
+ * XW ~ X W_hat + L(1) R(1), and the offline / online flow (R0 = top right singular vectors
+ * of W_res, prepared once).
+ *
+ * Conventions for every call:
+ *   - All matrices are row-major. X is [batch, n, d], Y is [batch, n, m].
+ *   - "host" pointers are ordinary CPU memory; "device" pointers are CUDA global memory
+ *     of the layer's device. The library never takes ownership of a caller pointer.
+ *   - A call that returns an error status has launched nothing and changed no caller
+ *     buffer, except where stated. Nothing prints, exits or traps.
+ *   - Every forward call is asynchronous on the caller's stream and allocates nothing.
+ */
+#ifndef DYRA_H_
+#define DYRA_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DYRA_ABI_VERSION 1
+
+typedef enum dyra_status {
+  DYRA_OK = 0,
+  DYRA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shapes            */
+  DYRA_ERR_UNSUPPORTED = 2,   /* valid request that this build does not implement       */
+  DYRA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (see dyra_last_error) */
+  DYRA_ERR_OOM = 4,           /* device or host allocation failed in dyra_prepare       */
+  DYRA_ERR_NOT_SPD = 5,       /* reported by dyra_workspace_status: some L^T L + lambda I
+                                 was not positive definite                               */
+  DYRA_ERR_TIMEOUT = 6,       /* a bounded in-kernel wait gave up (kernel returned early) */
+  DYRA_ERR_WORKSPACE = 7,     /* workspace too small or misaligned                      */
+  DYRA_ERR_NO_DEVICE = 8      /* no usable sm_103 device                                */
+} dyra_status;
+
+typedef enum dyra_static_kind {
+  DYRA_STATIC_LOWRANK = 0,    /* W_hat = U V, U: d x k, V: k x m (truncated SVD)        */
+  DYRA_STATIC_MONARCH = 1     /* W_hat = blockdiag(B1) . stride permutation . blockdiag(B2) */
+} dyra_static_kind;
+
+typedef enum dyra_dtype {
+  DYRA_F32 = 0,               /* X, Y, factors fp32; fp32 SIMT kernels                  */
+  DYRA_BF16 = 1               /* X, Y, factors bf16; fp32 accumulation on tcgen05        */
+} dyra_dtype;
+
+typedef enum dyra_solver {
+  DYRA_SOLVE_AUTO = 0,        /* Cholesky if r <= 64, else Newton-Schulz                 */
+  DYRA_SOLVE_CHOLESKY = 1,
+  DYRA_SOLVE_NEWTON_SCHULZ = 2
+} dyra_solver;
+
+/* Arguments of dyra_prepare / dyra_fit. All pointers are HOST pointers to float64, read
+ * only during the call. Zero-initialise the struct and set what you need. */
+typedef struct dyra_prepare_args {
+  const double *W;      /* [d, m] dense weight (required)                                 */
+  const double *b;      /* [m] bias, or NULL for zero bias                                */
+  int d, m;             /* input / output features                                        */
+  dyra_static_kind kind;
+  int k;                /* LOWRANK: static rank, 0 <= k < min(d, m).
+                           MONARCH: block count nb, d % nb == 0 and m % nb == 0
+                           (W_hat[(a,i),(c,j)] = B1[a][i,c] B2[c][a,j])                  */
+  int r;                /* residual rank, 1 <= r <= 256 (bf16) / 1 <= r <= 64 (f32)      */
+  const double *R0;     /* [r, m] fixed initial right factor, full row rank, or NULL for
+                           the top-r right singular vectors of W_res                     */
+  const double *F1;     /* optional static factors (both or neither):                     */
+  const double *F2;     /*   LOWRANK: F1 = U [d, k], F2 = V [k, m]
+                             MONARCH: F1 = B1 [nb, d/nb, nb], F2 = B2 [nb, nb, m/nb]
+                           NULL: fitted here (truncated SVD / blockwise rank-1 SVD)       */
+  double ridge;         /* lambda >= 0 added to the diagonal of L^T L (absolute)          */
+  dyra_solver solver;
+  int ns_iters;         /* Newton-Schulz iterations (0 => 8)                             */
+  dyra_dtype dtype;
+  int device;           /* CUDA device ordinal the layer lives on                        */
+  int fit_threads;      /* host threads for the fit, 0 => hardware concurrency           */
+} dyra_prepare_args;
+
+/* Read-only description of a prepared layer. */
+typedef struct dyra_layer_desc {
+  int d, m, k, r;
+  dyra_static_kind kind;
+  dyra_dtype dtype;
+  dyra_solver solver;   /* resolved (never AUTO)                                          */
+  int ns_iters;
+  double ridge;
+  int device;
+  int kernels_per_forward; /* kernel launches one dyra_linear_forward enqueues           */
+} dyra_layer_desc;
+
+typedef struct dyra_layer dyra_layer;   /* opaque; owns its device copies of the factors */
+
+/* Offline preparation (synchronous, not meant for the timed path): static fit of W (unless
+ * F1/F2 are given), W_res = W - W_hat, R0 (unless given), P = W_res R0^T (R0 R0^T)^-1, and
+ * upload of the factors in the layer's dtype to `device`. On success *out owns the layer;
+ * free it with dyra_layer_destroy. Errors: INVALID_ARG (shapes, null W, r out of range,
+ * R0 rank deficient), UNSUPPORTED (a shape the kernels do not take), NO_DEVICE, OOM, CUDA. */
+dyra_status dyra_prepare(const dyra_prepare_args *args, dyra_layer **out);
+
+/* The offline step alone, on the host (no device needed): the static fit (unless F1/F2
+ * are given), W_res, R0 (unless given) and P, in float64, written to caller-owned host
+ * buffers (any may be NULL; sizes as in dyra_export / dyra_export_factors). dtype, solver
+ * and device are not used. Lets a CPU machine prepare factors that dyra_prepare later
+ * uploads through F1/F2/R0. Errors: INVALID_ARG, OOM. */
+dyra_status dyra_fit(const dyra_prepare_args *args, double *W_hat, double *W_res, double *P,
+                     double *R0, double *F1, double *F2);
+
+void dyra_layer_destroy(dyra_layer *layer);
+
+dyra_status dyra_layer_info(const dyra_layer *layer, dyra_layer_desc *out);
+
+/* Host float64 copies of what dyra_prepare computed (before rounding to the device dtype).
+ * Any pointer may be NULL. Sizes: W_hat, W_res [d, m]; P [d, r]; R0 [r, m];
+ * F1/F2 as in dyra_prepare_args. */
+dyra_status dyra_export(const dyra_layer *layer, double *W_hat, double *W_res, double *P,
+                        double *R0);
+dyra_status dyra_export_factors(const dyra_layer *layer, double *F1, double *F2);
+
+/* Bytes of device workspace dyra_linear_forward needs for (batch, n). */
+dyra_status dyra_workspace_size(const dyra_layer *layer, int batch, int n, size_t *bytes);
+
+/* The online step. X: device [batch, n, d], Y: device [batch, n, m], both in the layer's
+ * dtype, 16-byte aligned, rows densely packed. workspace: device, >= dyra_workspace_size
+ * bytes, 256-byte aligned, owned by the caller; it must not be shared by two forwards that
+ * may run at the same time. Enqueues every kernel on `stream` (the bf16 path also forks
+ * the SPD solve onto an internal stream of the layer and joins it back before the output
+ * kernel) and returns without waiting. batch == 0 or n == 0 is a no-op. A sample whose
+ * L^T L + lambda I is not positive definite (e.g. an all-zero sample with lambda = 0) gets
+ * R = 0 -- its rows of Y are the static branch plus b -- and is counted in the status word
+ * that dyra_workspace_status reads. Errors (nothing launched): INVALID_ARG, WORKSPACE, CUDA. */
+dyra_status dyra_linear_forward(const dyra_layer *layer, const void *X, int batch, int n,
+                                void *Y, void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+/* Same step from HOST buffers: copies X_host -> X_dev, runs the forward, copies Y_dev ->
+ * Y_host, all enqueued on `stream` (use page-locked host memory for asynchronous copies;
+ * synchronise the stream before reading Y_host). X_dev / Y_dev are device staging buffers
+ * owned by the caller. */
+dyra_status dyra_linear_forward_host(const dyra_layer *layer, const void *X_host, int batch,
+                                     int n, void *Y_host, void *X_dev, void *Y_dev,
+                                     void *workspace, size_t workspace_bytes,
+                                     cudaStream_t stream);
+
+/* Forward that also records `events[i]` before kernel i and events[count] after the last
+ * one (count = kernels_per_forward, so max_events >= count + 1), to time each kernel. Every
+ * kernel runs on `stream` here (no fork), so consecutive events bracket one kernel.
+ * *recorded receives count + 1. */
+dyra_status dyra_linear_forward_profiled(const dyra_layer *layer, const void *X, int batch,
+                                         int n, void *Y, void *workspace,
+                                         size_t workspace_bytes, cudaStream_t stream,
+                                         cudaEvent_t *events, int max_events, int *recorded);
+
+/* Name of kernel `i` of the forward (static string), or NULL. */
+const char *dyra_kernel_name(const dyra_layer *layer, int i);
+
+/* Synchronises `stream`, then reads the status word the last forward on `workspace` left:
+ * *not_spd_samples = samples that fell back to the static branch, *timeouts = bounded
+ * in-kernel waits that gave up. Returns DYRA_ERR_TIMEOUT if *timeouts > 0, else
+ * DYRA_ERR_NOT_SPD if *not_spd_samples > 0, else DYRA_OK. */
+dyra_status dyra_workspace_status(const dyra_layer *layer, const void *workspace,
+                                  cudaStream_t stream, int *not_spd_samples, int *timeouts);
+
+/* Intermediates a forward leaves in its workspace, for tests that check each kernel. */
+typedef enum dyra_buffer {
+  DYRA_BUF_T = 0,      /* [batch, n, ld]. bf16 path: [X F1 | L (L^T L + lambda I)^-1] after
+                          the forward (the L columns are rewritten in place); f32 path:
+                          [X U | L]                                                         */
+  DYRA_BUF_C = 1,      /* C = L^T X, [batch, r, d] (bf16 / fp32)                           */
+  DYRA_BUF_G = 2,      /* L^T L without lambda, [batch, r, r] (fp32 / fp64)                */
+  DYRA_BUF_GINV = 3,   /* (L^T L + lambda I)^-1, [batch, r, r] (bf16 / fp64)               */
+  DYRA_BUF_B = 4,      /* B = C W_res: bf16 path B^T [batch, m, r]; f32 path B [batch, r, m] */
+  DYRA_BUF_R = 5       /* f32 path only: R = G^-1 B, [batch, r, m] fp32                    */
+} dyra_buffer;
+
+/* Byte offset of intermediate `which` inside the workspace for (batch, n) and its row
+ * stride in elements. Returns UNSUPPORTED for a buffer the layer's path does not have. */
+dyra_status dyra_workspace_tensor(const dyra_layer *layer, int batch, int n, int which,
+                                  size_t *offset_bytes, int *ld);
+
+const char *dyra_status_string(dyra_status status);
+/* Text of the last CUDA/driver error seen by this thread inside the library ("" if none). */
+const char *dyra_last_error(void);
+int dyra_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DYRA_H_ */

@@ -1,0 +1,1076 @@
+// C ABI of the DyRA linear layer (include/dyra.h): offline preparation and the online
+// forward, which enqueues the CUDA kernels of this library on the caller's stream.
+//
+// bf16 low-rank forward, per sample s (every contraction on tcgen05 through tc_gemm):
+//   1. T = X [U | P]                     -> [X U | L]                 (static branch, L = X P)
+//   2. [C^T ; G] = [X | L]^T L           -> C = L^T X, G = L^T L      (one pass over X's tokens)
+//   then two independent branches, the second on the layer's auxiliary stream:
+//   3. B = C W_res                       -> B^T                      (main stream)
+//   4. G^-1 = (G + lambda I)^-1          (Cholesky for r <= 64, Newton-Schulz otherwise)
+//   5. L~ = L G^-1                       written over the L columns of T
+//   6. Y = [X U | L~] [V ; B] + b        (joins the two branches)
+// Since L R = L (G^-1 B) = (L G^-1) B, step 6 produces X W_hat + b + L R of the one-step
+// ALS update without materialising R, and the SPD solve runs beside the B = C W_res GEMM
+// instead of between the GEMMs.
+#include "../../include/dyra.h"
+#include "fit.h"
+#include "kernels.cuh"
+#include "monarch.cuh"
+#include "tc_gemm.cuh"
+
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <array>
+#include <cmath>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+struct dyra_layer {
+  int d = 0, m = 0, k = 0, r = 0, kp = 0;
+  dyra_static_kind kind = DYRA_STATIC_LOWRANK;
+  dyra_dtype dtype = DYRA_BF16;
+  dyra_solver solver = DYRA_SOLVE_CHOLESKY;
+  int ns_iters = 8;
+  double ridge = 0.0;
+  int device = 0;
+  std::vector<double> W_hat, W_res, P, R0, F1, F2, bias;
+  // device copies; bf16: w1 = [U^T (padded to kp rows); P^T] [kp + r, d], v = V^T [m, kp],
+  // wres = W_res^T [m, d]; f32: w1 = [U | P] [d, k + r], v = V [k, m], wres = W_res [d, m]
+  void *w1 = nullptr, *v = nullptr, *wres = nullptr;
+  float *bias_d = nullptr;
+  cudaStream_t aux = nullptr;            // stream of the SPD-solve branch
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  mutable std::mutex mu;                 // plan cache and fork/join events
+  mutable std::vector<std::pair<std::array<uintptr_t, 5>, std::shared_ptr<void>>> plans;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dyra_status cuda_fail(cudaError_t e, const char *where) {
+  g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
+  return DYRA_ERR_CUDA;
+}
+
+#define DY_CUDA(call)                                   \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline int roundup(int x, int q) { return (x + q - 1) / q * q; }
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+// ------------------------------------------------------------------------ workspace
+
+struct WsLayout {
+  size_t T = 0, C = 0, G = 0, Ginv = 0, Gh = 0, X0 = 0, X1 = 0, Pt = 0, dinv = 0, flags = 0,
+         B = 0, R = 0, total = 0;
+  int ldT = 0;
+};
+
+WsLayout layout_of(const dyra_layer *L, int batch, int n) {
+  WsLayout w;
+  size_t off = 256;   // status words: [0] not-SPD samples, [1] bounded waits that gave up
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  const size_t B = (size_t)batch, N = (size_t)n, d = L->d, m = L->m, r = L->r;
+  if (L->dtype == DYRA_BF16) {
+    w.ldT = L->kp + L->r;
+    w.T = take(B * N * (size_t)w.ldT * 2);
+    w.C = take(B * r * d * 2);
+    w.G = take(B * r * r * 4);
+    w.Ginv = take(B * r * r * 2);
+    if (L->solver == DYRA_SOLVE_NEWTON_SCHULZ) {
+      w.Gh = take(B * r * r * 4);
+      w.X0 = take(B * r * r * 4);
+      w.X1 = take(B * r * r * 4);
+      w.Pt = take(B * r * r * 4);
+      w.dinv = take(B * r * 4);
+      w.flags = take(B * 4);
+    }
+    w.B = take(B * m * r * 2);
+  } else {
+    w.ldT = L->k + L->r;
+    w.T = take(B * N * (size_t)w.ldT * 4);
+    w.G = take(B * r * r * 8);
+    w.Ginv = take(B * r * r * 8);
+    w.C = take(B * r * d * 4);
+    w.B = take(B * r * m * 4);
+    w.R = take(B * r * m * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+// ------------------------------------------------------------------------ launch plans
+//
+// A plan is the list of launches of one forward for a fixed (X, Y, workspace, batch, n):
+// tensor maps and kernel parameters are encoded once and reused by later calls with the
+// same buffers, so a steady-state forward costs only its launches on the host.
+
+struct Step {
+  enum Kind { GEMM, CHOL, NS_PREP, NS_FINISH, FORK, JOIN } kind = GEMM;
+  bool aux = false;   // runs on the auxiliary stream
+  dyra::TcGemmParams p;
+  CUtensorMap a0, a1, b0, b1, out;
+  const float *G = nullptr;
+  float *Gh = nullptr, *X0 = nullptr, *dinv = nullptr;
+  const float *Xf = nullptr;
+  int *flags = nullptr;
+  __nv_bfloat16 *Ginv = nullptr;
+  int *status = nullptr;
+  int batch = 0, r = 0;
+  float ridge = 0.f;
+};
+
+struct Plan {
+  std::vector<Step> steps;
+};
+
+struct Recorder {
+  cudaEvent_t *ev = nullptr;
+  int max = 0, count = 0;
+  void mark(cudaStream_t s) {
+    if (ev && count < max) cudaEventRecord(ev[count], s);
+    ++count;
+  }
+};
+
+bool make_map(CUtensorMap *map, const void *base, int eb, long long inner, long long rows,
+              long long batch, long long row_stride_el, long long batch_stride_el, int box_rows) {
+  dyra::TcOperand op{base, eb, inner, rows, batch, row_stride_el * eb, batch_stride_el * eb};
+  return dyra::tc_make_map(map, op, box_rows);
+}
+
+bool make_store_map(CUtensorMap *map, const void *base, long long inner, long long rows,
+                    long long batch, long long row_stride_el, long long batch_stride_el) {
+  dyra::TcOperand op{base, 2, inner, rows, batch, row_stride_el * 2, batch_stride_el * 2};
+  return dyra::tc_make_store_map(map, op);
+}
+
+dyra::TcGemmParams base_params() {
+  dyra::TcGemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.rb = 1 << 30;
+  p.alpha = 1.f;
+  return p;
+}
+
+Step gemm_step(const dyra::TcGemmParams &p, const CUtensorMap &a0, const CUtensorMap &a1,
+               const CUtensorMap &b0, const CUtensorMap &b1, bool aux = false) {
+  Step st;
+  st.kind = Step::GEMM;
+  st.aux = aux;
+  st.p = p;
+  st.a0 = a0;
+  st.a1 = a1;
+  st.b0 = b0;
+  st.b1 = b1;
+  st.out = a0;
+  return st;
+}
+
+#define DY_MAP(expr)                                               \
+  do {                                                             \
+    if (!(expr)) {                                                 \
+      g_last_error = "cuTensorMapEncodeTiled failed: " #expr;      \
+      return DYRA_ERR_CUDA;                                        \
+    }                                                              \
+  } while (0)
+
+// ------------------------------------------------------------------------ bf16 low-rank path
+
+dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int n, void *Y,
+                              uint8_t *ws, const WsLayout &w, Plan &plan) {
+  using namespace dyra;
+  const int d = L->d, m = L->m, r = L->r, kp = L->kp, ldT = w.ldT;
+  int *status = reinterpret_cast<int *>(ws);
+  __nv_bfloat16 *T = reinterpret_cast<__nv_bfloat16 *>(ws + w.T);
+  __nv_bfloat16 *C = reinterpret_cast<__nv_bfloat16 *>(ws + w.C);
+  float *G = reinterpret_cast<float *>(ws + w.G);
+  __nv_bfloat16 *Ginv = reinterpret_cast<__nv_bfloat16 *>(ws + w.Ginv);
+  __nv_bfloat16 *Bt = reinterpret_cast<__nv_bfloat16 *>(ws + w.B);
+
+  // 1. T = X [U | P]
+  {
+    CUtensorMap a, b, o;
+    const int N = ldT;
+    const int nt = (int)cdiv(N, 256);
+    const int BN = roundup((int)cdiv(N, nt), 32);
+    DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
+    DY_MAP(make_map(&b, L->w1, 2, d, N, 1, d, 0, BN));
+    DY_MAP(make_store_map(&o, T, N, n, batch, ldT, (long long)n * ldT));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(n, 128);
+    p.n_tiles = nt;
+    p.batch = batch;
+    p.BN = BN;
+    p.k_chunks = (int)cdiv(d, 64);
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.a_batched0 = 1;
+    p.b_split = p.k_chunks;
+    p.idesc = tc_idesc(2, 0, 0, BN);
+    p.epi = EPI_ROW_BF16;
+    p.tma_store = 1;
+    p.out_batched = 1;
+    p.rows_valid = n;
+    p.cols_valid = N;
+    p.timeouts = status + 1;
+    Step st = gemm_step(p, a, a, b, b);
+    st.out = o;
+    plan.steps.push_back(st);
+  }
+  // 2. [C^T ; G] = [X | L]^T L   (both operands MN-major: the reduction runs over tokens)
+  {
+    CUtensorMap ax, al;
+    DY_MAP(make_map(&ax, X, 2, d, n, batch, d, (long long)n * d, 64));
+    DY_MAP(make_map(&al, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 64));
+    TcGemmParams p = base_params();
+    p.a_split = (int)cdiv(d, 128);
+    p.m_tiles = p.a_split + (int)cdiv(r, 128);
+    p.n_tiles = 1;
+    p.batch = batch;
+    p.BN = roundup(r, 64);
+    p.k_chunks = (int)cdiv(n, 64);
+    p.elem_bytes = 2;
+    p.a_major = 1;
+    p.b_major = 1;
+    p.a_batched0 = p.a_batched1 = 1;
+    p.b_split = p.k_chunks;
+    p.b_batched0 = 1;
+    p.idesc = tc_idesc(2, 1, 1, p.BN);
+    p.epi = EPI_CG;
+    p.out = C;                       // C [batch, r, d] from the C^T rows
+    p.out_bstride = (long long)r * d;
+    p.out_ld = d;
+    p.rows_valid = d;
+    p.cols_valid = r;
+    p.out2 = G;
+    p.out2_bstride = (long long)r * r;
+    p.out2_ld = r;
+    p.rows2_valid = r;
+    p.cols2_valid = r;
+    p.timeouts = status + 1;
+    plan.steps.push_back(gemm_step(p, ax, al, al, al));
+  }
+  {
+    Step f;
+    f.kind = Step::FORK;
+    plan.steps.push_back(f);
+  }
+  // 4. G^-1 (auxiliary stream)
+  if (L->solver == DYRA_SOLVE_CHOLESKY) {
+    Step st;
+    st.kind = Step::CHOL;
+    st.aux = true;
+    st.G = G;
+    st.batch = batch;
+    st.r = r;
+    st.ridge = (float)L->ridge;
+    st.Ginv = Ginv;
+    st.status = status;
+    plan.steps.push_back(st);
+  } else {
+    float *Gh = reinterpret_cast<float *>(ws + w.Gh);
+    float *Xa = reinterpret_cast<float *>(ws + w.X0);
+    float *Xb = reinterpret_cast<float *>(ws + w.X1);
+    float *Pt = reinterpret_cast<float *>(ws + w.Pt);
+    float *dinv = reinterpret_cast<float *>(ws + w.dinv);
+    int *flags = reinterpret_cast<int *>(ws + w.flags);
+    {
+      Step st;
+      st.kind = Step::NS_PREP;
+      st.aux = true;
+      st.G = G;
+      st.batch = batch;
+      st.r = r;
+      st.ridge = (float)L->ridge;
+      st.Gh = Gh;
+      st.X0 = Xa;
+      st.dinv = dinv;
+      st.flags = flags;
+      plan.steps.push_back(st);
+    }
+    // Both GEMMs of an iteration read K-major operands only. X_t stays symmetric (a
+    // polynomial in G_hat), so its rows serve as the columns of the B operand of
+    // P = G_hat X_t; P is stored transposed so X_{t+1} = 2 X_t - X_t P reads it K-major too.
+    const int BN = roundup(r, 16);
+    for (int it = 0; it < L->ns_iters; ++it) {
+      CUtensorMap a, b;
+      DY_MAP(make_map(&a, Gh, 4, r, r, batch, r, (long long)r * r, 128));
+      DY_MAP(make_map(&b, Xa, 4, r, r, batch, r, (long long)r * r, BN));
+      TcGemmParams p = base_params();
+      p.m_tiles = (int)cdiv(r, 128);
+      p.n_tiles = 1;
+      p.batch = batch;
+      p.BN = BN;
+      p.k_chunks = (int)cdiv(r, 32);
+      p.elem_bytes = 4;
+      p.a_split = p.m_tiles;
+      p.a_batched0 = 1;
+      p.b_split = p.k_chunks;
+      p.b_batched0 = 1;
+      p.idesc = tc_idesc(4, 0, 0, BN);
+      p.epi = EPI_TRANS_F32;
+      p.out = Pt;
+      p.out_bstride = (long long)r * r;
+      p.rb = r;
+      p.out_gstride = 0;
+      p.out_ld = r;
+      p.rows_valid = r;
+      p.cols_valid = r;
+      p.timeouts = status + 1;
+      plan.steps.push_back(gemm_step(p, a, a, b, b, true));   // P^T = (G_hat X)^T
+      DY_MAP(make_map(&a, Xa, 4, r, r, batch, r, (long long)r * r, 128));
+      DY_MAP(make_map(&b, Pt, 4, r, r, batch, r, (long long)r * r, BN));
+      p.epi = EPI_ROW_F32;
+      p.out = Xb;
+      p.out_bstride = (long long)r * r;
+      p.out_ld = r;
+      p.aux = Xa;
+      p.aux_bstride = (long long)r * r;
+      p.aux_ld = r;
+      p.alpha = -1.f;
+      p.beta = 2.f;
+      plan.steps.push_back(gemm_step(p, a, a, b, b, true));   // X' = 2X - X P
+      std::swap(Xa, Xb);
+    }
+    Step st;
+    st.kind = Step::NS_FINISH;
+    st.aux = true;
+    st.Xf = Xa;
+    st.dinv = dinv;
+    st.batch = batch;
+    st.r = r;
+    st.flags = flags;
+    st.Ginv = Ginv;
+    st.status = status;
+    plan.steps.push_back(st);
+  }
+  // 5. L~ = L G^-1, in place over the L columns of T (auxiliary stream)
+  {
+    CUtensorMap a, b, o;
+    const int BN = roundup(r, 16);
+    DY_MAP(make_map(&a, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 128));
+    DY_MAP(make_map(&b, Ginv, 2, r, r, batch, r, (long long)r * r, BN));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(n, 128);
+    p.n_tiles = 1;
+    p.batch = batch;
+    p.BN = BN;
+    p.k_chunks = (int)cdiv(r, 64);
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.a_batched0 = 1;
+    p.b_split = p.k_chunks;
+    p.b_batched0 = 1;
+    p.idesc = tc_idesc(2, 0, 0, BN);
+    p.epi = EPI_ROW_BF16;
+    p.rows_valid = n;
+    p.cols_valid = r;
+    p.timeouts = status + 1;
+    if (BN % 32 == 0) {
+      DY_MAP(make_store_map(&o, T + kp, r, n, batch, ldT, (long long)n * ldT));
+      p.tma_store = 1;
+      p.out_batched = 1;
+    } else {
+      o = a;
+      p.out = T + kp;
+      p.out_bstride = (long long)n * ldT;
+      p.out_ld = ldT;
+    }
+    Step st = gemm_step(p, a, a, b, b, true);
+    st.out = o;
+    plan.steps.push_back(st);
+  }
+  // 3. B = C W_res, written as B^T [batch, m, r] (main stream, beside the solve)
+  {
+    CUtensorMap a, b;
+    const int BN = 256;
+    DY_MAP(make_map(&a, C, 2, d, (long long)batch * r, 1, d, 0, 128));
+    DY_MAP(make_map(&b, L->wres, 2, d, m, 1, d, 0, BN));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv((long long)batch * r, 128);
+    p.n_tiles = (int)cdiv(m, BN);
+    p.batch = 1;
+    p.BN = BN;
+    p.k_chunks = (int)cdiv(d, 64);
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.b_split = p.k_chunks;
+    p.idesc = tc_idesc(2, 0, 0, BN);
+    p.epi = EPI_TRANS_BF16;
+    p.out = Bt;
+    p.out_bstride = 0;
+    p.rb = r;
+    p.out_gstride = (long long)m * r;
+    p.out_ld = r;
+    p.rows_valid = batch * r;
+    p.cols_valid = m;
+    p.timeouts = status + 1;
+    plan.steps.push_back(gemm_step(p, a, a, b, b));
+  }
+  {
+    Step j;
+    j.kind = Step::JOIN;
+    plan.steps.push_back(j);
+  }
+  // 6. Y = [X U | L~] [V ; B] + b
+  {
+    CUtensorMap a, b0, b1, o;
+    const int BN = 256;
+    DY_MAP(make_map(&a, T, 2, ldT, n, batch, ldT, (long long)n * ldT, 128));
+    DY_MAP(make_map(&b1, Bt, 2, r, m, batch, r, (long long)m * r, BN));
+    if (kp > 0)
+      DY_MAP(make_map(&b0, L->v, 2, kp, m, 1, kp, 0, BN));
+    else
+      b0 = b1;
+    DY_MAP(make_store_map(&o, Y, m, n, batch, m, (long long)n * m));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(n, 128);
+    p.n_tiles = (int)cdiv(m, BN);
+    p.batch = batch;
+    p.BN = BN;
+    p.b_split = kp / 64;
+    p.k_chunks = p.b_split + (int)cdiv(r, 64);
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.a_batched0 = 1;
+    p.b_batched0 = 0;
+    p.b_batched1 = 1;
+    p.idesc = tc_idesc(2, 0, 0, BN);
+    p.epi = EPI_ROW_BF16;
+    p.tma_store = 1;
+    p.out_batched = 1;
+    p.rows_valid = n;
+    p.cols_valid = m;
+    p.bias = L->bias_d;
+    p.timeouts = status + 1;
+    Step st = gemm_step(p, a, a, b0, b1);
+    st.out = o;
+    plan.steps.push_back(st);
+  }
+  return DYRA_OK;
+}
+
+// With events (profiled) every step runs on `s`, so consecutive events bracket one kernel.
+dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream_t s,
+                     Recorder &rec) {
+  using namespace dyra;
+  const bool fork = rec.ev == nullptr && L->aux != nullptr;
+  DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
+  for (const Step &st : plan.steps) {
+    if (st.kind == Step::FORK) {
+      if (fork) {
+        DY_CUDA(cudaEventRecord(L->ev_fork, s));
+        DY_CUDA(cudaStreamWaitEvent(L->aux, L->ev_fork, 0));
+      }
+      continue;
+    }
+    if (st.kind == Step::JOIN) {
+      if (fork) {
+        DY_CUDA(cudaEventRecord(L->ev_join, L->aux));
+        DY_CUDA(cudaStreamWaitEvent(s, L->ev_join, 0));
+      }
+      continue;
+    }
+    cudaStream_t ks = (fork && st.aux) ? L->aux : s;
+    rec.mark(ks);
+    switch (st.kind) {
+      case Step::GEMM:
+        DY_CUDA(tc_gemm_launch(st.p, st.a0, st.a1, st.b0, st.b1, st.out, ks));
+        break;
+      case Step::CHOL:
+        DY_CUDA(launch_chol_inverse(st.G, st.batch, st.r, st.ridge, st.Ginv, st.status, ks));
+        break;
+      case Step::NS_PREP:
+        DY_CUDA(launch_ns_prep(st.G, st.batch, st.r, st.ridge, st.Gh, st.X0, st.dinv, st.flags, ks));
+        break;
+      case Step::NS_FINISH:
+        DY_CUDA(launch_ns_finish(st.Xf, st.dinv, st.batch, st.r, st.flags, st.Ginv, st.status, ks));
+        break;
+      default:
+        break;
+    }
+  }
+  rec.mark(s);
+  return DYRA_OK;
+}
+
+// ------------------------------------------------------------------------ fp32 path
+
+dyra_status forward_f32(const dyra_layer *L, const float *X, int batch, int n, float *Y,
+                        uint8_t *ws, const WsLayout &w, cudaStream_t s, Recorder &rec) {
+  using namespace dyra;
+  const int d = L->d, m = L->m, k = L->k, r = L->r, ldT = w.ldT;
+  int *status = reinterpret_cast<int *>(ws);
+  float *T = reinterpret_cast<float *>(ws + w.T);
+  double *G = reinterpret_cast<double *>(ws + w.G);
+  double *Gi = reinterpret_cast<double *>(ws + w.Ginv);
+  float *C = reinterpret_cast<float *>(ws + w.C);
+  float *Bm = reinterpret_cast<float *>(ws + w.B);
+  float *R = reinterpret_cast<float *>(ws + w.R);
+  const float *Wcat = static_cast<const float *>(L->w1);
+  const float *V = static_cast<const float *>(L->v);
+  const float *Wr = static_cast<const float *>(L->wres);
+  const long long nT = (long long)n * ldT;
+  DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
+  rec.mark(s);   // T = X [U | P]
+  DY_CUDA(launch_sgemm(batch, n, ldT, d, X, (long long)n * d, d, 1, Wcat, 0, ldT, 1, T, nT, ldT, 1,
+                       false, nullptr, s));
+  rec.mark(s);   // G = L^T L (fp64)
+  DY_CUDA(launch_gram_f64(T, batch, n, ldT, k, r, nT, G, s));
+  rec.mark(s);   // C = L^T X
+  DY_CUDA(launch_sgemm(batch, r, d, n, T + k, nT, 1, ldT, X, (long long)n * d, d, 1, C,
+                       (long long)r * d, d, 1, false, nullptr, s));
+  rec.mark(s);   // B = C W_res
+  DY_CUDA(launch_sgemm(batch, r, m, d, C, (long long)r * d, d, 1, Wr, 0, m, 1, Bm, (long long)r * m,
+                       m, 1, false, nullptr, s));
+  rec.mark(s);   // (G + lambda I)^-1
+  DY_CUDA(launch_inverse_f64(G, batch, r, L->ridge, L->solver == DYRA_SOLVE_NEWTON_SCHULZ,
+                             L->ns_iters, Gi, status, s));
+  rec.mark(s);   // R = G^-1 B
+  DY_CUDA(launch_apply_inverse(Gi, Bm, batch, r, m, R, s));
+  rec.mark(s);   // Y = (X U) V + b
+  DY_CUDA(launch_sgemm(batch, n, m, k, T, nT, ldT, 1, V, 0, m, 1, Y, (long long)n * m, m, 1, false,
+                       L->bias_d, s));
+  rec.mark(s);   // Y += L R
+  DY_CUDA(launch_sgemm(batch, n, m, r, T + k, nT, ldT, 1, R, (long long)r * m, m, 1, Y,
+                       (long long)n * m, m, 1, true, nullptr, s));
+  rec.mark(s);
+  return DYRA_OK;
+}
+
+const char *const kNamesBf16[] = {"xproj_static_L", "cg_c_gram", "chol_inverse", "lsolve_apply",
+                                  "residual_product", "fused_output"};
+const char *const kNamesF32[] = {"f32_xproj", "f32_gram_f64", "f32_c", "f32_b",
+                                 "f32_inverse_f64", "f32_apply_inverse", "f32_static_out",
+                                 "f32_correction_out"};
+
+int kernels_per_forward(const dyra_layer *L) {
+  if (L->dtype == DYRA_F32) return 8;
+  if (L->solver == DYRA_SOLVE_CHOLESKY) return 6;
+  return 7 + 2 * L->ns_iters;
+}
+
+const char *kernel_name(const dyra_layer *L, int i) {
+  if (i < 0 || i >= kernels_per_forward(L)) return nullptr;
+  if (L->dtype == DYRA_F32) return kNamesF32[i];
+  if (L->solver == DYRA_SOLVE_CHOLESKY) return kNamesBf16[i];
+  const int it2 = 2 * L->ns_iters;
+  if (i < 2) return kNamesBf16[i];
+  if (i == 2) return "ns_prep";
+  if (i < 3 + it2) return ((i - 3) % 2 == 0) ? "ns_gemm_gx" : "ns_gemm_update";
+  if (i == 3 + it2) return "ns_finish";
+  return kNamesBf16[i - it2 - 1];   // lsolve_apply, residual_product, fused_output
+}
+
+dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, void *Y,
+                         void *workspace, size_t ws_bytes, cudaStream_t s, Recorder &rec) {
+  if (!L) return DYRA_ERR_INVALID_ARG;
+  if (batch < 0 || n < 0) return DYRA_ERR_INVALID_ARG;
+  if (batch == 0 || n == 0) return DYRA_OK;
+  if (!X || !Y || !workspace) return DYRA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(X) & 15) || (reinterpret_cast<uintptr_t>(Y) & 15))
+    return DYRA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return DYRA_ERR_WORKSPACE;
+  const WsLayout w = layout_of(L, batch, n);
+  if (ws_bytes < w.total) return DYRA_ERR_WORKSPACE;
+  DeviceGuard guard(L->device);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if (L->dtype == DYRA_F32)
+    return forward_f32(L, static_cast<const float *>(X), batch, n, static_cast<float *>(Y), ws, w,
+                       s, rec);
+  const std::array<uintptr_t, 5> key = {reinterpret_cast<uintptr_t>(X),
+                                         reinterpret_cast<uintptr_t>(Y),
+                                         reinterpret_cast<uintptr_t>(workspace), (uintptr_t)batch,
+                                         (uintptr_t)n};
+  std::lock_guard<std::mutex> lock(L->mu);
+  std::shared_ptr<Plan> plan;
+  for (auto &kv : L->plans)
+    if (kv.first == key) plan = std::static_pointer_cast<Plan>(kv.second);
+  if (!plan) {
+    plan = std::make_shared<Plan>();
+    dyra_status ps = plan_bf16_lowrank(L, X, batch, n, Y, ws, w, *plan);
+    if (ps != DYRA_OK) return ps;
+    if (L->plans.size() >= 64) L->plans.erase(L->plans.begin());
+    L->plans.emplace_back(key, plan);
+  }
+  return run_plan(L, *plan, ws, s, rec);
+}
+
+// ------------------------------------------------------------------------ preparation
+
+void to_bf16(const double *src, size_t count, std::vector<__nv_bfloat16> &dst) {
+  dst.resize(count);
+  for (size_t i = 0; i < count; ++i) dst[i] = __float2bfloat16_rn((float)src[i]);
+}
+
+template <typename T>
+dyra_status upload(void **dptr, const std::vector<T> &host) {
+  const size_t bytes = host.size() * sizeof(T);
+  cudaError_t e = cudaMalloc(dptr, bytes ? bytes : 16);
+  if (e != cudaSuccess) {
+    g_last_error = std::string("cudaMalloc: ") + cudaGetErrorString(e);
+    return DYRA_ERR_OOM;
+  }
+  if (bytes) DY_CUDA(cudaMemcpy(*dptr, host.data(), bytes, cudaMemcpyHostToDevice));
+  return DYRA_OK;
+}
+
+void free_device(dyra_layer *L) {
+  if (L->w1) cudaFree(L->w1);
+  if (L->v) cudaFree(L->v);
+  if (L->wres) cudaFree(L->wres);
+  if (L->bias_d) cudaFree(L->bias_d);
+  if (L->ev_fork) cudaEventDestroy(L->ev_fork);
+  if (L->ev_join) cudaEventDestroy(L->ev_join);
+  if (L->aux) cudaStreamDestroy(L->aux);
+  L->w1 = L->v = L->wres = nullptr;
+  L->bias_d = nullptr;
+  L->ev_fork = L->ev_join = nullptr;
+  L->aux = nullptr;
+}
+
+// Monarch fit: each (a, c) block of W gets its leading singular triplet.
+void fit_monarch(const std::vector<double> &W, int d, int m, int nb, std::vector<double> &B1,
+                 std::vector<double> &B2, int threads) {
+  const int bi = d / nb, bo = m / nb;
+  B1.assign((size_t)nb * bi * nb, 0.0);
+  B2.assign((size_t)nb * nb * bo, 0.0);
+  struct Ctx {
+    const double *W;
+    int d, m, nb, bi, bo;
+    double *B1, *B2;
+  } ctx{W.data(), d, m, nb, bi, bo, B1.data(), B2.data()};
+  dyra::fit::parallel_for(nb * nb, threads, &ctx, [](const void *vc, int t) {
+    const Ctx &c = *static_cast<const Ctx *>(vc);
+    const int a = t / c.nb, cc = t % c.nb;
+    std::vector<double> blk((size_t)c.bi * c.bo);
+    for (int i = 0; i < c.bi; ++i)
+      for (int j = 0; j < c.bo; ++j)
+        blk[(size_t)i * c.bo + j] = c.W[(size_t)(a * c.bi + i) * c.m + (size_t)cc * c.bo + j];
+    std::vector<double> U((size_t)c.bi), S(1), Vt((size_t)c.bo);
+    dyra::fit::top_svd(c.bi, c.bo, blk.data(), 1, U.data(), S.data(), Vt.data(), 1);
+    const double root = std::sqrt(std::max(S[0], 0.0));
+    for (int i = 0; i < c.bi; ++i) c.B1[((size_t)a * c.bi + i) * c.nb + cc] = root * U[i];
+    for (int j = 0; j < c.bo; ++j) c.B2[((size_t)cc * c.nb + a) * c.bo + j] = root * Vt[j];
+  });
+}
+
+void monarch_dense(const std::vector<double> &B1, const std::vector<double> &B2, int d, int m,
+                   int nb, std::vector<double> &Wh) {
+  const int bi = d / nb, bo = m / nb;
+  Wh.assign((size_t)d * m, 0.0);
+  for (int a = 0; a < nb; ++a)
+    for (int i = 0; i < bi; ++i)
+      for (int c = 0; c < nb; ++c) {
+        const double u = B1[((size_t)a * bi + i) * nb + c];
+        if (u == 0.0) continue;
+        const double *v = &B2[((size_t)c * nb + a) * bo];
+        double *row = &Wh[(size_t)(a * bi + i) * m + (size_t)c * bo];
+        for (int j = 0; j < bo; ++j) row[j] = u * v[j];
+      }
+}
+
+// Argument checks shared by dyra_fit and dyra_prepare.
+dyra_status validate(const dyra_prepare_args *a, dyra_solver *solver_out, int *ns_out,
+                     bool device_checks) {
+  if (!a || !a->W) return DYRA_ERR_INVALID_ARG;
+  const int d = a->d, m = a->m, k = a->k, r = a->r;
+  if (d <= 0 || m <= 0 || r <= 0 || k < 0) return DYRA_ERR_INVALID_ARG;
+  if ((a->F1 == nullptr) != (a->F2 == nullptr)) return DYRA_ERR_INVALID_ARG;
+  if (!(a->ridge >= 0.0) || !std::isfinite(a->ridge)) return DYRA_ERR_INVALID_ARG;
+  if (a->dtype != DYRA_F32 && a->dtype != DYRA_BF16) return DYRA_ERR_INVALID_ARG;
+  if (a->kind == DYRA_STATIC_LOWRANK) {
+    if (k >= std::min(d, m) || r > std::min(d, m)) return DYRA_ERR_INVALID_ARG;
+    if (!a->R0 && k + r > std::min(d, m)) return DYRA_ERR_INVALID_ARG;
+  } else if (a->kind == DYRA_STATIC_MONARCH) {
+    if (k <= 0 || d % k || m % k) return DYRA_ERR_INVALID_ARG;
+    if (r > std::min(d, m)) return DYRA_ERR_INVALID_ARG;
+  } else {
+    return DYRA_ERR_INVALID_ARG;
+  }
+  dyra_solver solver = a->solver;
+  if (solver == DYRA_SOLVE_AUTO) solver = r <= 64 ? DYRA_SOLVE_CHOLESKY : DYRA_SOLVE_NEWTON_SCHULZ;
+  if (solver != DYRA_SOLVE_CHOLESKY && solver != DYRA_SOLVE_NEWTON_SCHULZ) return DYRA_ERR_INVALID_ARG;
+  *solver_out = solver;
+  *ns_out = a->ns_iters > 0 ? a->ns_iters : 8;
+  if (!device_checks) return DYRA_OK;
+  if (a->dtype == DYRA_F32) {
+    if (r > 64) return DYRA_ERR_UNSUPPORTED;
+    if (a->kind != DYRA_STATIC_LOWRANK) return DYRA_ERR_UNSUPPORTED;
+  } else {
+    if (r > 256 || r % 8 || d % 8 || m % 8) return DYRA_ERR_UNSUPPORTED;
+    if (solver == DYRA_SOLVE_CHOLESKY && r > 64) return DYRA_ERR_UNSUPPORTED;
+    if (a->kind == DYRA_STATIC_MONARCH && !dyra::monarch_supported(d, m, k, r))
+      return DYRA_ERR_UNSUPPORTED;
+  }
+  return DYRA_OK;
+}
+
+// Host fp64 offline step: static fit, W_res, R0, P (no device needed).
+dyra_status fit_host(const dyra_prepare_args *a, dyra_layer *L) {
+  const int d = a->d, m = a->m, k = a->k, r = a->r;
+  const int th = a->fit_threads;
+  const std::vector<double> W(a->W, a->W + (size_t)d * m);
+  L->bias.assign(m, 0.0);
+  if (a->b) std::copy(a->b, a->b + m, L->bias.begin());
+  if (a->kind == DYRA_STATIC_LOWRANK) {
+    if (a->F1) {
+      L->F1.assign(a->F1, a->F1 + (size_t)d * k);
+      L->F2.assign(a->F2, a->F2 + (size_t)k * m);
+    } else {
+      const int cnt = k + (a->R0 ? 0 : r);
+      std::vector<double> U((size_t)d * cnt), S(cnt), Vt((size_t)cnt * m);
+      if (!dyra::fit::top_svd(d, m, W.data(), cnt, U.data(), S.data(), Vt.data(), th)) {
+        g_last_error = "eigen-decomposition did not converge";
+        return DYRA_ERR_INVALID_ARG;
+      }
+      L->F1.assign((size_t)d * k, 0.0);
+      L->F2.assign((size_t)k * m, 0.0);
+      for (int j = 0; j < k; ++j) {
+        const double root = std::sqrt(S[j]);
+        for (int i = 0; i < d; ++i) L->F1[(size_t)i * k + j] = U[(size_t)i * cnt + j] * root;
+        for (int i = 0; i < m; ++i) L->F2[(size_t)j * m + i] = Vt[(size_t)j * m + i] * root;
+      }
+      // for a truncated-SVD W_hat, the residual's top right singular vectors are W's
+      // singular vectors k+1..k+r
+      if (!a->R0) L->R0.assign(Vt.begin() + (size_t)k * m, Vt.begin() + (size_t)(k + r) * m);
+    }
+    L->W_hat.assign((size_t)d * m, 0.0);
+    if (k > 0) dyra::fit::gemm(d, m, k, L->F1.data(), false, L->F2.data(), false, L->W_hat.data(), th);
+  } else {
+    const int nb = k;
+    if (a->F1) {
+      L->F1.assign(a->F1, a->F1 + (size_t)d * nb);
+      L->F2.assign(a->F2, a->F2 + (size_t)nb * m);
+    } else {
+      fit_monarch(W, d, m, nb, L->F1, L->F2, th);
+    }
+    monarch_dense(L->F1, L->F2, d, m, nb, L->W_hat);
+  }
+  L->W_res.resize((size_t)d * m);
+  for (size_t i = 0; i < L->W_res.size(); ++i) L->W_res[i] = W[i] - L->W_hat[i];
+  if (a->R0) {
+    L->R0.assign(a->R0, a->R0 + (size_t)r * m);
+  } else if (L->R0.empty()) {
+    std::vector<double> U((size_t)d * r), S(r), Vt((size_t)r * m);
+    if (!dyra::fit::top_svd(d, m, L->W_res.data(), r, U.data(), S.data(), Vt.data(), th)) {
+      g_last_error = "eigen-decomposition did not converge";
+      return DYRA_ERR_INVALID_ARG;
+    }
+    L->R0 = Vt;
+  }
+  // P = W_res R0^T (R0 R0^T)^-1
+  std::vector<double> gram((size_t)r * r), WR((size_t)r * d);
+  dyra::fit::gemm(r, r, m, L->R0.data(), false, L->R0.data(), true, gram.data(), th);
+  if (!dyra::fit::cholesky(r, gram.data())) {
+    g_last_error = "R0 R0^T is not positive definite (R0 rank deficient)";
+    return DYRA_ERR_INVALID_ARG;
+  }
+  dyra::fit::gemm(r, d, m, L->R0.data(), false, L->W_res.data(), true, WR.data(), th);   // R0 W_res^T
+  dyra::fit::cholesky_solve(r, gram.data(), WR.data(), d);
+  L->P.resize((size_t)d * r);
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < r; ++j) L->P[(size_t)i * r + j] = WR[(size_t)j * d + i];
+  return DYRA_OK;
+}
+
+dyra_layer *new_layer(const dyra_prepare_args *a, dyra_solver solver, int ns_iters) {
+  dyra_layer *L = new (std::nothrow) dyra_layer();
+  if (!L) return nullptr;
+  L->d = a->d; L->m = a->m; L->k = a->k; L->r = a->r;
+  L->kp = (a->kind == DYRA_STATIC_LOWRANK) ? roundup(a->k, 64) : 0;
+  L->kind = a->kind; L->dtype = a->dtype; L->solver = solver; L->ns_iters = ns_iters;
+  L->ridge = a->ridge; L->device = a->device;
+  return L;
+}
+
+dyra_status upload_layer(const dyra_prepare_args *a, dyra_layer *L) {
+  const int d = L->d, m = L->m, k = L->k, r = L->r;
+  dyra_status st = DYRA_OK;
+  std::vector<float> bias32(L->bias.begin(), L->bias.end());
+  if (a->dtype == DYRA_BF16) {
+    const int kp = L->kp, N1 = kp + r;
+    std::vector<double> w1((size_t)N1 * d, 0.0), vt((size_t)m * std::max(kp, 1), 0.0),
+        wrt((size_t)m * d);
+    for (int j = 0; j < k; ++j)
+      for (int i = 0; i < d; ++i) w1[(size_t)j * d + i] = L->F1[(size_t)i * k + j];
+    for (int j = 0; j < r; ++j)
+      for (int i = 0; i < d; ++i) w1[(size_t)(kp + j) * d + i] = L->P[(size_t)i * r + j];
+    for (int i = 0; i < k; ++i)
+      for (int j = 0; j < m; ++j) vt[(size_t)j * kp + i] = L->F2[(size_t)i * m + j];
+    for (int i = 0; i < d; ++i)
+      for (int j = 0; j < m; ++j) wrt[(size_t)j * d + i] = L->W_res[(size_t)i * m + j];
+    std::vector<__nv_bfloat16> h;
+    to_bf16(w1.data(), w1.size(), h);
+    if (st == DYRA_OK) st = upload(&L->w1, h);
+    to_bf16(vt.data(), vt.size(), h);
+    if (st == DYRA_OK) st = upload(&L->v, h);
+    to_bf16(wrt.data(), wrt.size(), h);
+    if (st == DYRA_OK) st = upload(&L->wres, h);
+    if (st == DYRA_OK) {
+      cudaError_t e = cudaStreamCreateWithFlags(&L->aux, cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming);
+      if (e != cudaSuccess) st = cuda_fail(e, "auxiliary stream / events");
+    }
+  } else {
+    const int N1 = k + r;
+    std::vector<float> wc((size_t)d * N1), vv((size_t)std::max(k, 1) * m, 0.f), wr((size_t)d * m);
+    for (int i = 0; i < d; ++i) {
+      for (int j = 0; j < k; ++j) wc[(size_t)i * N1 + j] = (float)L->F1[(size_t)i * k + j];
+      for (int j = 0; j < r; ++j) wc[(size_t)i * N1 + k + j] = (float)L->P[(size_t)i * r + j];
+    }
+    for (size_t i = 0; i < L->F2.size(); ++i) vv[i] = (float)L->F2[i];
+    for (size_t i = 0; i < wr.size(); ++i) wr[i] = (float)L->W_res[i];
+    if (st == DYRA_OK) st = upload(&L->w1, wc);
+    if (st == DYRA_OK) st = upload(&L->v, vv);
+    if (st == DYRA_OK) st = upload(&L->wres, wr);
+  }
+  if (st == DYRA_OK) {
+    void *bp = nullptr;
+    st = upload(&bp, bias32);
+    L->bias_d = static_cast<float *>(bp);
+  }
+  return st;
+}
+
+dyra_status prepare_impl(const dyra_prepare_args *a, dyra_layer **out) {
+  if (!out) return DYRA_ERR_INVALID_ARG;
+  *out = nullptr;
+  dyra_solver solver;
+  int ns_iters;
+  dyra_status vs = validate(a, &solver, &ns_iters, true);
+  if (vs != DYRA_OK) return vs;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || a->device < 0 || a->device >= ndev)
+    return DYRA_ERR_NO_DEVICE;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, a->device) != cudaSuccess) return DYRA_ERR_NO_DEVICE;
+  if (prop.major != 10 || prop.minor != 3) {
+    g_last_error = "device is not sm_103";
+    return DYRA_ERR_NO_DEVICE;
+  }
+  dyra_layer *L = new_layer(a, solver, ns_iters);
+  if (!L) return DYRA_ERR_OOM;
+  dyra_status st = fit_host(a, L);
+  if (st == DYRA_OK) {
+    DeviceGuard guard(L->device);
+    st = upload_layer(a, L);
+    if (st != DYRA_OK) free_device(L);
+  }
+  if (st != DYRA_OK) {
+    delete L;
+    return st;
+  }
+  *out = L;
+  return DYRA_OK;
+}
+
+}  // namespace
+
+// ============================================================================ C ABI
+
+extern "C" {
+
+dyra_status dyra_prepare(const dyra_prepare_args *args, dyra_layer **out) {
+  try {
+    return prepare_impl(args, out);
+  } catch (const std::bad_alloc &) {
+    return DYRA_ERR_OOM;
+  } catch (...) {
+    g_last_error = "unexpected host exception in dyra_prepare";
+    return DYRA_ERR_INVALID_ARG;
+  }
+}
+
+dyra_status dyra_fit(const dyra_prepare_args *args, double *W_hat, double *W_res, double *P,
+                     double *R0, double *F1, double *F2) {
+  try {
+    dyra_solver solver;
+    int ns_iters;
+    dyra_status vs = validate(args, &solver, &ns_iters, false);
+    if (vs != DYRA_OK) return vs;
+    std::unique_ptr<dyra_layer> L(new_layer(args, solver, ns_iters));
+    if (!L) return DYRA_ERR_OOM;
+    dyra_status fs = fit_host(args, L.get());
+    if (fs == DYRA_OK) {
+      if (W_hat) std::copy(L->W_hat.begin(), L->W_hat.end(), W_hat);
+      if (W_res) std::copy(L->W_res.begin(), L->W_res.end(), W_res);
+      if (P) std::copy(L->P.begin(), L->P.end(), P);
+      if (R0) std::copy(L->R0.begin(), L->R0.end(), R0);
+      if (F1) std::copy(L->F1.begin(), L->F1.end(), F1);
+      if (F2) std::copy(L->F2.begin(), L->F2.end(), F2);
+    }
+    return fs;
+  } catch (const std::bad_alloc &) {
+    return DYRA_ERR_OOM;
+  } catch (...) {
+    g_last_error = "unexpected host exception in dyra_fit";
+    return DYRA_ERR_INVALID_ARG;
+  }
+}
+
+void dyra_layer_destroy(dyra_layer *layer) {
+  if (!layer) return;
+  {
+    DeviceGuard guard(layer->device);
+    if (layer->aux) cudaStreamSynchronize(layer->aux);
+    free_device(layer);
+  }
+  delete layer;
+}
+
+dyra_status dyra_layer_info(const dyra_layer *L, dyra_layer_desc *out) {
+  if (!L || !out) return DYRA_ERR_INVALID_ARG;
+  out->d = L->d; out->m = L->m; out->k = L->k; out->r = L->r;
+  out->kind = L->kind; out->dtype = L->dtype; out->solver = L->solver;
+  out->ns_iters = L->ns_iters; out->ridge = L->ridge; out->device = L->device;
+  out->kernels_per_forward = kernels_per_forward(L);
+  return DYRA_OK;
+}
+
+dyra_status dyra_export(const dyra_layer *L, double *W_hat, double *W_res, double *P, double *R0) {
+  if (!L) return DYRA_ERR_INVALID_ARG;
+  if (W_hat) std::copy(L->W_hat.begin(), L->W_hat.end(), W_hat);
+  if (W_res) std::copy(L->W_res.begin(), L->W_res.end(), W_res);
+  if (P) std::copy(L->P.begin(), L->P.end(), P);
+  if (R0) std::copy(L->R0.begin(), L->R0.end(), R0);
+  return DYRA_OK;
+}
+
+dyra_status dyra_export_factors(const dyra_layer *L, double *F1, double *F2) {
+  if (!L) return DYRA_ERR_INVALID_ARG;
+  if (F1) std::copy(L->F1.begin(), L->F1.end(), F1);
+  if (F2) std::copy(L->F2.begin(), L->F2.end(), F2);
+  return DYRA_OK;
+}
+
+dyra_status dyra_workspace_size(const dyra_layer *L, int batch, int n, size_t *bytes) {
+  if (!L || !bytes || batch < 0 || n < 0) return DYRA_ERR_INVALID_ARG;
+  *bytes = layout_of(L, batch, n).total;
+  return DYRA_OK;
+}
+
+dyra_status dyra_linear_forward(const dyra_layer *L, const void *X, int batch, int n, void *Y,
+                                void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Recorder rec;
+  return forward_impl(L, X, batch, n, Y, workspace, workspace_bytes, stream, rec);
+}
+
+dyra_status dyra_linear_forward_profiled(const dyra_layer *L, const void *X, int batch, int n,
+                                         void *Y, void *workspace, size_t workspace_bytes,
+                                         cudaStream_t stream, cudaEvent_t *events, int max_events,
+                                         int *recorded) {
+  if (!L || !events || max_events < kernels_per_forward(L) + 1) return DYRA_ERR_INVALID_ARG;
+  Recorder rec;
+  rec.ev = events;
+  rec.max = max_events;
+  dyra_status st = forward_impl(L, X, batch, n, Y, workspace, workspace_bytes, stream, rec);
+  if (recorded) *recorded = rec.count;
+  return st;
+}
+
+dyra_status dyra_linear_forward_host(const dyra_layer *L, const void *X_host, int batch, int n,
+                                     void *Y_host, void *X_dev, void *Y_dev, void *workspace,
+                                     size_t workspace_bytes, cudaStream_t stream) {
+  if (!L || batch < 0 || n < 0) return DYRA_ERR_INVALID_ARG;
+  if (batch == 0 || n == 0) return DYRA_OK;
+  if (!X_host || !Y_host || !X_dev || !Y_dev || !workspace) return DYRA_ERR_INVALID_ARG;
+  const size_t eb = L->dtype == DYRA_F32 ? 4 : 2;
+  const size_t xb = (size_t)batch * n * L->d * eb, yb = (size_t)batch * n * L->m * eb;
+  if (workspace_bytes < layout_of(L, batch, n).total) return DYRA_ERR_WORKSPACE;
+  DeviceGuard guard(L->device);
+  DY_CUDA(cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, stream));
+  Recorder rec;
+  dyra_status st = forward_impl(L, X_dev, batch, n, Y_dev, workspace, workspace_bytes, stream, rec);
+  if (st != DYRA_OK) return st;
+  DY_CUDA(cudaMemcpyAsync(Y_host, Y_dev, yb, cudaMemcpyDeviceToHost, stream));
+  return DYRA_OK;
+}
+
+const char *dyra_kernel_name(const dyra_layer *L, int i) {
+  if (!L) return nullptr;
+  return kernel_name(L, i);
+}
+
+dyra_status dyra_workspace_status(const dyra_layer *L, const void *workspace, cudaStream_t stream,
+                                  int *not_spd_samples, int *timeouts) {
+  if (!L || !workspace) return DYRA_ERR_INVALID_ARG;
+  DeviceGuard guard(L->device);
+  int h[2] = {0, 0};
+  DY_CUDA(cudaStreamSynchronize(stream));
+  DY_CUDA(cudaMemcpy(h, workspace, sizeof(h), cudaMemcpyDeviceToHost));
+  if (not_spd_samples) *not_spd_samples = h[0];
+  if (timeouts) *timeouts = h[1];
+  if (h[1] > 0) return DYRA_ERR_TIMEOUT;
+  if (h[0] > 0) return DYRA_ERR_NOT_SPD;
+  return DYRA_OK;
+}
+
+dyra_status dyra_workspace_tensor(const dyra_layer *L, int batch, int n, int which,
+                                  size_t *offset_bytes, int *ld) {
+  if (!L || !offset_bytes || !ld || batch < 0 || n < 0) return DYRA_ERR_INVALID_ARG;
+  const WsLayout w = layout_of(L, batch, n);
+  const bool bf = L->dtype == DYRA_BF16;
+  size_t off = 0;
+  int l = 0;
+  switch (which) {
+    case DYRA_BUF_T: off = w.T; l = w.ldT; break;
+    case DYRA_BUF_C: off = w.C; l = L->d; break;
+    case DYRA_BUF_G: off = w.G; l = L->r; break;
+    case DYRA_BUF_GINV: off = w.Ginv; l = L->r; break;
+    case DYRA_BUF_B: off = w.B; l = bf ? L->r : L->m; break;
+    case DYRA_BUF_R: if (bf) return DYRA_ERR_UNSUPPORTED; off = w.R; l = L->m; break;
+    default: return DYRA_ERR_INVALID_ARG;
+  }
+  *offset_bytes = off;
+  *ld = l;
+  return DYRA_OK;
+}
+
+const char *dyra_status_string(dyra_status s) {
+  switch (s) {
+    case DYRA_OK: return "ok";
+    case DYRA_ERR_INVALID_ARG: return "invalid argument";
+    case DYRA_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case DYRA_ERR_CUDA: return "CUDA error";
+    case DYRA_ERR_OOM: return "out of memory";
+    case DYRA_ERR_NOT_SPD: return "L^T L + lambda I not positive definite for some sample";
+    case DYRA_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+    case DYRA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case DYRA_ERR_NO_DEVICE: return "no usable sm_103 device";
+  }
+  return "unknown status";
+}
+
+const char *dyra_last_error(void) { return g_last_error.c_str(); }
+
+int dyra_abi_version(void) { return DYRA_ABI_VERSION; }
+
+}  // extern "C"

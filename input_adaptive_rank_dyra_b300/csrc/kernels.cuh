@@ -1,0 +1,28 @@
+// Launch helpers of the non-GEMM kernels of the DyRA forward.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace dyra {
+
+// bf16 path, SPD solves (solve.cu)
+cudaError_t launch_chol_inverse(const float *G, int batch, int r, float ridge, __nv_bfloat16 *Ginv,
+                                int *status, cudaStream_t s);
+cudaError_t launch_ns_prep(const float *G, int batch, int r, float ridge, float *Gh, float *X0,
+                           float *dinv, int *flags, cudaStream_t s);
+cudaError_t launch_ns_finish(const float *X, const float *dinv, int batch, int r, const int *flags,
+                             __nv_bfloat16 *Ginv, int *status, cudaStream_t s);
+
+// fp32 path (f32_path.cu)
+cudaError_t launch_sgemm(int batch, int M, int N, int K, const float *A, long long sAb,
+                         long long sAi, long long sAk, const float *B, long long sBb, long long sBk,
+                         long long sBj, float *C, long long sCb, long long sCi, long long sCj,
+                         bool accumulate, const float *bias, cudaStream_t s);
+cudaError_t launch_gram_f64(const float *T, int batch, int n, int ldT, int l0, int r,
+                            long long sTb, double *G, cudaStream_t s);
+cudaError_t launch_inverse_f64(const double *G, int batch, int r, double ridge, bool ns,
+                               int ns_iters, double *Ginv, int *status, cudaStream_t s);
+cudaError_t launch_apply_inverse(const double *Ginv, const float *B, int batch, int r, int m,
+                                 float *R, cudaStream_t s);
+
+}  // namespace dyra

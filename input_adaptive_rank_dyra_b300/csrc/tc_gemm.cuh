@@ -1,0 +1,88 @@
+// A TMA-fed tcgen05 GEMM engine for the DyRA forward: D[b] = A[b] B[b]^T with both operands
+// stored K-contiguous ("K-major") or MN-contiguous, fp32 accumulation in TMEM.
+//
+// Persistent kernel: a grid of at most one CTA per SM walks the tiles (batch, m tile,
+// n tile), n fastest, in a static round-robin. Each CTA has six warps:
+//   warp 0      TMA producer (one lane): 128-byte K chunks of A (128 rows) and B (BN rows)
+//               into a ring of smem stages; it runs ahead across tile boundaries
+//   warp 1      TMEM allocation and MMA issue (one lane): 4 MMAs (32 bytes of K each) per
+//               chunk into one of two TMEM accumulators, so the epilogue of tile i overlaps
+//               the main loop of tile i+1
+//   warps 2..5  epilogue: tcgen05.ld of the 128 x BN accumulator (one TMEM lane quarter per
+//               warp, one row per thread), then the epilogue mode below; row-major bf16
+//               results go through a swizzled smem staging buffer and TMA bulk stores
+// Operands are bf16 (kind::f16, K-major or MN-major) or fp32 read as tf32 (kind::tf32,
+// K-major only), always in the 128-byte swizzled layout that TMA writes.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dyra {
+
+enum TcEpi : int {
+  EPI_ROW_BF16 = 0,    // out[b][g][c] = bf16(acc + bias[c]); TMA store when tma_store is set
+  EPI_TRANS_BF16 = 1,  // out[b*bs + (g/rb)*gs + g%rb + c*ld] = bf16(acc)
+  EPI_CG = 2,          // m tiles < a_split: out[b*bs + c*ld + g] = bf16(acc)   (C from C^T)
+                       // m tiles >= a_split: out2[b*bs2 + g*ld2 + c] = acc    (G, fp32)
+  EPI_ROW_F32 = 3,     // out[b][g][c] = alpha*acc + beta*aux[b][g][c]   (fp32)
+  EPI_TRANS_F32 = 4    // out[b*bs + (g/rb)*gs + g%rb + c*ld] = alpha*acc (fp32)
+};
+
+struct TcGemmParams {
+  int m_tiles, n_tiles, batch;
+  int BN;            // MMA N of a tile: multiple of 16 (of 64 for MN-major B), <= 256
+  int k_chunks;      // K in 128-byte chunks
+  int elem_bytes;    // 2 = bf16, 4 = fp32/tf32
+  int a_major, b_major;   // 0 = K-major, 1 = MN-major
+  int a_split;       // m tiles >= a_split load from map A1 (M coordinate restarts at 0)
+  int a_batched0, a_batched1;  // map carries the batch coordinate
+  int b_split;       // k chunks >= b_split load from map B1 (K coordinate restarts at 0)
+  int b_batched0, b_batched1;
+  uint32_t idesc;
+  uint32_t acc_cols;  // TMEM columns of one accumulator (power of two >= BN)
+  int stages;
+  uint32_t smem_bytes;
+  uint32_t staging_off;  // byte offset of the epilogue staging buffers (TMA store)
+  // epilogue
+  int epi;
+  int tma_store;     // EPI_ROW_BF16 through the output tensor map (needs BN % 32 == 0)
+  int out_batched;   // output map carries the batch coordinate
+  void *out;
+  long long out_bstride, out_ld, out_gstride;
+  int rb;
+  int rows_valid, cols_valid;     // region of tiles < a_split
+  void *out2;
+  long long out2_bstride, out2_ld;
+  int rows2_valid, cols2_valid;   // region of tiles >= a_split (EPI_CG)
+  const float *bias;
+  const float *aux;
+  long long aux_bstride, aux_ld;
+  float alpha, beta;
+  int *timeouts;                  // device counter of bounded waits that gave up
+};
+
+struct TcOperand {
+  // One TMA source: a [batch][rows][inner] tensor (inner contiguous).
+  const void *base;
+  int elem_bytes;
+  long long inner, rows, batch;         // extents in elements
+  long long row_stride, batch_stride;   // in bytes
+};
+
+// Build the instruction descriptor (M = 128).
+uint32_t tc_idesc(int elem_bytes, int a_major, int b_major, int n);
+
+// Creates a 3-D tensor map with 128-byte swizzle, box = {chunk, box_rows, 1}.
+bool tc_make_map(CUtensorMap *map, const TcOperand &op, int box_rows);
+
+// Creates the bf16 output map of the TMA-store epilogue: box {32, 32, 1}, 64-byte swizzle.
+bool tc_make_store_map(CUtensorMap *map, const TcOperand &op);
+
+// Fills stages / smem / TMEM columns / grid for a given BN and launches the kernel.
+// `out_map` is used only when p.tma_store is set.
+cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensorMap &a1,
+                           const CUtensorMap &b0, const CUtensorMap &b1,
+                           const CUtensorMap &out_map, cudaStream_t stream);
+
+}  // namespace dyra

@@ -1,0 +1,123 @@
+"""CPU tests of the C ABI: the library loads, exports every entry point the header declares,
+rejects bad arguments without touching a device, and its host-side offline fit matches the
+oracle. No compute call runs on a GPU here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as WL
+from input_adaptive_rank_dyra_b300 import dyra as D
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "dyra.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dyra_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    lib = D.load()
+    declared = _header_functions()
+    assert "dyra_prepare" in declared and "dyra_linear_forward" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) <= set(D.EXPORTED)
+    assert lib.dyra_abi_version() == 1
+
+
+def test_status_strings():
+    lib = D.load()
+    for code in range(9):
+        assert lib.dyra_status_string(code)
+    assert lib.dyra_status_string(0) == b"ok"
+
+
+def _args(W, **kw):
+    W = np.ascontiguousarray(W, dtype=np.float64)
+    a = D.PrepareArgs()
+    a.W = W.ctypes.data_as(D._c_double_p)
+    a.d, a.m = W.shape
+    a.kind, a.k, a.r = 0, 4, 2
+    a.dtype = 1
+    for key, val in kw.items():
+        setattr(a, key, val)
+    return a, W
+
+
+@pytest.mark.parametrize("bad", [
+    dict(d=0), dict(r=0), dict(k=-1), dict(k=40), dict(ridge=-1.0), dict(kind=7), dict(dtype=9),
+    dict(solver=9),
+])
+def test_prepare_rejects_bad_arguments(bad):
+    lib = D.load()
+    W = np.random.default_rng(0).standard_normal((32, 48))
+    a, keep = _args(W, **bad)
+    h = ctypes.c_void_p()
+    assert lib.dyra_prepare(ctypes.byref(a), ctypes.byref(h)) == 1   # INVALID_ARG
+    assert not h.value
+
+
+def test_prepare_rejects_null_and_unsupported():
+    lib = D.load()
+    h = ctypes.c_void_p()
+    assert lib.dyra_prepare(None, ctypes.byref(h)) == 1
+    W = np.random.default_rng(0).standard_normal((32, 48))
+    a, keep = _args(W, r=6)          # the bf16 kernels need r % 8 == 0
+    assert lib.dyra_prepare(ctypes.byref(a), ctypes.byref(h)) == 2
+    a, keep = _args(W, r=8, solver=1, k=0)   # fine for validation; a device is then needed
+    assert lib.dyra_prepare(ctypes.byref(a), ctypes.byref(h)) in (0, 8)
+
+
+def test_forward_rejects_bad_arguments_without_device():
+    lib = D.load()
+    assert lib.dyra_linear_forward(None, None, 1, 1, None, None, 0, None) == 1
+    assert lib.dyra_workspace_size(None, 1, 1, None) == 1
+    assert lib.dyra_workspace_status(None, None, None, None, None) == 1
+    assert lib.dyra_kernel_name(None, 0) is None
+
+
+def test_fit_lowrank_matches_oracle():
+    cfg = WL.get_config("c2")
+    W, b = WL.make_weights(cfg)
+    f = D.fit(W, kind="lowrank", k=cfg.k, r=cfg.r)
+    p = O.prepare(W, b, "lowrank", cfg.k, cfg.r)
+    scale = np.abs(W).max()
+    assert np.abs(f["W_hat"] - p["W_hat"]).max() < 1e-9 * scale
+    assert np.abs(f["W_res"] - p["W_res"]).max() < 1e-9 * scale
+    # R0 and P are fixed up to an r x r rotation; the projector and P R0 are not
+    assert np.allclose(f["R0"].T @ f["R0"], p["R0"].T @ p["R0"], atol=1e-8)
+    assert np.abs(f["P"] @ f["R0"] - p["P"] @ p["R0"]).max() < 1e-9 * scale
+
+
+def test_fit_with_supplied_r0_and_factors():
+    rng = np.random.default_rng(3)
+    W = rng.standard_normal((40, 56))
+    p = O.prepare(W, np.zeros(56), "lowrank", 6, 5)
+    R0 = rng.standard_normal((5, 56))
+    f = D.fit(W, kind="lowrank", k=6, r=5, R0=R0, F1=p["F1"], F2=p["F2"])
+    assert np.allclose(f["W_hat"], p["W_hat"], atol=1e-12)
+    assert np.allclose(f["P"], O.projection(p["W_res"], R0), atol=1e-10)
+
+
+def test_fit_monarch_matches_oracle():
+    cfg = WL.get_config("c4")
+    W, b = WL.make_weights(cfg)
+    f = D.fit(W, kind="monarch", k=cfg.k, r=cfg.r)
+    p = O.prepare(W, b, "monarch", cfg.k, cfg.r)
+    scale = np.abs(W).max()
+    assert np.abs(f["W_hat"] - p["W_hat"]).max() < 1e-9 * scale
+    assert np.abs(f["P"] @ f["R0"] - p["P"] @ p["R0"]).max() < 1e-8 * scale
+
+
+def test_fit_rejects_rank_deficient_r0():
+    W = np.random.default_rng(4).standard_normal((20, 30))
+    R0 = np.zeros((3, 30))
+    R0[0, 0] = R0[1, 0] = R0[2, 1] = 1.0
+    with pytest.raises(D.DyraError):
+        D.fit(W, kind="lowrank", k=2, r=3, R0=R0)

@@ -158,10 +158,12 @@ dyra_status dyra_linear_forward_host(const dyra_layer *layer, const void *X_host
                                      void *workspace, size_t workspace_bytes,
                                      cudaStream_t stream);
 
-/* Forward that also records `events[i]` before kernel i and events[count] after the last
- * one (count = kernels_per_forward, so max_events >= count + 1), to time each kernel. Every
- * kernel runs on `stream` here (no fork), so consecutive events bracket one kernel.
- * *recorded receives count + 1. */
+/* The same forward (same streams, same kernels) that also records two events around every
+ * kernel it launches: events[2i] just before kernel i and events[2i + 1] just after it, both
+ * on the stream kernel i runs on (the caller's stream, or the layer's auxiliary stream for
+ * the SPD-solve branch), so cudaEventElapsedTime(events[2i], events[2i + 1]) is kernel i's
+ * device time. count = kernels_per_forward; max_events must be >= 2 * count. *recorded
+ * receives 2 * count. Errors as dyra_linear_forward, plus INVALID_ARG for too few events. */
 dyra_status dyra_linear_forward_profiled(const dyra_layer *layer, const void *X, int batch,
                                          int n, void *Y, void *workspace,
                                          size_t workspace_bytes, cudaStream_t stream,

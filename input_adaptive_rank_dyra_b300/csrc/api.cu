@@ -149,6 +149,7 @@ struct Plan {
   std::vector<Step> steps;
 };
 
+// Records an event pair around each kernel, on the stream that kernel runs on.
 struct Recorder {
   cudaEvent_t *ev = nullptr;
   int max = 0, count = 0;
@@ -157,6 +158,13 @@ struct Recorder {
     ++count;
   }
 };
+
+#define DY_TIMED(rec, stream, call) \
+  do {                              \
+    (rec).mark(stream);             \
+    DY_CUDA(call);                  \
+    (rec).mark(stream);             \
+  } while (0)
 
 bool make_map(CUtensorMap *map, const void *base, int eb, long long inner, long long rows,
               long long batch, long long row_stride_el, long long batch_stride_el, int box_rows) {
@@ -476,11 +484,10 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
   return DYRA_OK;
 }
 
-// With events (profiled) every step runs on `s`, so consecutive events bracket one kernel.
 dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream_t s,
                      Recorder &rec) {
   using namespace dyra;
-  const bool fork = rec.ev == nullptr && L->aux != nullptr;
+  const bool fork = L->aux != nullptr;
   DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
   for (const Step &st : plan.steps) {
     if (st.kind == Step::FORK) {
@@ -498,25 +505,25 @@ dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream
       continue;
     }
     cudaStream_t ks = (fork && st.aux) ? L->aux : s;
-    rec.mark(ks);
     switch (st.kind) {
       case Step::GEMM:
-        DY_CUDA(tc_gemm_launch(st.p, st.a0, st.a1, st.b0, st.b1, st.out, ks));
+        DY_TIMED(rec, ks, tc_gemm_launch(st.p, st.a0, st.a1, st.b0, st.b1, st.out, ks));
         break;
       case Step::CHOL:
-        DY_CUDA(launch_chol_inverse(st.G, st.batch, st.r, st.ridge, st.Ginv, st.status, ks));
+        DY_TIMED(rec, ks, launch_chol_inverse(st.G, st.batch, st.r, st.ridge, st.Ginv, st.status, ks));
         break;
       case Step::NS_PREP:
-        DY_CUDA(launch_ns_prep(st.G, st.batch, st.r, st.ridge, st.Gh, st.X0, st.dinv, st.flags, ks));
+        DY_TIMED(rec, ks,
+                 launch_ns_prep(st.G, st.batch, st.r, st.ridge, st.Gh, st.X0, st.dinv, st.flags, ks));
         break;
       case Step::NS_FINISH:
-        DY_CUDA(launch_ns_finish(st.Xf, st.dinv, st.batch, st.r, st.flags, st.Ginv, st.status, ks));
+        DY_TIMED(rec, ks,
+                 launch_ns_finish(st.Xf, st.dinv, st.batch, st.r, st.flags, st.Ginv, st.status, ks));
         break;
       default:
         break;
     }
   }
-  rec.mark(s);
   return DYRA_OK;
 }
 
@@ -538,29 +545,28 @@ dyra_status forward_f32(const dyra_layer *L, const float *X, int batch, int n, f
   const float *Wr = static_cast<const float *>(L->wres);
   const long long nT = (long long)n * ldT;
   DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
-  rec.mark(s);   // T = X [U | P]
-  DY_CUDA(launch_sgemm(batch, n, ldT, d, X, (long long)n * d, d, 1, Wcat, 0, ldT, 1, T, nT, ldT, 1,
-                       false, nullptr, s));
-  rec.mark(s);   // G = L^T L (fp64)
-  DY_CUDA(launch_gram_f64(T, batch, n, ldT, k, r, nT, G, s));
-  rec.mark(s);   // C = L^T X
-  DY_CUDA(launch_sgemm(batch, r, d, n, T + k, nT, 1, ldT, X, (long long)n * d, d, 1, C,
-                       (long long)r * d, d, 1, false, nullptr, s));
-  rec.mark(s);   // B = C W_res
-  DY_CUDA(launch_sgemm(batch, r, m, d, C, (long long)r * d, d, 1, Wr, 0, m, 1, Bm, (long long)r * m,
-                       m, 1, false, nullptr, s));
-  rec.mark(s);   // (G + lambda I)^-1
-  DY_CUDA(launch_inverse_f64(G, batch, r, L->ridge, L->solver == DYRA_SOLVE_NEWTON_SCHULZ,
-                             L->ns_iters, Gi, status, s));
-  rec.mark(s);   // R = G^-1 B
-  DY_CUDA(launch_apply_inverse(Gi, Bm, batch, r, m, R, s));
-  rec.mark(s);   // Y = (X U) V + b
-  DY_CUDA(launch_sgemm(batch, n, m, k, T, nT, ldT, 1, V, 0, m, 1, Y, (long long)n * m, m, 1, false,
-                       L->bias_d, s));
-  rec.mark(s);   // Y += L R
-  DY_CUDA(launch_sgemm(batch, n, m, r, T + k, nT, ldT, 1, R, (long long)r * m, m, 1, Y,
-                       (long long)n * m, m, 1, true, nullptr, s));
-  rec.mark(s);
+  // T = X [U | P]
+  DY_TIMED(rec, s, launch_sgemm(batch, n, ldT, d, X, (long long)n * d, d, 1, Wcat, 0, ldT, 1, T,
+                                nT, ldT, 1, false, nullptr, s));
+  // G = L^T L (fp64)
+  DY_TIMED(rec, s, launch_gram_f64(T, batch, n, ldT, k, r, nT, G, s));
+  // C = L^T X
+  DY_TIMED(rec, s, launch_sgemm(batch, r, d, n, T + k, nT, 1, ldT, X, (long long)n * d, d, 1, C,
+                                (long long)r * d, d, 1, false, nullptr, s));
+  // B = C W_res
+  DY_TIMED(rec, s, launch_sgemm(batch, r, m, d, C, (long long)r * d, d, 1, Wr, 0, m, 1, Bm,
+                                (long long)r * m, m, 1, false, nullptr, s));
+  // (G + lambda I)^-1
+  DY_TIMED(rec, s, launch_inverse_f64(G, batch, r, L->ridge, L->solver == DYRA_SOLVE_NEWTON_SCHULZ,
+                                      L->ns_iters, Gi, status, s));
+  // R = G^-1 B
+  DY_TIMED(rec, s, launch_apply_inverse(Gi, Bm, batch, r, m, R, s));
+  // Y = (X U) V + b
+  DY_TIMED(rec, s, launch_sgemm(batch, n, m, k, T, nT, ldT, 1, V, 0, m, 1, Y, (long long)n * m, m,
+                                1, false, L->bias_d, s));
+  // Y += L R
+  DY_TIMED(rec, s, launch_sgemm(batch, n, m, r, T + k, nT, ldT, 1, R, (long long)r * m, m, 1, Y,
+                                (long long)n * m, m, 1, true, nullptr, s));
   return DYRA_OK;
 }
 
@@ -987,7 +993,7 @@ dyra_status dyra_linear_forward_profiled(const dyra_layer *L, const void *X, int
                                          void *Y, void *workspace, size_t workspace_bytes,
                                          cudaStream_t stream, cudaEvent_t *events, int max_events,
                                          int *recorded) {
-  if (!L || !events || max_events < kernels_per_forward(L) + 1) return DYRA_ERR_INVALID_ARG;
+  if (!L || !events || max_events < 2 * kernels_per_forward(L)) return DYRA_ERR_INVALID_ARG;
   Recorder rec;
   rec.ev = events;
   rec.max = max_events;

@@ -289,7 +289,8 @@ def linear_forward_host(layer: Layer, X_host, Y_host, X_dev, Y_dev, workspace, s
 
 def linear_forward_profiled(layer: Layer, X, Y, workspace, events, stream=None) -> int:
     """dyra_linear_forward_profiled: `events` = torch.cuda.Event(enable_timing=True) objects,
-    at least kernels_per_forward + 1; returns how many were recorded."""
+    at least 2 * kernels_per_forward; events[2i] and events[2i + 1] bracket kernel i on the
+    stream it runs on. Returns how many were recorded."""
     for e in events:           # torch creates the CUDA event lazily, on first record
         if e.cuda_event == 0:
             e.record()

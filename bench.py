@@ -87,8 +87,8 @@ def kernel_work(cfg, name: str):
         return 2.0 * B * n * d * (k + r), e * (B * n * d + (k + r) * d + B * n * (k + r))
     if name == "cg_c_gram":
         return 2.0 * B * n * r * (d + r), e * (B * n * d + B * n * r + B * r * d) + 4 * B * r * r
-    if name == "chol_inverse":
-        return B * (r ** 3) * 1.0, 4 * B * r * r + e * B * r * r
+    if name == "chol_solve_apply":   # in-place elimination (r^3 FMA) + L~ = L G^-1
+        return B * (2.0 * r ** 3 + 2.0 * n * r * r), 4 * B * r * r + e * (2 * B * n * r + B * r * r)
     if name == "lsolve_apply":
         return 2.0 * B * n * r * r, e * (2 * B * n * r + B * r * r)
     if name == "residual_product":
@@ -117,59 +117,107 @@ def layer_bytes(cfg):
 
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML while the timed region runs."""
+    """Samples the SM clock and the clock-event reasons while the timed region runs: through
+    NVML when pynvml is importable, else from an `nvidia-smi -lms` subprocess."""
     REASONS = {"gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
                "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
                "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
+    def __init__(self, device_index: int, period_s: float = 0.002):
         self.samples, self.reasons, self.ok = [], set(), False
         self.max_mhz = None
+        self.error = None
+        self.source = None
         self._stop = threading.Event()
         self._period = period_s
+        self._t = None
+        self._proc = None
+        self._bus = None
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(device_index)
+            self._bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        except Exception as e:
+            self.error = f"{type(e).__name__}: {e}"
         try:
             import pynvml
             pynvml.nvmlInit()
             self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            try:
+                self._h = pynvml.nvmlDeviceGetHandleByPciBusId(self._bus.encode())
+            except Exception:
+                self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
-            self.ok = False
-        self._t = None
+            self.ok, self.source = True, "nvml"
+        except Exception as e:   # reported in the JSON line, never fatal
+            self.error = f"{type(e).__name__}: {e}"
+            if self._bus is not None:
+                self.ok, self.source = True, "nvidia-smi"
 
     def _run(self):
         nv = self._nv
+        get = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                get = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                    nv.nvmlDeviceGetCurrentClocksThrottleReasons
-                mask = get(self._h)
-                for name, bit in self.REASONS.items():
-                    if mask & bit and name != "gpu_idle":
-                        self.reasons.add(name)
+                self._add_mask(get(self._h))
             except Exception:
                 pass
             time.sleep(self._period)
 
+    def _add_mask(self, mask: int):
+        for name, bit in self.REASONS.items():
+            if mask & bit and name != "gpu_idle":
+                self.reasons.add(name)
+
     def __enter__(self):
-        if self.ok:
+        if not self.ok:
+            return self
+        if self.source == "nvml":
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
+        else:
+            import subprocess
+            cmd = ["nvidia-smi", "-i", self._bus,
+                   "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                   "--format=csv,noheader,nounits", "-lms", "50"]
+            try:
+                self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                              stderr=subprocess.DEVNULL, text=True)
+            except Exception as e:
+                self.ok, self.error = False, f"{type(e).__name__}: {e}"
         return self
 
     def __exit__(self, *exc):
         if self._t is not None:
             self._stop.set()
             self._t.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                out, _ = self._proc.communicate(timeout=5)
+            except Exception:
+                self._proc.kill()
+                out, _ = self._proc.communicate()
+            for line in out.splitlines():
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 3:
+                    continue
+                try:
+                    self.samples.append(float(parts[0]))
+                    self.max_mhz = float(parts[1])
+                    self._add_mask(int(parts[2], 16))
+                except ValueError:
+                    continue
 
     def summary(self):
         if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None,
+                    "reasons": [f"clock sampling unavailable: {self.error}"]}
         med = statistics.median(self.samples) if self.samples else None
         return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+                "samples": len(self.samples), "source": self.source}
 
 
 def dist_init(gpus: int):
@@ -309,23 +357,49 @@ def run_dyra(args, cfg):
     names = layer.kernel_names()
     K, Wm = args.steps, args.warmup
 
-    # ---- device-resident timed region: forward with a start/end event around every kernel
+    # ---- device-resident timed region. Each timed step replays a CUDA graph of one forward
+    # (captured from the same C-ABI call), so the GPU runs the step's kernels back to back
+    # instead of waiting on host launches; each step's graph carries its own start/end event
+    # around every kernel, recorded on the stream the kernel runs on.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(K)]
     st = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     en = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for _ in range(Wm):
-        flush.fill_(1.0)
+    for _ in range(3):   # builds and caches the launch plan before capture
         dy.linear_forward(layer, Xd, Y, ws)
+        dy.linear_forward_profiled(layer, Xd, Y, ws, ev[0])
+    torch.cuda.synchronize()
+    graphs = []
+    cap = torch.cuda.Stream(dev)
+    for i in range(K):
+        g = torch.cuda.CUDAGraph()
+        for e in ev[i]:
+            e.record(cap)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            dy.linear_forward_profiled(layer, Xd, Y, ws, ev[i], stream=cap)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    # host cost of one forward call (enqueue only), for reference
+    t0 = time.perf_counter()
+    for _ in range(20):
+        dy.linear_forward(layer, Xd, Y, ws)
+    host_us = (time.perf_counter() - t0) / 20 * 1e6
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.__enter__()
+    for i in range(Wm):
+        flush.fill_(1.0)
+        graphs[i % K].replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        for i in range(K):
-            flush.fill_(float(i))
-            st[i].record(stream)
-            dy.linear_forward_profiled(layer, Xd, Y, ws, ev[i])
-            en[i].record(stream)
-        torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(float(i))
+        st[i].record(stream)
+        graphs[i].replay()
+        en[i].record(stream)
+    torch.cuda.synchronize()
+    clocks.__exit__(None, None, None)
     barrier(world)
     torch.cuda.synchronize()
     step_ms = [st[i].elapsed_time(en[i]) for i in range(K)]
@@ -416,6 +490,7 @@ def run_dyra(args, cfg):
                 "h2d_bytes_per_step": tokens * cfg.d * ebytes,
                 "d2h_bytes_per_step": tokens * cfg.m * ebytes},
         "gpu_launches": K * nk,
+        "host_enqueue_us": host_us,
         "clocks": clocks.summary(),
         "not_spd_samples": nsp,
         "prepare_s": prep_s,
@@ -430,8 +505,8 @@ def run_dyra(args, cfg):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="c2", choices=sorted(WL.CONFIGS))
     ap.add_argument("--impl", default="dyra", choices=["dyra", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -163,7 +163,9 @@ dyra_status dyra_linear_forward_host(const dyra_layer *layer, const void *X_host
  * on the stream kernel i runs on (the caller's stream, or the layer's auxiliary stream for
  * the SPD-solve branch), so cudaEventElapsedTime(events[2i], events[2i + 1]) is kernel i's
  * device time. count = kernels_per_forward; max_events must be >= 2 * count. *recorded
- * receives 2 * count. Errors as dyra_linear_forward, plus INVALID_ARG for too few events. */
+ * receives 2 * count. Called while `stream` is being captured into a CUDA graph, the records
+ * become event-record nodes (cudaEventRecordExternal), so every replay of the graph times
+ * its kernels. Errors as dyra_linear_forward, plus INVALID_ARG for too few events. */
 dyra_status dyra_linear_forward_profiled(const dyra_layer *layer, const void *X, int batch,
                                          int n, void *Y, void *workspace,
                                          size_t workspace_bytes, cudaStream_t stream,
@@ -187,7 +189,7 @@ typedef enum dyra_buffer {
   DYRA_BUF_C = 1,      /* C = L^T X, [batch, r, d] (bf16 / fp32)                           */
   DYRA_BUF_G = 2,      /* L^T L without lambda, [batch, r, r] (fp32 / fp64)                */
   DYRA_BUF_GINV = 3,   /* (L^T L + lambda I)^-1, [batch, r, r] (bf16 / fp64)               */
-  DYRA_BUF_B = 4,      /* B = C W_res: bf16 path B^T [batch, m, r]; f32 path B [batch, r, m] */
+  DYRA_BUF_B = 4,      /* B = C W_res, [batch, r, m] (bf16 / fp32)                          */
   DYRA_BUF_R = 5       /* f32 path only: R = G^-1 B, [batch, r, m] fp32                    */
 } dyra_buffer;
 

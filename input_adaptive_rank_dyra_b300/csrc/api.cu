@@ -131,7 +131,7 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
 // same buffers, so a steady-state forward costs only its launches on the host.
 
 struct Step {
-  enum Kind { GEMM, CHOL, NS_PREP, NS_FINISH, FORK, JOIN } kind = GEMM;
+  enum Kind { GEMM, CHOL_APPLY, NS_PREP, NS_FINISH, FORK, JOIN } kind = GEMM;
   bool aux = false;   // runs on the auxiliary stream
   dyra::TcGemmParams p;
   CUtensorMap a0, a1, b0, b1, out;
@@ -140,8 +140,10 @@ struct Step {
   const float *Xf = nullptr;
   int *flags = nullptr;
   __nv_bfloat16 *Ginv = nullptr;
+  __nv_bfloat16 *T = nullptr;
   int *status = nullptr;
-  int batch = 0, r = 0;
+  int batch = 0, r = 0, n = 0, ldT = 0, l0 = 0;
+  long long sTb = 0;
   float ridge = 0.f;
 };
 
@@ -149,12 +151,20 @@ struct Plan {
   std::vector<Step> steps;
 };
 
-// Records an event pair around each kernel, on the stream that kernel runs on.
+// Records an event pair around each kernel, on the stream that kernel runs on. Under stream
+// capture the records become event-record nodes of the graph (external records), so the
+// graph's replays time the kernels too.
 struct Recorder {
   cudaEvent_t *ev = nullptr;
   int max = 0, count = 0;
   void mark(cudaStream_t s) {
-    if (ev && count < max) cudaEventRecord(ev[count], s);
+    if (ev && count < max) {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev[count], s, cudaEventRecordExternal);
+      else
+        cudaEventRecord(ev[count], s);
+    }
     ++count;
   }
 };
@@ -210,6 +220,27 @@ Step gemm_step(const dyra::TcGemmParams &p, const CUtensorMap &a0, const CUtenso
 
 // ------------------------------------------------------------------------ bf16 low-rank path
 
+// N width of a GEMM tile (multiple of `q`, <= 256) for an M x N output on a persistent grid
+// of one CTA per SM: fewest rounds of tiles, weighed by a tile's main-loop time (which grows
+// with its width plus a fixed per-chunk issue cost).
+int pick_bn(long long M, int N, int q) {
+  int best = 256, sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  double best_cost = 1e300;
+  for (int bn = 256; bn >= 64; bn -= q) {
+    if (bn % q) continue;
+    const long long tiles = cdiv(M, 128) * cdiv(N, bn);
+    const double cost = (double)cdiv(tiles, sms) * (bn + 96);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
 dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int n, void *Y,
                               uint8_t *ws, const WsLayout &w, Plan &plan) {
   using namespace dyra;
@@ -219,7 +250,7 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
   __nv_bfloat16 *C = reinterpret_cast<__nv_bfloat16 *>(ws + w.C);
   float *G = reinterpret_cast<float *>(ws + w.G);
   __nv_bfloat16 *Ginv = reinterpret_cast<__nv_bfloat16 *>(ws + w.Ginv);
-  __nv_bfloat16 *Bt = reinterpret_cast<__nv_bfloat16 *>(ws + w.B);
+  __nv_bfloat16 *Bm = reinterpret_cast<__nv_bfloat16 *>(ws + w.B);
 
   // 1. T = X [U | P]
   {
@@ -240,7 +271,7 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     p.a_split = p.m_tiles;
     p.a_batched0 = 1;
     p.b_split = p.k_chunks;
-    p.idesc = tc_idesc(2, 0, 0, BN);
+    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
     p.epi = EPI_ROW_BF16;
     p.tma_store = 1;
     p.out_batched = 1;
@@ -289,16 +320,21 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     f.kind = Step::FORK;
     plan.steps.push_back(f);
   }
-  // 4. G^-1 (auxiliary stream)
+  // 4-5. G^-1 and L~ = L G^-1 over the L columns of T (auxiliary stream)
   if (L->solver == DYRA_SOLVE_CHOLESKY) {
     Step st;
-    st.kind = Step::CHOL;
+    st.kind = Step::CHOL_APPLY;
     st.aux = true;
     st.G = G;
     st.batch = batch;
     st.r = r;
     st.ridge = (float)L->ridge;
     st.Ginv = Ginv;
+    st.T = T;
+    st.n = n;
+    st.ldT = ldT;
+    st.l0 = kp;
+    st.sTb = (long long)n * ldT;
     st.status = status;
     plan.steps.push_back(st);
   } else {
@@ -377,51 +413,53 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     st.Ginv = Ginv;
     st.status = status;
     plan.steps.push_back(st);
+    // L~ = L G^-1, in place over the L columns of T (auxiliary stream)
+    {
+      CUtensorMap a, b, o;
+      const int BN = roundup(r, 16);
+      DY_MAP(make_map(&a, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 128));
+      DY_MAP(make_map(&b, Ginv, 2, r, r, batch, r, (long long)r * r, BN));
+      TcGemmParams p = base_params();
+      p.m_tiles = (int)cdiv(n, 128);
+      p.n_tiles = 1;
+      p.batch = batch;
+      p.BN = BN;
+      p.k_chunks = (int)cdiv(r, 64);
+      p.elem_bytes = 2;
+      p.a_split = p.m_tiles;
+      p.a_batched0 = 1;
+      p.b_split = p.k_chunks;
+      p.b_batched0 = 1;
+      p.idesc = tc_idesc(2, 0, 0, BN);
+      p.epi = EPI_ROW_BF16;
+      p.rows_valid = n;
+      p.cols_valid = r;
+      p.timeouts = status + 1;
+      if (BN % 32 == 0) {
+        DY_MAP(make_store_map(&o, T + kp, r, n, batch, ldT, (long long)n * ldT));
+        p.tma_store = 1;
+        p.out_batched = 1;
+      } else {
+        o = a;
+        p.out = T + kp;
+        p.out_bstride = (long long)n * ldT;
+        p.out_ld = ldT;
+      }
+      Step st = gemm_step(p, a, a, b, b, true);
+      st.out = o;
+      plan.steps.push_back(st);
+    }
   }
-  // 5. L~ = L G^-1, in place over the L columns of T (auxiliary stream)
+  // 3. B = C W_res, row-major [batch * r, m] (main stream, beside the solve)
   {
     CUtensorMap a, b, o;
-    const int BN = roundup(r, 16);
-    DY_MAP(make_map(&a, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 128));
-    DY_MAP(make_map(&b, Ginv, 2, r, r, batch, r, (long long)r * r, BN));
-    TcGemmParams p = base_params();
-    p.m_tiles = (int)cdiv(n, 128);
-    p.n_tiles = 1;
-    p.batch = batch;
-    p.BN = BN;
-    p.k_chunks = (int)cdiv(r, 64);
-    p.elem_bytes = 2;
-    p.a_split = p.m_tiles;
-    p.a_batched0 = 1;
-    p.b_split = p.k_chunks;
-    p.b_batched0 = 1;
-    p.idesc = tc_idesc(2, 0, 0, BN);
-    p.epi = EPI_ROW_BF16;
-    p.rows_valid = n;
-    p.cols_valid = r;
-    p.timeouts = status + 1;
-    if (BN % 32 == 0) {
-      DY_MAP(make_store_map(&o, T + kp, r, n, batch, ldT, (long long)n * ldT));
-      p.tma_store = 1;
-      p.out_batched = 1;
-    } else {
-      o = a;
-      p.out = T + kp;
-      p.out_bstride = (long long)n * ldT;
-      p.out_ld = ldT;
-    }
-    Step st = gemm_step(p, a, a, b, b, true);
-    st.out = o;
-    plan.steps.push_back(st);
-  }
-  // 3. B = C W_res, written as B^T [batch, m, r] (main stream, beside the solve)
-  {
-    CUtensorMap a, b;
-    const int BN = 256;
-    DY_MAP(make_map(&a, C, 2, d, (long long)batch * r, 1, d, 0, 128));
+    const long long rows = (long long)batch * r;
+    const int BN = pick_bn(rows, m, 32);
+    DY_MAP(make_map(&a, C, 2, d, rows, 1, d, 0, 128));
     DY_MAP(make_map(&b, L->wres, 2, d, m, 1, d, 0, BN));
+    DY_MAP(make_store_map(&o, Bm, m, rows, 1, m, 0));
     TcGemmParams p = base_params();
-    p.m_tiles = (int)cdiv((long long)batch * r, 128);
+    p.m_tiles = (int)cdiv(rows, 128);
     p.n_tiles = (int)cdiv(m, BN);
     p.batch = 1;
     p.BN = BN;
@@ -429,29 +467,28 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     p.elem_bytes = 2;
     p.a_split = p.m_tiles;
     p.b_split = p.k_chunks;
-    p.idesc = tc_idesc(2, 0, 0, BN);
-    p.epi = EPI_TRANS_BF16;
-    p.out = Bt;
-    p.out_bstride = 0;
-    p.rb = r;
-    p.out_gstride = (long long)m * r;
-    p.out_ld = r;
-    p.rows_valid = batch * r;
+    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    p.epi = EPI_ROW_BF16;
+    p.tma_store = 1;
+    p.rows_valid = (int)rows;
     p.cols_valid = m;
     p.timeouts = status + 1;
-    plan.steps.push_back(gemm_step(p, a, a, b, b));
+    Step st = gemm_step(p, a, a, b, b);
+    st.out = o;
+    plan.steps.push_back(st);
   }
   {
     Step j;
     j.kind = Step::JOIN;
     plan.steps.push_back(j);
   }
-  // 6. Y = [X U | L~] [V ; B] + b
+  // 6. Y = [X U | L~] [V ; B] + b: K chunks of V^T (K-major, shared by all samples), then
+  //    the sample's B (MN-major, [r, m] with m contiguous)
   {
     CUtensorMap a, b0, b1, o;
-    const int BN = 256;
+    const int BN = pick_bn((long long)batch * cdiv(n, 128) * 128, m, 64);
     DY_MAP(make_map(&a, T, 2, ldT, n, batch, ldT, (long long)n * ldT, 128));
-    DY_MAP(make_map(&b1, Bt, 2, r, m, batch, r, (long long)m * r, BN));
+    DY_MAP(make_map(&b1, Bm, 2, m, r, batch, m, (long long)r * m, 64));
     if (kp > 0)
       DY_MAP(make_map(&b0, L->v, 2, kp, m, 1, kp, 0, BN));
     else
@@ -469,7 +506,9 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     p.a_batched0 = 1;
     p.b_batched0 = 0;
     p.b_batched1 = 1;
+    p.b_major1 = 1;
     p.idesc = tc_idesc(2, 0, 0, BN);
+    p.idesc1 = tc_idesc(2, 0, 1, BN);
     p.epi = EPI_ROW_BF16;
     p.tma_store = 1;
     p.out_batched = 1;
@@ -509,8 +548,9 @@ dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream
       case Step::GEMM:
         DY_TIMED(rec, ks, tc_gemm_launch(st.p, st.a0, st.a1, st.b0, st.b1, st.out, ks));
         break;
-      case Step::CHOL:
-        DY_TIMED(rec, ks, launch_chol_inverse(st.G, st.batch, st.r, st.ridge, st.Ginv, st.status, ks));
+      case Step::CHOL_APPLY:
+        DY_TIMED(rec, ks, launch_chol_apply(st.G, st.batch, st.r, st.ridge, st.T, st.n, st.ldT, st.l0,
+                                            st.sTb, st.Ginv, st.status, ks));
         break;
       case Step::NS_PREP:
         DY_TIMED(rec, ks,
@@ -570,7 +610,7 @@ dyra_status forward_f32(const dyra_layer *L, const float *X, int batch, int n, f
   return DYRA_OK;
 }
 
-const char *const kNamesBf16[] = {"xproj_static_L", "cg_c_gram", "chol_inverse", "lsolve_apply",
+const char *const kNamesChol[] = {"xproj_static_L", "cg_c_gram", "chol_solve_apply",
                                   "residual_product", "fused_output"};
 const char *const kNamesF32[] = {"f32_xproj", "f32_gram_f64", "f32_c", "f32_b",
                                  "f32_inverse_f64", "f32_apply_inverse", "f32_static_out",
@@ -578,20 +618,21 @@ const char *const kNamesF32[] = {"f32_xproj", "f32_gram_f64", "f32_c", "f32_b",
 
 int kernels_per_forward(const dyra_layer *L) {
   if (L->dtype == DYRA_F32) return 8;
-  if (L->solver == DYRA_SOLVE_CHOLESKY) return 6;
+  if (L->solver == DYRA_SOLVE_CHOLESKY) return 5;
   return 7 + 2 * L->ns_iters;
 }
 
 const char *kernel_name(const dyra_layer *L, int i) {
   if (i < 0 || i >= kernels_per_forward(L)) return nullptr;
   if (L->dtype == DYRA_F32) return kNamesF32[i];
-  if (L->solver == DYRA_SOLVE_CHOLESKY) return kNamesBf16[i];
+  if (L->solver == DYRA_SOLVE_CHOLESKY) return kNamesChol[i];
   const int it2 = 2 * L->ns_iters;
-  if (i < 2) return kNamesBf16[i];
+  if (i < 2) return kNamesChol[i];
   if (i == 2) return "ns_prep";
   if (i < 3 + it2) return ((i - 3) % 2 == 0) ? "ns_gemm_gx" : "ns_gemm_update";
   if (i == 3 + it2) return "ns_finish";
-  return kNamesBf16[i - it2 - 1];   // lsolve_apply, residual_product, fused_output
+  if (i == 4 + it2) return "lsolve_apply";
+  return kNamesChol[i - it2 - 2];   // residual_product, fused_output
 }
 
 dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, void *Y,
@@ -1051,7 +1092,7 @@ dyra_status dyra_workspace_tensor(const dyra_layer *L, int batch, int n, int whi
     case DYRA_BUF_C: off = w.C; l = L->d; break;
     case DYRA_BUF_G: off = w.G; l = L->r; break;
     case DYRA_BUF_GINV: off = w.Ginv; l = L->r; break;
-    case DYRA_BUF_B: off = w.B; l = bf ? L->r : L->m; break;
+    case DYRA_BUF_B: off = w.B; l = L->m; break;
     case DYRA_BUF_R: if (bf) return DYRA_ERR_UNSUPPORTED; off = w.R; l = L->m; break;
     default: return DYRA_ERR_INVALID_ARG;
   }

@@ -6,8 +6,11 @@
 namespace dyra {
 
 // bf16 path, SPD solves (solve.cu)
-cudaError_t launch_chol_inverse(const float *G, int batch, int r, float ridge, __nv_bfloat16 *Ginv,
-                                int *status, cudaStream_t s);
+// (G + ridge I)^-1 for r <= 64, and L~ = L (G + ridge I)^-1 written over the L columns
+// [l0, l0 + r) of T [batch][n][ldT] (batch stride sTb elements); G^-1 also to Ginv (bf16).
+cudaError_t launch_chol_apply(const float *G, int batch, int r, float ridge, __nv_bfloat16 *T,
+                              int n, int ldT, int l0, long long sTb, __nv_bfloat16 *Ginv,
+                              int *status, cudaStream_t s);
 cudaError_t launch_ns_prep(const float *G, int batch, int r, float ridge, float *Gh, float *X0,
                            float *dinv, int *flags, cudaStream_t s);
 cudaError_t launch_ns_finish(const float *X, const float *dinv, int batch, int r, const int *flags,

@@ -1,18 +1,23 @@
 // Per-sample SPD solves of the one-step ALS R-update, R = (L^T L + lambda I)^-1 (L^T X) W_res
 // ("DyRA" summary page, 2.2 ridge; 2.4: Cholesky for small r, Newton-Schulz for larger r).
 //
-// The bf16 forward needs (G + lambda I)^-1 explicitly (bf16), which a tensor-core GEMM then
-// applies to L (L G^-1). These kernels produce it from G = L^T L (fp32):
-//   * r <= 64: Cholesky G = Lc Lc^T, W = Lc^-1, G^-1 = W^T W, all in fp32, one CTA of 256
-//     threads per sample. The r x r matrix is padded to 64 x 64 with the identity; each
-//     thread keeps 16 entries (row tid/4, columns tid%4 + 4k) in registers, and every
-//     elimination step publishes one column (or row) through shared memory behind a single
-//     barrier, so a step costs one barrier and 16 register FMAs.
+// The bf16 forward never forms R: since L R = (L G^-1) B with B = (L^T X) W_res, it rewrites
+// the L columns of T as L~ = L G^-1 and lets the output GEMM multiply L~ by B. These kernels
+// produce G^-1 from G = L^T L (fp32) and, for small r, apply it:
+//   * r <= 64 (the Cholesky branch): chol_apply. Every CTA takes one sample and a block of
+//     128 of its token rows. It inverts G + lambda I in place by Gauss-Jordan elimination
+//     without pivoting -- for an SPD matrix the pivots are the successive Schur complements,
+//     i.e. the squared diagonal of its Cholesky factor, so this is the Cholesky solve
+//     organised as one elimination step per column -- with the r x r matrix padded to R x R
+//     by the identity and held in registers (256 threads, R*R/256 entries each), one barrier
+//     per step. It then multiplies its rows of L by the inverse (fp32 FMA) and writes L~
+//     over them in T. CTAs of the first row block also store G^-1 (bf16).
 //   * larger r: Newton-Schulz. ns_prep scales G symmetrically to unit diagonal and sets
 //     X0 = I / ||G_hat||_inf; the iterations X <- X (2I - G_hat X) run as tf32 tensor-core
-//     GEMMs (tc_gemm); ns_finish undoes the scaling.
-// A sample whose pivot is not positive (or not finite) is counted in status[0] and gets
-// G^-1 = 0, so its correction vanishes and its output is the static branch plus bias.
+//     GEMMs (tc_gemm); ns_finish undoes the scaling; a bf16 tensor-core GEMM applies the
+//     result to L.
+// A sample with a pivot that is not positive (or not finite) is counted in status[0] and
+// gets G^-1 = 0, so its correction vanishes and its output is the static branch plus bias.
 #include "kernels.cuh"
 
 #include <cuda_bf16.h>
@@ -21,99 +26,137 @@ namespace dyra {
 
 namespace {
 
-constexpr int kCholMax = 64;
+constexpr int kApplyRows = 128;   // token rows per chol_apply CTA
 
+template <int R>
 __global__ void __launch_bounds__(256)
-    chol_inverse_kernel(const float *__restrict__ G, int r, float ridge,
-                        __nv_bfloat16 *__restrict__ Ginv, int *status) {
-  __shared__ float Lm[kCholMax][kCholMax + 1];   // Cholesky factor, later W = Lc^-1
-  __shared__ float cbuf[2][kCholMax];            // column j of the trailing matrix
-  __shared__ float rbuf[2][kCholMax];            // row j of W
-  __shared__ int bad;
-  const int tid = threadIdx.x, b = blockIdx.x;
-  const int i = tid >> 2, p = tid & 3;           // row i, columns p + 4k
+    chol_apply_kernel(const float *__restrict__ G, int r, float ridge, __nv_bfloat16 *T, int n,
+                      int ldT, int l0, long long sTb, __nv_bfloat16 *__restrict__ Ginv,
+                      int *status) {
+  constexpr int TPR = 256 / R;   // threads per matrix row
+  constexpr int E = R / TPR;     // entries per thread: row i, columns p + TPR * e
+  __shared__ float rowk[2][R];   // row k of the matrix before step k
+  __shared__ float colk[2][R];   // column k of the matrix before step k
+  __shared__ __align__(16) float Gi[R][R];
+  const int tid = threadIdx.x, b = blockIdx.y;
+  const int i = tid / TPR, p = tid % TPR;
   const float *g = G + (size_t)b * r * r;
-  float a[16];
+  float a[E];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const int c = p + 4 * k;
-    a[k] = (i < r && c < r) ? g[i * r + c] + (i == c ? ridge : 0.f) : (i == c ? 1.f : 0.f);
-    Lm[i][c] = (i == c && i >= r) ? 1.f : 0.f;
+  for (int e = 0; e < E; ++e) {
+    const int c = p + TPR * e;
+    a[e] = (i < r && c < r) ? g[i * r + c] + (i == c ? ridge : 0.f) : (i == c ? 1.f : 0.f);
   }
-  if (tid == 0) bad = 0;
-  if (p == 0) cbuf[0][i] = a[0];
+  if (i == 0) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) rowk[0][p + TPR * e] = a[e];
+  }
+  if (p == 0) colk[0][i] = a[0];
   __syncthreads();
-  bool mybad = false;
-  // ---- Cholesky, right-looking on the unscaled trailing matrix (pivot d_j = A_jj)
-  for (int j = 0; j < r; ++j) {
-    const float *cb = cbuf[j & 1];
-    float d = cb[j];
-    if (!(d > 0.f) || !isfinite(d)) {
-      mybad = true;
-      d = 1.f;
+  bool bad = false;
+  for (int k = 0; k < r; ++k) {
+    const float *rk = rowk[k & 1];
+    const float piv = rk[k];
+    if (!(piv > 0.f) || !isfinite(piv)) bad = true;   // same decision in every thread
+    const float inv = bad ? 0.f : __frcp_rn(piv);
+    const float f = colk[k & 1][i] * inv;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int c = p + TPR * e;
+      if (i == k)
+        a[e] = (c == k) ? inv : a[e] * inv;
+      else
+        a[e] = (c == k) ? -f : fmaf(-f, rk[c], a[e]);
     }
-    const float li = cb[i];
-    if (p == 0 && i >= j) Lm[i][j] = li * rsqrtf(d);
-    if (i > j) {
-      const float s = li / d;
+    const int kn = k + 1;
+    if (kn < r) {
+      if (i == kn) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (p + 4 * k > j) a[k] -= s * cb[p + 4 * k];
-    }
-    const int jn = j + 1;
-    if (jn < r && p == (jn & 3)) {
-      float v = 0.f;
+        for (int e = 0; e < E; ++e) rowk[kn & 1][p + TPR * e] = a[e];
+      }
+      if (p == kn % TPR) {
+        float v = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (k == (jn >> 2)) v = a[k];
-      cbuf[jn & 1][i] = v;
-    }
-    __syncthreads();
-  }
-  // ---- W = Lc^-1 by right-looking forward substitution on the identity
-  float w[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) w[k] = (i == p + 4 * k) ? 1.f : 0.f;
-  for (int j = 0; j < r; ++j) {
-    if (i == j) {
-      const float inv = 1.f / Lm[j][j];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        w[k] *= inv;
-        rbuf[j & 1][p + 4 * k] = w[k];
+        for (int e = 0; e < E; ++e)
+          if (e == kn / TPR) v = a[e];
+        colk[kn & 1][i] = v;
       }
     }
     __syncthreads();
-    if (i > j) {
-      const float lij = Lm[i][j];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) w[k] -= lij * rbuf[j & 1][p + 4 * k];
-    }
   }
-  __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 16; ++k) Lm[i][p + 4 * k] = w[k];
-  if (mybad) atomicOr(&bad, 1);
-  __syncthreads();
-  // ---- G^-1 = W^T W (W lower triangular: rows t >= i contribute)
-  if (i < r) {
-    float s[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) s[k] = 0.f;
-    for (int t = i; t < r; ++t) {
-      const float wa = Lm[t][i];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) s[k] += wa * Lm[t][p + 4 * k];
-    }
+  for (int e = 0; e < E; ++e) {
+    const int c = p + TPR * e;
+    const float v = (bad || !isfinite(a[e])) ? 0.f : a[e];
+    Gi[i][c] = (i < r && c < r) ? v : 0.f;
+  }
+  if (blockIdx.x == 0 && i < r) {
     __nv_bfloat16 *out = Ginv + (size_t)b * r * r + (size_t)i * r;
-    const bool zero = bad != 0;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int c = p + 4 * k;
-      if (c < r) out[c] = __float2bfloat16_rn((zero || !isfinite(s[k])) ? 0.f : s[k]);
+    for (int e = 0; e < E; ++e) {
+      const int c = p + TPR * e;
+      if (c < r) out[c] = __float2bfloat16_rn(bad ? 0.f : a[e]);
     }
   }
-  if (tid == 0 && bad) atomicAdd(status, 1);
+  if (blockIdx.x == 0 && tid == 0 && bad) atomicAdd(status, 1);
+  __syncthreads();
+  // L~ = L G^-1 for this CTA's rows: two threads per row, each producing R/2 columns
+  const int row = blockIdx.x * kApplyRows + (tid >> 1);
+  const int half = tid & 1;
+  const bool active = row < n;   // the same for both threads of a pair
+  __nv_bfloat16 *Lrow = T + (size_t)b * sTb + (size_t)(active ? row : 0) * ldT + l0;
+  constexpr int H = R / 2;
+  float acc[H];
+#pragma unroll
+  for (int c = 0; c < H; ++c) acc[c] = 0.f;
+  if (active) {
+    float x[R];
+#pragma unroll
+    for (int k = 0; k < R; k += 8) {
+      if (k < r) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(Lrow + k);
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&w);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f2 = __bfloat1622float2(h[j]);
+          x[k + 2 * j] = f2.x;
+          x[k + 2 * j + 1] = f2.y;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[k + j] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      const float4 *gk = reinterpret_cast<const float4 *>(&Gi[k][half * H]);
+#pragma unroll
+      for (int c4 = 0; c4 < H / 4; ++c4) {
+        const float4 gg = gk[c4];
+        acc[4 * c4 + 0] = fmaf(x[k], gg.x, acc[4 * c4 + 0]);
+        acc[4 * c4 + 1] = fmaf(x[k], gg.y, acc[4 * c4 + 1]);
+        acc[4 * c4 + 2] = fmaf(x[k], gg.z, acc[4 * c4 + 2]);
+        acc[4 * c4 + 3] = fmaf(x[k], gg.w, acc[4 * c4 + 3]);
+      }
+    }
+  }
+  // both threads of a pair (adjacent lanes) have read the whole row of L before either
+  // overwrites its half of it
+  __syncwarp();
+  if (active) {
+#pragma unroll
+    for (int c = 0; c < H; c += 8) {
+      const int col = half * H + c;
+      if (col < r) {
+        uint4 w;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          h[j] = __floats2bfloat162_rn(acc[c + 2 * j], acc[c + 2 * j + 1]);
+        *reinterpret_cast<uint4 *>(Lrow + col) = w;
+      }
+    }
+  }
 }
 
 // Jacobi scaling and start of Newton-Schulz: dinv = diag(G + lambda I)^-1/2,
@@ -185,10 +228,16 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_chol_inverse(const float *G, int batch, int r, float ridge, __nv_bfloat16 *Ginv,
-                                int *status, cudaStream_t s) {
-  if (r > kCholMax) return cudaErrorInvalidValue;
-  chol_inverse_kernel<<<batch, 256, 0, s>>>(G, r, ridge, Ginv, status);
+cudaError_t launch_chol_apply(const float *G, int batch, int r, float ridge, __nv_bfloat16 *T,
+                              int n, int ldT, int l0, long long sTb, __nv_bfloat16 *Ginv,
+                              int *status, cudaStream_t s) {
+  if (r > 64 || r % 8 || l0 % 8 || ldT % 8) return cudaErrorInvalidValue;
+  if (batch <= 0 || n <= 0) return cudaSuccess;
+  dim3 grid((n + kApplyRows - 1) / kApplyRows, batch);
+  if (r <= 32)
+    chol_apply_kernel<32><<<grid, 256, 0, s>>>(G, r, ridge, T, n, ldT, l0, sTb, Ginv, status);
+  else
+    chol_apply_kernel<64><<<grid, 256, 0, s>>>(G, r, ridge, T, n, ldT, l0, sTb, Ginv, status);
   return cudaGetLastError();
 }
 

@@ -10,27 +10,12 @@ namespace dyra {
 
 namespace {
 
-constexpr uint32_t kStagingBytesPerWarp = 2 * 2048;   // two 32 x 32 bf16 buffers
+constexpr uint32_t kStagingBytesPerWarp = 4 * 2048;   // four 32 x 32 bf16 buffers
+constexpr uint32_t kBiasBytesPerWarp = 1024;           // one fp32 bias row of <= 256 columns
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// Row of 16 fp32 values -> bf16, written with two 16-byte stores when in range and aligned.
-__device__ __forceinline__ void store_row16_bf16(__nv_bfloat16 *dst, const float *f, int valid) {
-  if (valid >= 16 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-    uint4 w0 = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                          pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-    uint4 w1 = make_uint4(pack_bf16x2(f[8], f[9]), pack_bf16x2(f[10], f[11]),
-                          pack_bf16x2(f[12], f[13]), pack_bf16x2(f[14], f[15]));
-    reinterpret_cast<uint4 *>(dst)[0] = w0;
-    reinterpret_cast<uint4 *>(dst)[1] = w1;
-  } else {
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < valid) dst[j] = __float2bfloat16_rn(f[j]);
-  }
 }
 
 struct TileCoord {
@@ -46,7 +31,8 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const TcGemmParams &p) {
   return c;
 }
 
-// Epilogue of 16 accumulator columns [col0, col0 + 16) of row g, direct global stores.
+// Epilogue of 16 accumulator columns [col0, col0 + 16) of row g, direct global stores
+// (the modes without a TMA store: C / G of the Gram kernel, fp32 Newton-Schulz products).
 __device__ __forceinline__ void epilogue16(const TcGemmParams &p, const float *f, long long g,
                                            int col0, int bz, bool second) {
   const int cols_lim = (p.epi == EPI_CG && second) ? p.cols2_valid : p.cols_valid;
@@ -54,21 +40,11 @@ __device__ __forceinline__ void epilogue16(const TcGemmParams &p, const float *f
   if (valid <= 0) return;
   if (p.epi == EPI_ROW_BF16) {
     if (g < p.rows_valid) {
-      float h[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        h[j] = f[j] + ((p.bias && j < valid) ? __ldg(p.bias + col0 + j) : 0.f);
       __nv_bfloat16 *dst =
           reinterpret_cast<__nv_bfloat16 *>(p.out) + bz * p.out_bstride + g * p.out_ld + col0;
-      store_row16_bf16(dst, h, valid);
-    }
-  } else if (p.epi == EPI_TRANS_BF16) {
-    if (g < p.rows_valid) {
-      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + bz * p.out_bstride +
-                           (g / p.rb) * p.out_gstride + (g % p.rb);
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if (j < valid) dst[(long long)(col0 + j) * p.out_ld] = __float2bfloat16_rn(f[j]);
+        if (j < valid) dst[j] = __float2bfloat16_rn(f[j] + (p.bias ? __ldg(p.bias + col0 + j) : 0.f));
     }
   } else if (p.epi == EPI_CG) {
     if (!second) {
@@ -103,7 +79,30 @@ __device__ __forceinline__ void epilogue16(const TcGemmParams &p, const float *f
   }
 }
 
-__global__ void __launch_bounds__(192, 1)
+// 32 fp32 values of one row -> bf16 into a 32 x 32 staging tile (64-byte rows, 64-byte
+// swizzle: 16-byte chunk c of row l lands at chunk c ^ ((l >> 1) & 3)).
+__device__ __forceinline__ void stage_row32(uint32_t buf, int lane, const float *f) {
+  const uint32_t dst = buf + (uint32_t)lane * 64u;
+  const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t w0 = pack_bf16x2(f[8 * c + 0], f[8 * c + 1]);
+    const uint32_t w1 = pack_bf16x2(f[8 * c + 2], f[8 * c + 3]);
+    const uint32_t w2 = pack_bf16x2(f[8 * c + 4], f[8 * c + 5]);
+    const uint32_t w3 = pack_bf16x2(f[8 * c + 6], f[8 * c + 7]);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (((uint32_t)c ^ sw) << 4)),
+                 "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                 : "memory");
+  }
+}
+
+// Warp roles. Every issuing loop runs on one lane and is a short dependent instruction chain,
+// so A and B are issued by two warps in parallel.
+constexpr int kWarpLoadA = 0, kWarpMma = 1, kWarpLoadB = 2;
+constexpr int kEpiWarp0 = 4, kEpiWarps = 8;      // warps 4..11: two per TMEM lane quarter
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+
+__global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ TcGemmParams p) {
@@ -111,12 +110,13 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw_addr);
-  const int S = p.stages;
+  const uint32_t S = (uint32_t)p.stages;
   const uint32_t a_bytes = 16384u;
   const uint32_t b_bytes = (uint32_t)p.BN * 128u;
   const uint32_t stage_bytes = a_bytes + b_bytes;
   const uint32_t staging = base + p.staging_off;
-  const uint32_t bar_base = staging + (p.tma_store ? 4u * kStagingBytesPerWarp : 0u);
+  const uint32_t bar_base =
+      base + p.bias_off + ((p.tma_store && p.bias) ? kEpiWarps * kBiasBytesPerWarp : 0u);
   // full[S] | empty[S] | tfull[2] | tempty[2] | tmem slot
   const uint32_t full_bar = bar_base, empty_bar = bar_base + 8u * S;
   const uint32_t tfull_bar = bar_base + 16u * S, tempty_bar = tfull_bar + 16u;
@@ -128,20 +128,25 @@ __global__ void __launch_bounds__(192, 1)
   const int chunk = 128 / p.elem_bytes;   // elements in one 128-byte row
   const int total = p.batch * p.m_tiles * p.n_tiles;
 
-  if (warp == 0 && lane == 0) {
-    for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(full_bar + 8u * s, 1);
+  if (warp == kWarpLoadA && lane == 0) {
+    for (uint32_t s = 0; s < S; ++s) {
+      ptx::mbar_init(full_bar + 8u * s, 2);    // the A and the B issuer
       ptx::mbar_init(empty_bar + 8u * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar + 8u * a, 1);
-      ptx::mbar_init(tempty_bar + 8u * a, 4);   // one arrival per epilogue warp
+      ptx::mbar_init(tempty_bar + 8u * a, kEpiWarps);
     }
     ptx::mbar_init_fence();
     ptx::tma_prefetch_desc(&tmA0);
-    ptx::tma_prefetch_desc(&tmB0);
+    if (p.a_split < p.m_tiles) ptx::tma_prefetch_desc(&tmA1);
+    if (p.tma_store) ptx::tma_prefetch_desc(&tmOut);
   }
-  if (warp == 1) {
+  if (warp == kWarpLoadB && lane == 0) {
+    ptx::tma_prefetch_desc(&tmB0);
+    if (p.b_split < p.k_chunks) ptx::tma_prefetch_desc(&tmB1);
+  }
+  if (warp == kWarpMma) {
     ptx::tmem_alloc(tmem_slot, 2u * p.acc_cols);
     ptx::tmem_relinquish();
   }
@@ -150,28 +155,24 @@ __global__ void __launch_bounds__(192, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_ptr;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == kWarpLoadA) {
+    // ------------------------------------------------------------ TMA producer, operand A
     if (lane == 0) {
-      uint32_t q = 0;
+      uint32_t s = 0, ph = 0, sa = base;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const TileCoord tc = decode_tile(t, p);
         const bool a_second = tc.m_tile >= p.a_split;
         const int m0 = (a_second ? tc.m_tile - p.a_split : tc.m_tile) * 128;
-        const int n0 = tc.n_tile * p.BN;
         const CUtensorMap *ma = a_second ? &tmA1 : &tmA0;
         const int a_b = (a_second ? p.a_batched1 : p.a_batched0) ? tc.bz : 0;
-        for (int kc = 0; kc < p.k_chunks; ++kc, ++q) {
-          const uint32_t s = q % (uint32_t)S;
-          const uint32_t round = q / (uint32_t)S;
-          if (!ptx::mbar_wait(empty_bar + 8u * s, (round & 1u) ^ 1u, p.timeouts)) {
+        for (int kc = 0; kc < p.k_chunks; ++kc) {
+          if (!ptx::mbar_wait(empty_bar + 8u * s, ph ^ 1u, p.timeouts)) {
             ok = false;
             break;
           }
           const uint32_t full = full_bar + 8u * s;
-          ptx::mbar_arrive_expect_tx(full, stage_bytes);
-          const uint32_t sa = base + s * stage_bytes, sb = sa + a_bytes;
+          ptx::mbar_arrive_expect_tx(full, a_bytes);
           if (p.a_major == 0) {
             ptx::tma_load_3d(sa, ma, full, kc * chunk, m0, a_b);
           } else {
@@ -179,66 +180,120 @@ __global__ void __launch_bounds__(192, 1)
               ptx::tma_load_3d(sa + (uint32_t)(i * chunk * 128), ma, full, m0 + i * chunk,
                                kc * chunk, a_b);
           }
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+            sa = base;
+          } else {
+            sa += stage_bytes;
+          }
+        }
+      }
+    }
+  } else if (warp == kWarpLoadB) {
+    // ------------------------------------------------------------ TMA producer, operand B
+    if (lane == 0) {
+      uint32_t s = 0, ph = 0, sb = base + a_bytes;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileCoord tc = decode_tile(t, p);
+        const int n0 = tc.n_tile * p.BN;
+        const int b_b0 = p.b_batched0 ? tc.bz : 0, b_b1 = p.b_batched1 ? tc.bz : 0;
+        for (int kc = 0; kc < p.k_chunks; ++kc) {
+          if (!ptx::mbar_wait(empty_bar + 8u * s, ph ^ 1u, p.timeouts)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = full_bar + 8u * s;
+          ptx::mbar_arrive_expect_tx(full, b_bytes);
           const bool b_second = kc >= p.b_split;
           const CUtensorMap *mb = b_second ? &tmB1 : &tmB0;
           const int kk = b_second ? kc - p.b_split : kc;
-          const int b_b = (b_second ? p.b_batched1 : p.b_batched0) ? tc.bz : 0;
-          if (p.b_major == 0) {
+          const int b_b = b_second ? b_b1 : b_b0;
+          if ((b_second ? p.b_major1 : p.b_major) == 0) {
             ptx::tma_load_3d(sb, mb, full, kk * chunk, n0, b_b);
           } else {
             for (int i = 0; i < p.BN / chunk; ++i)
               ptx::tma_load_3d(sb + (uint32_t)(i * chunk * 128), mb, full, n0 + i * chunk,
                                kk * chunk, b_b);
           }
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+            sb = base + a_bytes;
+          } else {
+            sb += stage_bytes;
+          }
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       // K-major SW128: rows of 128 B, 8-row groups 1024 B apart (SBO), K advance inside the row.
       // MN-major SW128: 128-byte rows hold `chunk` MN elements; MN groups LBO apart, 8-row K
       // groups 1024 B apart; one MMA consumes 32 bytes of K = 32/elem rows.
-      const uint32_t a_lbo = p.a_major ? (uint32_t)(chunk * 128) : 16u;
-      const uint32_t b_lbo = p.b_major ? (uint32_t)(chunk * 128) : 16u;
-      const uint32_t a_kstep = p.a_major ? 4096u / (uint32_t)p.elem_bytes : 32u;
-      const uint32_t b_kstep = p.b_major ? 4096u / (uint32_t)p.elem_bytes : 32u;
-      uint32_t q = 0, i = 0;
+      const uint32_t mn_lbo = (uint32_t)(chunk * 128);
+      const uint32_t mn_kstep16 = (4096u / (uint32_t)p.elem_bytes) >> 4;
+      const uint64_t a_desc0 = ptx::sdesc_sw128(base, p.a_major ? mn_lbo : 16u, 1024u);
+      const uint64_t b_desc0 = ptx::sdesc_sw128(base + a_bytes, p.b_major ? mn_lbo : 16u, 1024u);
+      const uint64_t b_desc1 = ptx::sdesc_sw128(base + a_bytes, p.b_major1 ? mn_lbo : 16u, 1024u);
+      const uint32_t a_k16 = p.a_major ? mn_kstep16 : 2u;
+      const uint32_t b_k16_0 = p.b_major ? mn_kstep16 : 2u;
+      const uint32_t b_k16_1 = p.b_major1 ? mn_kstep16 : 2u;
+      const uint32_t st16 = stage_bytes >> 4;
+      const bool f16 = p.elem_bytes == 2;
+      uint32_t s = 0, ph = 0, soff = 0, i = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
         const uint32_t acc = i & 1u;
         if (!ptx::mbar_wait(tempty_bar + 8u * acc, ((i >> 1) & 1u) ^ 1u, p.timeouts)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * p.acc_cols;
-        for (int kc = 0; kc < p.k_chunks; ++kc, ++q) {
-          const uint32_t s = q % (uint32_t)S;
-          const uint32_t round = q / (uint32_t)S;
-          if (!ptx::mbar_wait(full_bar + 8u * s, round & 1u, p.timeouts)) {
+        for (int kc = 0; kc < p.k_chunks; ++kc) {
+          if (!ptx::mbar_wait(full_bar + 8u * s, ph, p.timeouts)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = base + s * stage_bytes, sb = sa + a_bytes;
+          const bool b_second = kc >= p.b_split;
+          const uint64_t ad = a_desc0 + soff;
+          const uint64_t bd = (b_second ? b_desc1 : b_desc0) + soff;
+          const uint32_t bk = b_second ? b_k16_1 : b_k16_0;
+          const uint32_t idesc = b_second ? p.idesc1 : p.idesc;
+          if (f16) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = ptx::sdesc_sw128(sa + ks * a_kstep, a_lbo, 1024u);
-            const uint64_t bd = ptx::sdesc_sw128(sb + ks * b_kstep, b_lbo, 1024u);
-            const uint32_t accum = (kc | ks) ? 1u : 0u;
-            if (p.elem_bytes == 2)
-              ptx::tc_mma_f16(d_tmem, ad, bd, p.idesc, accum);
-            else
-              ptx::tc_mma_tf32(d_tmem, ad, bd, p.idesc, accum);
+            for (uint32_t ks = 0; ks < 4; ++ks)
+              ptx::tc_mma_f16(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (uint32_t ks = 0; ks < 4; ++ks)
+              ptx::tc_mma_tf32(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
           }
           ptx::tc_commit(empty_bar + 8u * s);   // frees the smem stage when these MMAs finish
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+            soff = 0;
+          } else {
+            soff += st16;
+          }
         }
         if (ok) ptx::tc_commit(tfull_bar + 8u * acc);   // accumulator ready
       }
     }
-  } else {
+  } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
+    const int e = warp - kEpiWarp0;
     const int q = warp & 3;   // TMEM lane quarter this warp may read
-    const uint32_t stg = staging + (uint32_t)(warp - 2) * kStagingBytesPerWarp;
-    uint32_t buf = 0, i = 0;
+    // column split of a tile between the two warps of a quarter, in 32-column units
+    const int units = p.BN / 32 + ((p.BN % 32) ? 1 : 0);
+    const int u_lo = (e < 4) ? 0 : (units + 1) / 2;
+    const int u_hi = (e < 4) ? (units + 1) / 2 : units;
+    const int c_lo = u_lo * 32, c_hi = u_hi * 32 < p.BN ? u_hi * 32 : p.BN;
+    const uint32_t stg = staging + (uint32_t)e * kStagingBytesPerWarp;
+    float *bias_w = reinterpret_cast<float *>(smem + p.bias_off + (uint32_t)e * kBiasBytesPerWarp);
+    uint32_t pair = 0, i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
       const uint32_t acc = i & 1u;
       int got = 0;
@@ -251,49 +306,59 @@ __global__ void __launch_bounds__(192, 1)
       const int m0 = (second ? tc.m_tile - p.a_split : tc.m_tile) * 128;
       const int n0 = tc.n_tile * p.BN;
       const uint32_t taddr = tmem_base + acc * p.acc_cols + ((uint32_t)(q * 32) << 16);
-      const long long g = (long long)m0 + q * 32 + lane;
       const int cols_lim = (p.epi == EPI_CG && second) ? p.cols2_valid : p.cols_valid;
       if (p.tma_store) {
-        // bf16 rows through a 64B-swizzled 32 x 32 staging tile and a TMA bulk store
+        // bf16 rows: 64 columns per step (two TMEM loads in flight), staged in a pair of
+        // 64B-swizzled 32 x 32 tiles and written by TMA; a pair is reused only after the
+        // stores that last read it have finished reading (one group of slack).
         const int row0 = m0 + q * 32;
-        for (int c0 = 0; c0 < p.BN; c0 += 32) {
+        if (p.bias) {
+          for (int j = c_lo + lane; j < c_hi; j += 32)
+            bias_w[j - c_lo] = (n0 + j < cols_lim) ? __ldg(p.bias + n0 + j) : 0.f;
+          __syncwarp();
+        }
+        for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
           const int col0 = n0 + c0;
           if (col0 >= cols_lim) break;   // uniform across the warp
-          uint32_t v[32];
-          ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+          const bool two = (c0 + 32 < c_hi) && (col0 + 32 < cols_lim);
+          uint32_t v[64];
+          ptx::tmem_ld32(taddr + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+          if (two) ptx::tmem_ld32(taddr + (uint32_t)c0 + 32u, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
           ptx::tmem_ld_wait();
           if (row0 >= p.rows_valid) continue;   // whole 32-row slab outside the tensor
-          float f[32];
+          float f[64];
+          if (p.bias) {
+            const float4 *b4 = reinterpret_cast<const float4 *>(bias_w + (c0 - c_lo));
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            f[j] = __uint_as_float(v[j]);
-            if (p.bias && col0 + j < cols_lim) f[j] += __ldg(p.bias + col0 + j);
+            for (int j = 0; j < 16; ++j) {
+              const float4 bb = b4[j];
+              f[4 * j + 0] = __uint_as_float(v[4 * j + 0]) + bb.x;
+              f[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + bb.y;
+              f[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + bb.z;
+              f[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + bb.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) f[j] = __uint_as_float(v[j]);
           }
-          if (lane == 0) ptx::bulk_wait_read<1>();   // this buffer's previous store has read it
+          if (lane == 0) ptx::bulk_wait_read<1>();   // the pair's previous stores have read it
           __syncwarp();
-          const uint32_t dst = stg + buf * 2048u + (uint32_t)lane * 64u;
-          const uint32_t sw = (uint32_t)((lane >> 1) & 3);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t w0 = pack_bf16x2(f[8 * c + 0], f[8 * c + 1]);
-            const uint32_t w1 = pack_bf16x2(f[8 * c + 2], f[8 * c + 3]);
-            const uint32_t w2 = pack_bf16x2(f[8 * c + 4], f[8 * c + 5]);
-            const uint32_t w3 = pack_bf16x2(f[8 * c + 6], f[8 * c + 7]);
-            const uint32_t addr = dst + (((uint32_t)c ^ sw) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1),
-                         "r"(w2), "r"(w3)
-                         : "memory");
-          }
+          const uint32_t buf = stg + pair * 4096u;
+          stage_row32(buf, lane, f);
+          if (two) stage_row32(buf + 2048u, lane, f + 32);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tmOut, stg + buf * 2048u, col0, row0, p.out_batched ? tc.bz : 0);
+            const int zb = p.out_batched ? tc.bz : 0;
+            ptx::tma_store_3d(&tmOut, buf, col0, row0, zb);
+            if (two) ptx::tma_store_3d(&tmOut, buf + 2048u, col0 + 32, row0, zb);
             ptx::bulk_commit();
           }
-          buf ^= 1u;
+          pair ^= 1u;
         }
       } else {
-        for (int c0 = 0; c0 < p.BN; c0 += 32) {
+        const long long g = (long long)m0 + q * 32 + lane;
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           const int col0 = n0 + c0;
           if (col0 >= cols_lim) break;   // uniform across the warp
           if (c0 + 32 <= p.BN) {
@@ -324,7 +389,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, 2u * p.acc_cols);
   }
@@ -417,26 +482,29 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
   if (p.m_tiles <= 0 || p.n_tiles <= 0 || p.batch <= 0 || p.k_chunks <= 0) return cudaSuccess;
   // MN-major tf32 operands need the 32-byte-atom 128B swizzle, which this engine does not
   // set up; every tf32 use here is K-major.
-  if (p.elem_bytes == 4 && (p.a_major || p.b_major)) return cudaErrorNotSupported;
+  if (p.elem_bytes == 4 && (p.a_major || p.b_major || p.b_major1)) return cudaErrorNotSupported;
   if (p.BN < 16 || p.BN > 256 || p.BN % 16) return cudaErrorInvalidValue;
   if (p.tma_store && (p.epi != EPI_ROW_BF16 || p.BN % 32)) return cudaErrorInvalidValue;
+  if ((p.b_major || p.b_major1) && p.BN % 64) return cudaErrorInvalidValue;
   p.acc_cols = 32;
   while (p.acc_cols < (uint32_t)p.BN) p.acc_cols <<= 1;
   const uint32_t stage = 16384u + (uint32_t)p.BN * 128u;
-  const uint32_t staging = p.tma_store ? 4u * kStagingBytesPerWarp : 0u;
-  const uint32_t fixed = 1024u + staging + 256u;   // alignment slack, staging, barriers
+  const uint32_t staging = p.tma_store ? (uint32_t)kEpiWarps * kStagingBytesPerWarp : 0u;
+  const uint32_t bias = (p.tma_store && p.bias) ? (uint32_t)kEpiWarps * kBiasBytesPerWarp : 0u;
+  const uint32_t fixed = 1024u + staging + bias + 256u;   // alignment slack, staging, bias, barriers
   int S = (int)((232448u - fixed) / stage);
   if (S > 8) S = 8;
   if (S < 2) return cudaErrorInvalidValue;
   p.stages = S;
   p.staging_off = (uint32_t)S * stage;
+  p.bias_off = p.staging_off + staging;
   uint32_t smem = (uint32_t)S * stage + fixed;
   // one CTA per SM: the two accumulators may take all 512 TMEM columns
   if (smem < 116u * 1024u) smem = 116u * 1024u;
   p.smem_bytes = smem;
   const long long total = (long long)p.batch * p.m_tiles * p.n_tiles;
   const int grid = (int)(total < num_sms() ? total : num_sms());
-  tc_gemm_kernel<<<grid, 192, smem, stream>>>(a0, a1, b0, b1, out_map, p);
+  tc_gemm_kernel<<<grid, kThreads, smem, stream>>>(a0, a1, b0, b1, out_map, p);
   return cudaGetLastError();
 }
 

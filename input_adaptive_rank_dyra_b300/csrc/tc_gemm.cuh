@@ -10,9 +10,16 @@
 //               the main loop of tile i+1
 //   warps 2..5  epilogue: tcgen05.ld of the 128 x BN accumulator (one TMEM lane quarter per
 //               warp, one row per thread), then the epilogue mode below; row-major bf16
-//               results go through a swizzled smem staging buffer and TMA bulk stores
+//               results go through swizzled smem staging buffers and TMA bulk stores
 // Operands are bf16 (kind::f16, K-major or MN-major) or fp32 read as tf32 (kind::tf32,
-// K-major only), always in the 128-byte swizzled layout that TMA writes.
+// K-major only), always in the 128-byte swizzled layout that TMA writes. The B operand
+// may switch major-ness at the K chunk b_split (e.g. a K-major weight followed by an
+// MN-major per-sample factor).
+//
+// The two issuing threads run short dependent instruction chains, so their loops keep
+// everything precomputed: shared-memory descriptors are built once and advanced by adding
+// to their address field, the ring position advances by increment and wrap, and no
+// division happens inside the K loop.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -22,7 +29,6 @@ namespace dyra {
 
 enum TcEpi : int {
   EPI_ROW_BF16 = 0,    // out[b][g][c] = bf16(acc + bias[c]); TMA store when tma_store is set
-  EPI_TRANS_BF16 = 1,  // out[b*bs + (g/rb)*gs + g%rb + c*ld] = bf16(acc)
   EPI_CG = 2,          // m tiles < a_split: out[b*bs + c*ld + g] = bf16(acc)   (C from C^T)
                        // m tiles >= a_split: out2[b*bs2 + g*ld2 + c] = acc    (G, fp32)
   EPI_ROW_F32 = 3,     // out[b][g][c] = alpha*acc + beta*aux[b][g][c]   (fp32)
@@ -39,11 +45,14 @@ struct TcGemmParams {
   int a_batched0, a_batched1;  // map carries the batch coordinate
   int b_split;       // k chunks >= b_split load from map B1 (K coordinate restarts at 0)
   int b_batched0, b_batched1;
+  int b_major1;      // major of the chunks read from map B1
   uint32_t idesc;
+  uint32_t idesc1;   // instruction descriptor of the chunks read from map B1
   uint32_t acc_cols;  // TMEM columns of one accumulator (power of two >= BN)
   int stages;
   uint32_t smem_bytes;
   uint32_t staging_off;  // byte offset of the epilogue staging buffers (TMA store)
+  uint32_t bias_off;     // byte offset of the per-warp bias rows
   // epilogue
   int epi;
   int tma_store;     // EPI_ROW_BF16 through the output tensor map (needs BN % 32 == 0)

@@ -53,35 +53,34 @@ __global__ void __launch_bounds__(256)
   }
   if (p == 0) colk[0][i] = a[0];
   __syncthreads();
+  // Branch-free elimination step: every thread computes the pivot-row and the other-row
+  // update and selects, so no warp diverges between the barriers.
   bool bad = false;
   for (int k = 0; k < r; ++k) {
-    const float *rk = rowk[k & 1];
-    const float piv = rk[k];
+    const int kb = k & 1;
+    const float piv = rowk[kb][k];
     if (!(piv > 0.f) || !isfinite(piv)) bad = true;   // same decision in every thread
     const float inv = bad ? 0.f : __frcp_rn(piv);
-    const float f = colk[k & 1][i] * inv;
+    const bool prow = (i == k);
+    const float f = prow ? 0.f : colk[kb][i] * inv;
+    float rc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) rc[e] = rowk[kb][p + TPR * e];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const int c = p + TPR * e;
-      if (i == k)
-        a[e] = (c == k) ? inv : a[e] * inv;
-      else
-        a[e] = (c == k) ? -f : fmaf(-f, rk[c], a[e]);
+      const bool pcol = (p + TPR * e == k);
+      const float v = prow ? a[e] * inv : fmaf(-f, rc[e], a[e]);
+      a[e] = pcol ? (prow ? inv : -f) : v;
     }
     const int kn = k + 1;
-    if (kn < r) {
-      if (i == kn) {
+    if (i == kn) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) rowk[kn & 1][p + TPR * e] = a[e];
-      }
-      if (p == kn % TPR) {
-        float v = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          if (e == kn / TPR) v = a[e];
-        colk[kn & 1][i] = v;
-      }
+      for (int e = 0; e < E; ++e) rowk[kn & 1][p + TPR * e] = a[e];
     }
+    float v = a[0];
+#pragma unroll
+    for (int e = 1; e < E; ++e) v = (e == kn / TPR) ? a[e] : v;
+    if (p == kn % TPR) colk[kn & 1][i] = v;
     __syncthreads();
   }
 #pragma unroll

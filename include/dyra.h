@@ -198,6 +198,29 @@ typedef enum dyra_buffer {
 dyra_status dyra_workspace_tensor(const dyra_layer *layer, int batch, int n, int which,
                                   size_t *offset_bytes, int *ld);
 
+/* Bytes of the library's static device scratch (see dyra_linear_forward_static). */
+#define DYRA_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* dyra_linear_forward for callers that cannot allocate device memory: code running inside
+ * an allocator that must not re-enter itself, a host that forbids cudaMalloc after start-up
+ * (fixed-budget serving processes), or plugins handed only input and output buffers. The
+ * pages have no counterpart of this call; it is a packaging variant of the forward.
+ * It runs the same kernels as dyra_linear_forward, with the workspace taken from a static
+ * device array of DYRA_STATIC_SCRATCH_BYTES bytes that the library image carries: every GPU
+ * that loads the library holds that array until the process exits. It calls no cudaMalloc,
+ * cudaFree or other device-allocating routine. X, Y: as in dyra_linear_forward (device,
+ * caller-owned). The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with the layer's device current); make that first call before any
+ * stream capture. All calls share the one array and it keeps the previous call's contents;
+ * the forward clears its own status words, so the layer's samples that were not positive
+ * definite are not readable afterwards through this entry point. Two calls whose work can
+ * overlap on the GPU (different streams, or different layers on one device) race on the
+ * array: serialise them. Errors: WORKSPACE (with dyra_last_error naming the sizes) when
+ * (batch, n) needs more scratch than the array holds -- dyra_workspace_size gives the need --
+ * otherwise as dyra_linear_forward. */
+dyra_status dyra_linear_forward_static(const dyra_layer *layer, const void *X, int batch, int n,
+                                       void *Y, cudaStream_t stream);
+
 const char *dyra_status_string(dyra_status status);
 /* Text of the last CUDA/driver error seen by this thread inside the library ("" if none). */
 const char *dyra_last_error(void);

@@ -941,6 +941,36 @@ dyra_status prepare_impl(const dyra_prepare_args *a, dyra_layer **out) {
 
 }  // namespace
 
+// ------------------------------------------------------------------------ static scratch
+//
+// Device scratch for dyra_linear_forward_static: a fixed array in the library's own device
+// image, so that entry point needs no allocation. Host code may not use the symbol as a
+// device address (it names a host-side stand-in); the device address is queried once per
+// device with cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) unsigned char g_static_scratch[DYRA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device (set up on first use).
+dyra_status static_scratch(int device, void **out) {
+  if (device < 0 || device >= kMaxDevices) return DYRA_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[device]) {
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(g_static_scratch)");
+    g_static_ptr[device] = ptr;
+  }
+  *out = g_static_ptr[device];
+  return DYRA_OK;
+}
+
+}  // namespace
+
 // ============================================================================ C ABI
 
 extern "C" {
@@ -1099,6 +1129,26 @@ dyra_status dyra_workspace_tensor(const dyra_layer *L, int batch, int n, int whi
   *offset_bytes = off;
   *ld = l;
   return DYRA_OK;
+}
+
+dyra_status dyra_linear_forward_static(const dyra_layer *L, const void *X, int batch, int n,
+                                       void *Y, cudaStream_t stream) {
+  if (!L || batch < 0 || n < 0) return DYRA_ERR_INVALID_ARG;
+  if (batch == 0 || n == 0) return DYRA_OK;
+  const size_t need = layout_of(L, batch, n).total;
+  if (need > (size_t)DYRA_STATIC_SCRATCH_BYTES) {
+    g_last_error = "dyra_linear_forward_static: batch " + std::to_string(batch) + " x n " +
+                   std::to_string(n) + " needs " + std::to_string(need) +
+                   " bytes of scratch, more than the static " +
+                   std::to_string((size_t)DYRA_STATIC_SCRATCH_BYTES) + " bytes";
+    return DYRA_ERR_WORKSPACE;
+  }
+  DeviceGuard guard(L->device);
+  void *ws = nullptr;
+  const dyra_status ss = static_scratch(L->device, &ws);
+  if (ss != DYRA_OK) return ss;
+  Recorder rec;
+  return forward_impl(L, X, batch, n, Y, ws, (size_t)DYRA_STATIC_SCRATCH_BYTES, stream, rec);
 }
 
 const char *dyra_status_string(dyra_status s) {

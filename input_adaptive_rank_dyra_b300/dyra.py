@@ -50,7 +50,7 @@ EXPORTED = [
     "dyra_export_factors", "dyra_workspace_size", "dyra_linear_forward",
     "dyra_linear_forward_host", "dyra_linear_forward_profiled", "dyra_kernel_name",
     "dyra_workspace_status", "dyra_workspace_tensor", "dyra_status_string", "dyra_last_error",
-    "dyra_abi_version",
+    "dyra_abi_version", "dyra_linear_forward_static",
 ]
 
 _lib = None
@@ -99,6 +99,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.dyra_last_error.argtypes = []
     lib.dyra_last_error.restype = ctypes.c_char_p
     lib.dyra_abi_version.argtypes = []
+    lib.dyra_linear_forward_static.argtypes = [vp, vp, i, i, vp, vp]
     for name in EXPORTED:   # raises AttributeError if the library lacks an entry point
         getattr(lib, name)
     if path is None:
@@ -271,6 +272,17 @@ def linear_forward(layer: Layer, X, Y=None, workspace=None, stream=None):
                                     ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                                     _stream_handle(stream))
     _check(st, "dyra_linear_forward")
+    return Y
+
+
+def linear_forward_static(layer: Layer, X, Y=None, stream=None):
+    """dyra_linear_forward_static: the forward with the library's static device scratch
+    (no workspace argument, no device allocation by the library)."""
+    Y = _check_io(layer, X, Y)
+    st = load().dyra_linear_forward_static(layer.handle, ctypes.c_void_p(X.data_ptr()),
+                                           X.shape[0], X.shape[1], ctypes.c_void_p(Y.data_ptr()),
+                                           _stream_handle(stream))
+    _check(st, "dyra_linear_forward_static")
     return Y
 
 

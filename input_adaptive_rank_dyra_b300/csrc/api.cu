@@ -188,11 +188,18 @@ bool make_store_map(CUtensorMap *map, const void *base, long long inner, long lo
   return dyra::tc_make_store_map(map, op);
 }
 
+// CTAs per cluster for every GEMM of the plan. With 2, CTA pairs share (multicast) the B
+// tile and K-major B maps are encoded with a box of BN / 2 rows. On the ViT-B fc1 layer the
+// pairs measured slightly slower than single CTAs (the kernels there are bound by the
+// epilogue's stores and launch latency, not by L2 reads of B), so single CTAs are the default.
+constexpr int kCluster = 1;
+
 dyra::TcGemmParams base_params() {
   dyra::TcGemmParams p;
   std::memset(&p, 0, sizeof(p));
   p.rb = 1 << 30;
   p.alpha = 1.f;
+  p.cluster = kCluster;
   return p;
 }
 
@@ -259,7 +266,7 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     const int nt = (int)cdiv(N, 256);
     const int BN = roundup((int)cdiv(N, nt), 32);
     DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
-    DY_MAP(make_map(&b, L->w1, 2, d, N, 1, d, 0, BN));
+    DY_MAP(make_map(&b, L->w1, 2, d, N, 1, d, 0, BN / kCluster));
     DY_MAP(make_store_map(&o, T, N, n, batch, ldT, (long long)n * ldT));
     TcGemmParams p = base_params();
     p.m_tiles = (int)cdiv(n, 128);
@@ -365,7 +372,7 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     for (int it = 0; it < L->ns_iters; ++it) {
       CUtensorMap a, b;
       DY_MAP(make_map(&a, Gh, 4, r, r, batch, r, (long long)r * r, 128));
-      DY_MAP(make_map(&b, Xa, 4, r, r, batch, r, (long long)r * r, BN));
+      DY_MAP(make_map(&b, Xa, 4, r, r, batch, r, (long long)r * r, BN / kCluster));
       TcGemmParams p = base_params();
       p.m_tiles = (int)cdiv(r, 128);
       p.n_tiles = 1;
@@ -389,7 +396,7 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
       p.timeouts = status + 1;
       plan.steps.push_back(gemm_step(p, a, a, b, b, true));   // P^T = (G_hat X)^T
       DY_MAP(make_map(&a, Xa, 4, r, r, batch, r, (long long)r * r, 128));
-      DY_MAP(make_map(&b, Pt, 4, r, r, batch, r, (long long)r * r, BN));
+      DY_MAP(make_map(&b, Pt, 4, r, r, batch, r, (long long)r * r, BN / kCluster));
       p.epi = EPI_ROW_F32;
       p.out = Xb;
       p.out_bstride = (long long)r * r;
@@ -418,7 +425,7 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
       CUtensorMap a, b, o;
       const int BN = roundup(r, 16);
       DY_MAP(make_map(&a, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 128));
-      DY_MAP(make_map(&b, Ginv, 2, r, r, batch, r, (long long)r * r, BN));
+      DY_MAP(make_map(&b, Ginv, 2, r, r, batch, r, (long long)r * r, BN / kCluster));
       TcGemmParams p = base_params();
       p.m_tiles = (int)cdiv(n, 128);
       p.n_tiles = 1;
@@ -456,7 +463,7 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     const long long rows = (long long)batch * r;
     const int BN = pick_bn(rows, m, 32);
     DY_MAP(make_map(&a, C, 2, d, rows, 1, d, 0, 128));
-    DY_MAP(make_map(&b, L->wres, 2, d, m, 1, d, 0, BN));
+    DY_MAP(make_map(&b, L->wres, 2, d, m, 1, d, 0, BN / kCluster));
     DY_MAP(make_store_map(&o, Bm, m, rows, 1, m, 0));
     TcGemmParams p = base_params();
     p.m_tiles = (int)cdiv(rows, 128);
@@ -490,7 +497,7 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     DY_MAP(make_map(&a, T, 2, ldT, n, batch, ldT, (long long)n * ldT, 128));
     DY_MAP(make_map(&b1, Bm, 2, m, r, batch, m, (long long)r * m, 64));
     if (kp > 0)
-      DY_MAP(make_map(&b0, L->v, 2, kp, m, 1, kp, 0, BN));
+      DY_MAP(make_map(&b0, L->v, 2, kp, m, 1, kp, 0, BN / kCluster));
     else
       b0 = b1;
     DY_MAP(make_store_map(&o, Y, m, n, batch, m, (long long)n * m));

@@ -4,14 +4,14 @@
 #include "ptx.cuh"
 
 #include <cuda_bf16.h>
+#include <cstring>
 #include <mutex>
 
 namespace dyra {
 
 namespace {
 
-constexpr uint32_t kStagingBytesPerWarp = 4 * 2048;   // four 32 x 32 bf16 buffers
-constexpr uint32_t kBiasBytesPerWarp = 1024;           // one fp32 bias row of <= 256 columns
+constexpr uint32_t kStagingBytesPerWarp = 4 * 2048;   // two pairs of 32 x 32 bf16 buffers
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -22,12 +22,16 @@ struct TileCoord {
   int bz, m_tile, n_tile;
 };
 
-__device__ __forceinline__ TileCoord decode_tile(int t, const TcGemmParams &p) {
+// Unit u of the persistent walk (n fastest); with cluster = 2 a unit is a pair of M tiles
+// and CTA rank `crank` of the cluster takes M tile 2 * pair + crank (possibly one past the
+// last M tile: then its loads read zeros and its epilogue stores nothing).
+__device__ __forceinline__ TileCoord decode_tile(int u, const TcGemmParams &p, int mp_tiles,
+                                                 int crank) {
   TileCoord c;
-  c.n_tile = t % p.n_tiles;
-  const int rest = t / p.n_tiles;
-  c.m_tile = rest % p.m_tiles;
-  c.bz = rest / p.m_tiles;
+  c.n_tile = u % p.n_tiles;
+  const int rest = u / p.n_tiles;
+  c.m_tile = (rest % mp_tiles) * p.cluster + crank;
+  c.bz = rest / mp_tiles;
   return c;
 }
 
@@ -107,6 +111,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ TcGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
+  // the next kernel of the stream may start launching now; it waits for this grid to finish
+  // before it reads anything (pdl_wait), so this only overlaps launch latency and set-up
+  ptx::pdl_launch_dependents();
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw_addr);
@@ -116,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t stage_bytes = a_bytes + b_bytes;
   const uint32_t staging = base + p.staging_off;
   const uint32_t bar_base =
-      base + p.bias_off + ((p.tma_store && p.bias) ? kEpiWarps * kBiasBytesPerWarp : 0u);
+      base + p.bar_off;
   // full[S] | empty[S] | tfull[2] | tempty[2] | tmem slot
   const uint32_t full_bar = bar_base, empty_bar = bar_base + 8u * S;
   const uint32_t tfull_bar = bar_base + 16u * S, tempty_bar = tfull_bar + 16u;
@@ -126,12 +133,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = 128 / p.elem_bytes;   // elements in one 128-byte row
-  const int total = p.batch * p.m_tiles * p.n_tiles;
+  const bool pair = p.cluster == 2;
+  const int crank = pair ? (int)ptx::cluster_ctarank() : 0;
+  const int cid = (int)blockIdx.x / p.cluster, ncl = (int)gridDim.x / p.cluster;
+  const int mp_tiles = (p.m_tiles + p.cluster - 1) / p.cluster;
+  const int total = p.batch * mp_tiles * p.n_tiles;
 
   if (warp == kWarpLoadA && lane == 0) {
     for (uint32_t s = 0; s < S; ++s) {
       ptx::mbar_init(full_bar + 8u * s, 2);    // the A and the B issuer
-      ptx::mbar_init(empty_bar + 8u * s, 1);
+      ptx::mbar_init(empty_bar + 8u * s, (uint32_t)p.cluster);   // the MMA of every CTA
+                                                                  // reading this stage
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar + 8u * a, 1);
@@ -152,18 +164,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // the peer's barriers must be initialised before its multicasts and commits reach them
+  if (pair) ptx::cluster_sync_all();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_ptr;
+  // set-up above overlaps the previous kernel; its outputs are read only after this
+  ptx::pdl_wait();
 
   if (warp == kWarpLoadA) {
     // ------------------------------------------------------------ TMA producer, operand A
     if (lane == 0) {
       uint32_t s = 0, ph = 0, sa = base;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileCoord tc = decode_tile(t, p);
-        const bool a_second = tc.m_tile >= p.a_split;
-        const int m0 = (a_second ? tc.m_tile - p.a_split : tc.m_tile) * 128;
+      for (int t = cid; t < total && ok; t += ncl) {
+        const TileCoord tc = decode_tile(t, p, mp_tiles, crank);
+        // a pair's tile past the last M tile reads rows past the end of map A0 (zeros)
+        const bool phantom = tc.m_tile >= p.m_tiles;
+        const bool a_second = !phantom && tc.m_tile >= p.a_split;
+        const int m0 = phantom ? p.a_split * 128 : (a_second ? tc.m_tile - p.a_split : tc.m_tile) * 128;
         const CUtensorMap *ma = a_second ? &tmA1 : &tmA0;
         const int a_b = (a_second ? p.a_batched1 : p.a_batched0) ? tc.bz : 0;
         for (int kc = 0; kc < p.k_chunks; ++kc) {
@@ -195,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t s = 0, ph = 0, sb = base + a_bytes;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileCoord tc = decode_tile(t, p);
+      for (int t = cid; t < total && ok; t += ncl) {
+        const TileCoord tc = decode_tile(t, p, mp_tiles, crank);
         const int n0 = tc.n_tile * p.BN;
         const int b_b0 = p.b_batched0 ? tc.bz : 0, b_b1 = p.b_batched1 ? tc.bz : 0;
         for (int kc = 0; kc < p.k_chunks; ++kc) {
@@ -210,12 +228,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap *mb = b_second ? &tmB1 : &tmB0;
           const int kk = b_second ? kc - p.b_split : kc;
           const int b_b = b_second ? b_b1 : b_b0;
-          if ((b_second ? p.b_major1 : p.b_major) == 0) {
-            ptx::tma_load_3d(sb, mb, full, kk * chunk, n0, b_b);
+          if (!pair) {
+            if ((b_second ? p.b_major1 : p.b_major) == 0) {
+              ptx::tma_load_3d(sb, mb, full, kk * chunk, n0, b_b);
+            } else {
+              for (int i = 0; i < p.BN / chunk; ++i)
+                ptx::tma_load_3d(sb + (uint32_t)(i * chunk * 128), mb, full, n0 + i * chunk,
+                                 kk * chunk, b_b);
+            }
+          } else if ((b_second ? p.b_major1 : p.b_major) == 0) {
+            // this CTA's half of the B rows, into both CTAs of the pair
+            const int half = p.BN / 2;
+            ptx::tma_load_3d_mc(sb + (uint32_t)(crank * half * 128), mb, full, kk * chunk,
+                                n0 + crank * half, b_b, (uint16_t)3);
           } else {
-            for (int i = 0; i < p.BN / chunk; ++i)
-              ptx::tma_load_3d(sb + (uint32_t)(i * chunk * 128), mb, full, n0 + i * chunk,
-                               kk * chunk, b_b);
+            for (int i = crank; i < p.BN / chunk; i += 2)
+              ptx::tma_load_3d_mc(sb + (uint32_t)(i * chunk * 128), mb, full, n0 + i * chunk,
+                                  kk * chunk, b_b, (uint16_t)3);
           }
           if (++s == S) {
             s = 0;
@@ -245,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool f16 = p.elem_bytes == 2;
       uint32_t s = 0, ph = 0, soff = 0, i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+      for (int t = cid; t < total && ok; t += ncl, ++i) {
         const uint32_t acc = i & 1u;
         if (!ptx::mbar_wait(tempty_bar + 8u * acc, ((i >> 1) & 1u) ^ 1u, p.timeouts)) break;
         ptx::tc_fence_after();
@@ -270,7 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t ks = 0; ks < 4; ++ks)
               ptx::tc_mma_tf32(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
           }
-          ptx::tc_commit(empty_bar + 8u * s);   // frees the smem stage when these MMAs finish
+          // frees the smem stage (in both CTAs of a pair) when these MMAs finish
+          if (pair)
+            ptx::tc_commit_mc(empty_bar + 8u * s, (uint16_t)3);
+          else
+            ptx::tc_commit(empty_bar + 8u * s);
           if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -292,31 +325,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int u_hi = (e < 4) ? (units + 1) / 2 : units;
     const int c_lo = u_lo * 32, c_hi = u_hi * 32 < p.BN ? u_hi * 32 : p.BN;
     const uint32_t stg = staging + (uint32_t)e * kStagingBytesPerWarp;
-    float *bias_w = reinterpret_cast<float *>(smem + p.bias_off + (uint32_t)e * kBiasBytesPerWarp);
-    uint32_t pair = 0, i = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+    uint32_t buf_i = 0, i = 0;
+    for (int t = cid; t < total; t += ncl, ++i) {
       const uint32_t acc = i & 1u;
       int got = 0;
       if (lane == 0) got = ptx::mbar_wait(tfull_bar + 8u * acc, (i >> 1) & 1u, p.timeouts) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       ptx::tc_fence_after();
-      const TileCoord tc = decode_tile(t, p);
+      const TileCoord tc = decode_tile(t, p, mp_tiles, crank);
+      if (tc.m_tile >= p.m_tiles) {   // a pair's tile past the last M tile: nothing to store
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty_bar + 8u * acc);
+        continue;
+      }
       const bool second = tc.m_tile >= p.a_split;
       const int m0 = (second ? tc.m_tile - p.a_split : tc.m_tile) * 128;
       const int n0 = tc.n_tile * p.BN;
       const uint32_t taddr = tmem_base + acc * p.acc_cols + ((uint32_t)(q * 32) << 16);
       const int cols_lim = (p.epi == EPI_CG && second) ? p.cols2_valid : p.cols_valid;
       if (p.tma_store) {
-        // bf16 rows: 64 columns per step (two TMEM loads in flight), staged in a pair of
-        // 64B-swizzled 32 x 32 tiles and written by TMA; a pair is reused only after the
-        // stores that last read it have finished reading (one group of slack).
+        // bf16 rows, 64 columns per step: two TMEM loads in flight, (+ bias), two 64B-swizzled
+        // 32 x 32 staging tiles, two TMA stores in one bulk group. The warp alternates two
+        // pairs of staging tiles and reuses a pair only after the group that last read it has
+        // finished reading.
         const int row0 = m0 + q * 32;
-        if (p.bias) {
-          for (int j = c_lo + lane; j < c_hi; j += 32)
-            bias_w[j - c_lo] = (n0 + j < cols_lim) ? __ldg(p.bias + n0 + j) : 0.f;
-          __syncwarp();
-        }
         for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
           const int col0 = n0 + c0;
           if (col0 >= cols_lim) break;   // uniform across the warp
@@ -327,11 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld_wait();
           if (row0 >= p.rows_valid) continue;   // whole 32-row slab outside the tensor
           float f[64];
-          if (p.bias) {
-            const float4 *b4 = reinterpret_cast<const float4 *>(bias_w + (c0 - c_lo));
+          if (p.bias && col0 + 64 <= cols_lim) {
+            // every lane reads the same 256 bytes: a broadcast from L1
+            const float4 *b4 = reinterpret_cast<const float4 *>(p.bias + col0);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float4 bb = b4[j];
+              const float4 bb = __ldg(b4 + j);
               f[4 * j + 0] = __uint_as_float(v[4 * j + 0]) + bb.x;
               f[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + bb.y;
               f[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + bb.z;
@@ -339,11 +374,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) f[j] = __uint_as_float(v[j]);
+            for (int j = 0; j < 64; ++j)
+              f[j] = __uint_as_float(v[j]) +
+                     ((p.bias && col0 + j < cols_lim) ? __ldg(p.bias + col0 + j) : 0.f);
           }
-          if (lane == 0) ptx::bulk_wait_read<1>();   // the pair's previous stores have read it
+          if (lane == 0) ptx::bulk_wait_read<1>();   // this pair's previous stores have read it
           __syncwarp();
-          const uint32_t buf = stg + pair * 4096u;
+          const uint32_t buf = stg + buf_i * 4096u;
           stage_row32(buf, lane, f);
           if (two) stage_row32(buf + 2048u, lane, f + 32);
           ptx::fence_proxy_async_smem();
@@ -354,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (two) ptx::tma_store_3d(&tmOut, buf + 2048u, col0 + 32, row0, zb);
             ptx::bulk_commit();
           }
-          pair ^= 1u;
+          buf_i ^= 1u;
         }
       } else {
         const long long g = (long long)m0 + q * 32 + lane;
@@ -389,6 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair leaves while the other may still write its shared memory or
+  // arrive on its barriers
+  if (pair) ptx::cluster_sync_all();
   if (warp == kWarpMma) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, 2u * p.acc_cols);
@@ -490,21 +530,49 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
   while (p.acc_cols < (uint32_t)p.BN) p.acc_cols <<= 1;
   const uint32_t stage = 16384u + (uint32_t)p.BN * 128u;
   const uint32_t staging = p.tma_store ? (uint32_t)kEpiWarps * kStagingBytesPerWarp : 0u;
-  const uint32_t bias = (p.tma_store && p.bias) ? (uint32_t)kEpiWarps * kBiasBytesPerWarp : 0u;
-  const uint32_t fixed = 1024u + staging + bias + 256u;   // alignment slack, staging, bias, barriers
+  const uint32_t fixed = 1024u + staging + 256u;   // alignment slack, staging, barriers
   int S = (int)((232448u - fixed) / stage);
   if (S > 8) S = 8;
   if (S < 2) return cudaErrorInvalidValue;
   p.stages = S;
   p.staging_off = (uint32_t)S * stage;
-  p.bias_off = p.staging_off + staging;
+  p.bar_off = p.staging_off + staging;   // barriers follow the staging buffers
   uint32_t smem = (uint32_t)S * stage + fixed;
   // one CTA per SM: the two accumulators may take all 512 TMEM columns
   if (smem < 116u * 1024u) smem = 116u * 1024u;
   p.smem_bytes = smem;
-  const long long total = (long long)p.batch * p.m_tiles * p.n_tiles;
-  const int grid = (int)(total < num_sms() ? total : num_sms());
-  tc_gemm_kernel<<<grid, kThreads, smem, stream>>>(a0, a1, b0, b1, out_map, p);
+  if (p.cluster != 2) p.cluster = 1;
+  const long long units =
+      (long long)p.batch * ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
+  // programmatic stream serialization: this grid may launch while the previous kernel of
+  // the stream finishes (the kernel waits for it with pdl_wait before reading)
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.cluster == 1) {
+    cfg.gridDim = dim3((unsigned)(units < num_sms() ? units : num_sms()), 1, 1);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, a0, a1, b0, b1, out_map, p);
+  }
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.numAttrs = 2;
+  int max_clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, tc_gemm_kernel, &cfg) != cudaSuccess ||
+      max_clusters <= 0)
+    max_clusters = num_sms() / 2;
+  const long long clusters = units < max_clusters ? units : max_clusters;
+  cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel, a0, a1, b0, b1, out_map, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -2,7 +2,10 @@
 // stored K-contiguous ("K-major") or MN-contiguous, fp32 accumulation in TMEM.
 //
 // Persistent kernel: a grid of at most one CTA per SM walks the tiles (batch, m tile,
-// n tile), n fastest, in a static round-robin. Each CTA has six warps:
+// n tile), n fastest, in a static round-robin. With cluster = 2 the unit of that walk is a
+// pair of M tiles handled by the two CTAs of a cluster, which share the B tile: each loads
+// half of it and multicasts it to both, which halves the L2 reads of B. Each CTA has
+// these warps:
 //   warp 0      TMA producer (one lane): 128-byte K chunks of A (128 rows) and B (BN rows)
 //               into a ring of smem stages; it runs ahead across tile boundaries
 //   warp 1      TMEM allocation and MMA issue (one lane): 4 MMAs (32 bytes of K each) per
@@ -37,6 +40,9 @@ enum TcEpi : int {
 
 struct TcGemmParams {
   int m_tiles, n_tiles, batch;
+  int cluster;       // 1, or 2: CTA pairs take adjacent M tiles of one (batch, N tile) and
+                     // each loads half of the B tile, multicast to both (K-major B maps then
+                     // need a box of BN / 2 rows)
   int BN;            // MMA N of a tile: multiple of 16 (of 64 for MN-major B), <= 256
   int k_chunks;      // K in 128-byte chunks
   int elem_bytes;    // 2 = bf16, 4 = fp32/tf32
@@ -52,7 +58,7 @@ struct TcGemmParams {
   int stages;
   uint32_t smem_bytes;
   uint32_t staging_off;  // byte offset of the epilogue staging buffers (TMA store)
-  uint32_t bias_off;     // byte offset of the per-warp bias rows
+  uint32_t bar_off;      // byte offset of the mbarriers (after the staging buffers)
   // epilogue
   int epi;
   int tma_store;     // EPI_ROW_BF16 through the output tensor map (needs BN % 32 == 0)

@@ -83,6 +83,16 @@ def kernel_work(cfg, name: str):
     (bf16 = 2 B; G fp32)."""
     B, n, d, m, k, r = cfg.batch, cfg.n, cfg.d, cfg.m, cfg.k, cfg.r
     e = 2
+    if cfg.kind == "monarch":   # k = number of blocks; Z = X BD1 has nb * nb = d columns
+        if name == "monarch_bd1":
+            return 2.0 * B * n * d * k, e * (2 * B * n * d + d * k)
+        if name == "xproj_L":
+            return 2.0 * B * n * d * r, e * (B * n * d + d * r + B * n * r)
+        if name == "monarch_permute":
+            return 0.0, e * 2 * B * n * d
+        if name == "fused_output":
+            return (2.0 * B * n * m * (k + r),
+                    e * (B * n * (d + r) + m * k + B * r * m + B * n * m) + 4 * m)
     if name == "xproj_static_L":
         return 2.0 * B * n * d * (k + r), e * (B * n * d + (k + r) * d + B * n * (k + r))
     if name == "cg_c_gram":
@@ -101,7 +111,8 @@ def kernel_work(cfg, name: str):
 
 
 def layer_flops(cfg):
-    """Algorithmic FLOPs of the whole one-step DyRA forward (per batch)."""
+    """Algorithmic FLOPs of the whole one-step DyRA forward (per batch). Monarch: two
+    block-diagonal factors of nb blocks (2 n d nb + 2 n m nb)."""
     B, n, d, m, k, r = cfg.batch, cfg.n, cfg.d, cfg.m, cfg.k, cfg.r
     static = 2.0 * n * (d * k + k * m)
     dyn = 2.0 * n * d * r + 2.0 * n * r * r + 2.0 * n * r * d + 2.0 * r * d * m + 2.0 * n * r * m
@@ -110,6 +121,11 @@ def layer_flops(cfg):
 
 def layer_bytes(cfg):
     B, n, d, m, k, r = cfg.batch, cfg.n, cfg.d, cfg.m, cfg.k, cfg.r
+    if cfg.kind == "monarch":
+        weights = 2 * (d * k + k * m + d * r + d * m) + 4 * m
+        acts = 2 * (B * n * d + B * n * m)
+        inter = 2 * (3 * B * n * (d + r) + 2 * B * r * d + 2 * B * r * m) + 4 * B * r * r
+        return weights + acts + inter
     weights = 2 * (d * (k + r) + k * m + d * m) + 4 * m
     acts = 2 * (B * n * d + B * n * m)
     inter = 2 * (2 * B * n * (k + r) + 2 * B * r * d + 2 * B * r * m) + 4 * B * r * r

@@ -39,9 +39,12 @@ struct dyra_layer {
   double ridge = 0.0;
   int device = 0;
   std::vector<double> W_hat, W_res, P, R0, F1, F2, bias;
-  // device copies; bf16: w1 = [U^T (padded to kp rows); P^T] [kp + r, d], v = V^T [m, kp],
-  // wres = W_res^T [m, d]; f32: w1 = [U | P] [d, k + r], v = V [k, m], wres = W_res [d, m]
-  void *w1 = nullptr, *v = nullptr, *wres = nullptr;
+  // device copies. kp = the static columns of T: roundup(k, 64) (low rank) or d (Monarch).
+  // bf16 low rank: w1 = [U^T (padded to kp rows); P^T] [kp + r, d], v = V^T [m, kp];
+  // bf16 Monarch: w1 = P^T [r, d], bd1 / bd2 = the block-diagonal factors as K-major tiles
+  // [d][256] / [m][256] (row = output column, K local to the output's 256-column tile);
+  // wres = W_res^T [m, d] (bf16); f32: w1 = [U | P] [d, k + r], v = V [k, m], wres = W_res [d, m]
+  void *w1 = nullptr, *v = nullptr, *wres = nullptr, *bd1 = nullptr, *bd2 = nullptr;
   float *bias_d = nullptr;
   cudaStream_t aux = nullptr;            // stream of the SPD-solve branch
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -131,7 +134,7 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
 // same buffers, so a steady-state forward costs only its launches on the host.
 
 struct Step {
-  enum Kind { GEMM, CHOL_APPLY, NS_PREP, NS_FINISH, FORK, JOIN } kind = GEMM;
+  enum Kind { GEMM, CHOL_APPLY, NS_PREP, NS_FINISH, PERMUTE, FORK, JOIN } kind = GEMM;
   bool aux = false;   // runs on the auxiliary stream
   dyra::TcGemmParams p;
   CUtensorMap a0, a1, b0, b1, out;
@@ -142,8 +145,8 @@ struct Step {
   __nv_bfloat16 *Ginv = nullptr;
   __nv_bfloat16 *T = nullptr;
   int *status = nullptr;
-  int batch = 0, r = 0, n = 0, ldT = 0, l0 = 0;
-  long long sTb = 0;
+  int batch = 0, r = 0, n = 0, ldT = 0, l0 = 0, nb = 0;
+  long long sTb = 0, rows = 0;
   float ridge = 0.f;
 };
 
@@ -200,6 +203,7 @@ dyra::TcGemmParams base_params() {
   p.rb = 1 << 30;
   p.alpha = 1.f;
   p.cluster = kCluster;
+  p.a_k1 = -1;
   return p;
 }
 
@@ -248,8 +252,90 @@ int pick_bn(long long M, int N, int q) {
   return best;
 }
 
-dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int n, void *Y,
-                              uint8_t *ws, const WsLayout &w, Plan &plan) {
+// Monarch static branch, front half: T[:, 0:d] = the permuted X BD1, T[:, d:d+r] = L = X P.
+dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, int n,
+                               __nv_bfloat16 *T, int ldT, int *status, Plan &plan) {
+  using namespace dyra;
+  const int d = L->d, r = L->r, nb = L->k;
+  // Z = X BD1: 256-column tiles, each contracting with its own 256 input columns
+  {
+    CUtensorMap a, b, o;
+    const int BN = 256;
+    DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
+    DY_MAP(make_map(&b, L->bd1, 2, 256, d, 1, 256, 0, BN / kCluster));
+    DY_MAP(make_store_map(&o, T, d, n, batch, ldT, (long long)n * ldT));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(n, 128);
+    p.n_tiles = d / BN;
+    p.batch = batch;
+    p.BN = BN;
+    p.k_chunks = BN / 64;
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.a_batched0 = 1;
+    p.a_kdiag = 1;
+    p.b_split = p.k_chunks;
+    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    p.epi = EPI_ROW_BF16;
+    p.tma_store = 1;
+    p.out_batched = 1;
+    p.rows_valid = n;
+    p.cols_valid = d;
+    p.timeouts = status + 1;
+    Step st = gemm_step(p, a, a, b, b);
+    st.out = o;
+    plan.steps.push_back(st);
+  }
+  // L = X P into T[:, d:d+r]
+  {
+    CUtensorMap a, b, o;
+    const int BN = roundup(r, 16);
+    DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
+    DY_MAP(make_map(&b, L->w1, 2, d, r, 1, d, 0, BN / kCluster));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(n, 128);
+    p.n_tiles = 1;
+    p.batch = batch;
+    p.BN = BN;
+    p.k_chunks = (int)cdiv(d, 64);
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.a_batched0 = 1;
+    p.b_split = p.k_chunks;
+    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    p.epi = EPI_ROW_BF16;
+    p.rows_valid = n;
+    p.cols_valid = r;
+    p.timeouts = status + 1;
+    if (BN % 32 == 0) {
+      DY_MAP(make_store_map(&o, T + d, r, n, batch, ldT, (long long)n * ldT));
+      p.tma_store = 1;
+      p.out_batched = 1;
+    } else {
+      o = a;
+      p.out = T + d;
+      p.out_bstride = (long long)n * ldT;
+      p.out_ld = ldT;
+    }
+    Step st = gemm_step(p, a, a, b, b);
+    st.out = o;
+    plan.steps.push_back(st);
+  }
+  // the stride permutation between the two factors, in place
+  {
+    Step st;
+    st.kind = Step::PERMUTE;
+    st.T = T;
+    st.rows = (long long)batch * n;
+    st.ldT = ldT;
+    st.nb = nb;
+    plan.steps.push_back(st);
+  }
+  return DYRA_OK;
+}
+
+dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void *Y,
+                      uint8_t *ws, const WsLayout &w, Plan &plan) {
   using namespace dyra;
   const int d = L->d, m = L->m, r = L->r, kp = L->kp, ldT = w.ldT;
   int *status = reinterpret_cast<int *>(ws);
@@ -259,8 +345,11 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
   __nv_bfloat16 *Ginv = reinterpret_cast<__nv_bfloat16 *>(ws + w.Ginv);
   __nv_bfloat16 *Bm = reinterpret_cast<__nv_bfloat16 *>(ws + w.B);
 
-  // 1. T = X [U | P]
-  {
+  // 1. T = X [U | P]   (Monarch: permuted X BD1 and L)
+  if (L->kind == DYRA_STATIC_MONARCH) {
+    const dyra_status fs = plan_monarch_front(L, X, batch, n, T, ldT, status, plan);
+    if (fs != DYRA_OK) return fs;
+  } else {
     CUtensorMap a, b, o;
     const int N = ldT;
     const int nt = (int)cdiv(N, 256);
@@ -490,7 +579,44 @@ dyra_status plan_bf16_lowrank(const dyra_layer *L, const void *X, int batch, int
     plan.steps.push_back(j);
   }
   // 6. Y = [X U | L~] [V ; B] + b: K chunks of V^T (K-major, shared by all samples), then
-  //    the sample's B (MN-major, [r, m] with m contiguous)
+  //    the sample's B (MN-major, [r, m] with m contiguous). Monarch: the first chunks are
+  //    Zp BD2 on 256-column tiles (each contracting with its own 256 columns of Zp).
+  if (L->kind == DYRA_STATIC_MONARCH) {
+    CUtensorMap a, b0, b1, o;
+    const int BN = 256;
+    DY_MAP(make_map(&a, T, 2, ldT, n, batch, ldT, (long long)n * ldT, 128));
+    DY_MAP(make_map(&b1, Bm, 2, m, r, batch, m, (long long)r * m, 64));
+    DY_MAP(make_map(&b0, L->bd2, 2, 256, m, 1, 256, 0, BN / kCluster));
+    DY_MAP(make_store_map(&o, Y, m, n, batch, m, (long long)n * m));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(n, 128);
+    p.n_tiles = m / BN;
+    p.batch = batch;
+    p.BN = BN;
+    p.b_split = BN / 64;
+    p.k_chunks = p.b_split + (int)cdiv(r, 64);
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.a_batched0 = 1;
+    p.a_kdiag = 1;
+    p.a_k1 = kp;
+    p.b_batched0 = 0;
+    p.b_batched1 = 1;
+    p.b_major1 = 1;
+    p.idesc = tc_idesc(2, 0, 0, BN);
+    p.idesc1 = tc_idesc(2, 0, 1, BN);
+    p.epi = EPI_ROW_BF16;
+    p.tma_store = 1;
+    p.out_batched = 1;
+    p.rows_valid = n;
+    p.cols_valid = m;
+    p.bias = L->bias_d;
+    p.timeouts = status + 1;
+    Step st = gemm_step(p, a, a, b0, b1);
+    st.out = o;
+    plan.steps.push_back(st);
+    return DYRA_OK;
+  }
   {
     CUtensorMap a, b0, b1, o;
     const int BN = pick_bn((long long)batch * cdiv(n, 128) * 128, m, 64);
@@ -563,6 +689,9 @@ dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream
         DY_TIMED(rec, ks,
                  launch_ns_prep(st.G, st.batch, st.r, st.ridge, st.Gh, st.X0, st.dinv, st.flags, ks));
         break;
+      case Step::PERMUTE:
+        DY_TIMED(rec, ks, launch_monarch_permute(st.T, st.rows, st.ldT, st.nb, ks));
+        break;
       case Step::NS_FINISH:
         DY_TIMED(rec, ks,
                  launch_ns_finish(st.Xf, st.dinv, st.batch, st.r, st.flags, st.Ginv, st.status, ks));
@@ -619,19 +748,24 @@ dyra_status forward_f32(const dyra_layer *L, const float *X, int batch, int n, f
 
 const char *const kNamesChol[] = {"xproj_static_L", "cg_c_gram", "chol_solve_apply",
                                   "residual_product", "fused_output"};
+const char *const kNamesMonarchFront[] = {"monarch_bd1", "xproj_L", "monarch_permute"};
 const char *const kNamesF32[] = {"f32_xproj", "f32_gram_f64", "f32_c", "f32_b",
                                  "f32_inverse_f64", "f32_apply_inverse", "f32_static_out",
                                  "f32_correction_out"};
 
 int kernels_per_forward(const dyra_layer *L) {
   if (L->dtype == DYRA_F32) return 8;
-  if (L->solver == DYRA_SOLVE_CHOLESKY) return 5;
-  return 7 + 2 * L->ns_iters;
+  const int front = L->kind == DYRA_STATIC_MONARCH ? 3 : 1;
+  if (L->solver == DYRA_SOLVE_CHOLESKY) return front + 4;
+  return front + 6 + 2 * L->ns_iters;
 }
 
 const char *kernel_name(const dyra_layer *L, int i) {
   if (i < 0 || i >= kernels_per_forward(L)) return nullptr;
   if (L->dtype == DYRA_F32) return kNamesF32[i];
+  const int front = L->kind == DYRA_STATIC_MONARCH ? 3 : 1;
+  if (i < front) return L->kind == DYRA_STATIC_MONARCH ? kNamesMonarchFront[i] : kNamesChol[0];
+  i -= front - 1;   // now indexes the low-rank list from "cg_c_gram" (= 1) on
   if (L->solver == DYRA_SOLVE_CHOLESKY) return kNamesChol[i];
   const int it2 = 2 * L->ns_iters;
   if (i < 2) return kNamesChol[i];
@@ -668,7 +802,7 @@ dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, v
     if (kv.first == key) plan = std::static_pointer_cast<Plan>(kv.second);
   if (!plan) {
     plan = std::make_shared<Plan>();
-    dyra_status ps = plan_bf16_lowrank(L, X, batch, n, Y, ws, w, *plan);
+    dyra_status ps = plan_bf16(L, X, batch, n, Y, ws, w, *plan);
     if (ps != DYRA_OK) return ps;
     if (L->plans.size() >= 64) L->plans.erase(L->plans.begin());
     L->plans.emplace_back(key, plan);
@@ -699,11 +833,13 @@ void free_device(dyra_layer *L) {
   if (L->w1) cudaFree(L->w1);
   if (L->v) cudaFree(L->v);
   if (L->wres) cudaFree(L->wres);
+  if (L->bd1) cudaFree(L->bd1);
+  if (L->bd2) cudaFree(L->bd2);
   if (L->bias_d) cudaFree(L->bias_d);
   if (L->ev_fork) cudaEventDestroy(L->ev_fork);
   if (L->ev_join) cudaEventDestroy(L->ev_join);
   if (L->aux) cudaStreamDestroy(L->aux);
-  L->w1 = L->v = L->wres = nullptr;
+  L->w1 = L->v = L->wres = L->bd1 = L->bd2 = nullptr;
   L->bias_d = nullptr;
   L->ev_fork = L->ev_join = nullptr;
   L->aux = nullptr;
@@ -858,7 +994,7 @@ dyra_layer *new_layer(const dyra_prepare_args *a, dyra_solver solver, int ns_ite
   dyra_layer *L = new (std::nothrow) dyra_layer();
   if (!L) return nullptr;
   L->d = a->d; L->m = a->m; L->k = a->k; L->r = a->r;
-  L->kp = (a->kind == DYRA_STATIC_LOWRANK) ? roundup(a->k, 64) : 0;
+  L->kp = (a->kind == DYRA_STATIC_LOWRANK) ? roundup(a->k, 64) : a->d;
   L->kind = a->kind; L->dtype = a->dtype; L->solver = solver; L->ns_iters = ns_iters;
   L->ridge = a->ridge; L->device = a->device;
   return L;
@@ -868,7 +1004,36 @@ dyra_status upload_layer(const dyra_prepare_args *a, dyra_layer *L) {
   const int d = L->d, m = L->m, k = L->k, r = L->r;
   dyra_status st = DYRA_OK;
   std::vector<float> bias32(L->bias.begin(), L->bias.end());
-  if (a->dtype == DYRA_BF16) {
+  if (a->dtype == DYRA_BF16 && L->kind == DYRA_STATIC_MONARCH) {
+    const int nb = k, T0 = 256;
+    std::vector<double> pt((size_t)r * d), b1((size_t)d * T0, 0.0), b2((size_t)m * T0, 0.0),
+        wrt((size_t)m * d);
+    for (int j = 0; j < r; ++j)
+      for (int i = 0; i < d; ++i) pt[(size_t)j * d + i] = L->P[(size_t)i * r + j];
+    // Z[:, a*nb + c] = sum_i X[:, a*nb + i] B1[a][i][c]
+    for (int n = 0; n < d; ++n) {
+      const int a_ = n / nb, c = n % nb, n0 = n / T0 * T0;
+      for (int i = 0; i < nb; ++i)
+        b1[(size_t)n * T0 + (a_ * nb + i - n0)] = L->F1[((size_t)a_ * nb + i) * nb + c];
+    }
+    // Y[:, c*nb + j] = sum_a Zp[:, c*nb + a] B2[c][a][j]
+    for (int o = 0; o < m; ++o) {
+      const int c = o / nb, j = o % nb, n0 = o / T0 * T0;
+      for (int a_ = 0; a_ < nb; ++a_)
+        b2[(size_t)o * T0 + (c * nb + a_ - n0)] = L->F2[((size_t)c * nb + a_) * nb + j];
+    }
+    for (int i = 0; i < d; ++i)
+      for (int j = 0; j < m; ++j) wrt[(size_t)j * d + i] = L->W_res[(size_t)i * m + j];
+    std::vector<__nv_bfloat16> h;
+    to_bf16(pt.data(), pt.size(), h);
+    if (st == DYRA_OK) st = upload(&L->w1, h);
+    to_bf16(b1.data(), b1.size(), h);
+    if (st == DYRA_OK) st = upload(&L->bd1, h);
+    to_bf16(b2.data(), b2.size(), h);
+    if (st == DYRA_OK) st = upload(&L->bd2, h);
+    to_bf16(wrt.data(), wrt.size(), h);
+    if (st == DYRA_OK) st = upload(&L->wres, h);
+  } else if (a->dtype == DYRA_BF16) {
     const int kp = L->kp, N1 = kp + r;
     std::vector<double> w1((size_t)N1 * d, 0.0), vt((size_t)m * std::max(kp, 1), 0.0),
         wrt((size_t)m * d);
@@ -887,12 +1052,6 @@ dyra_status upload_layer(const dyra_prepare_args *a, dyra_layer *L) {
     if (st == DYRA_OK) st = upload(&L->v, h);
     to_bf16(wrt.data(), wrt.size(), h);
     if (st == DYRA_OK) st = upload(&L->wres, h);
-    if (st == DYRA_OK) {
-      cudaError_t e = cudaStreamCreateWithFlags(&L->aux, cudaStreamNonBlocking);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming);
-      if (e != cudaSuccess) st = cuda_fail(e, "auxiliary stream / events");
-    }
   } else {
     const int N1 = k + r;
     std::vector<float> wc((size_t)d * N1), vv((size_t)std::max(k, 1) * m, 0.f), wr((size_t)d * m);
@@ -905,6 +1064,12 @@ dyra_status upload_layer(const dyra_prepare_args *a, dyra_layer *L) {
     if (st == DYRA_OK) st = upload(&L->w1, wc);
     if (st == DYRA_OK) st = upload(&L->v, vv);
     if (st == DYRA_OK) st = upload(&L->wres, wr);
+  }
+  if (a->dtype == DYRA_BF16 && st == DYRA_OK) {
+    cudaError_t e = cudaStreamCreateWithFlags(&L->aux, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming);
+    if (e != cudaSuccess) st = cuda_fail(e, "auxiliary stream / events");
   }
   if (st == DYRA_OK) {
     void *bp = nullptr;

@@ -184,6 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = phantom ? p.a_split * 128 : (a_second ? tc.m_tile - p.a_split : tc.m_tile) * 128;
         const CUtensorMap *ma = a_second ? &tmA1 : &tmA0;
         const int a_b = (a_second ? p.a_batched1 : p.a_batched0) ? tc.bz : 0;
+        const int a_k0 = p.a_kdiag ? tc.n_tile * p.BN : 0;
+        const int a_k1 = p.a_k1 >= 0 ? p.a_k1 : p.b_split * chunk;
         for (int kc = 0; kc < p.k_chunks; ++kc) {
           if (!ptx::mbar_wait(empty_bar + 8u * s, ph ^ 1u, p.timeouts)) {
             ok = false;
@@ -192,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full = full_bar + 8u * s;
           ptx::mbar_arrive_expect_tx(full, a_bytes);
           if (p.a_major == 0) {
-            ptx::tma_load_3d(sa, ma, full, kc * chunk, m0, a_b);
+            const int ka = kc < p.b_split ? a_k0 + kc * chunk : a_k1 + (kc - p.b_split) * chunk;
+            ptx::tma_load_3d(sa, ma, full, ka, m0, a_b);
           } else {
             for (int i = 0; i < 128 / chunk; ++i)
               ptx::tma_load_3d(sa + (uint32_t)(i * chunk * 128), ma, full, m0 + i * chunk,
@@ -546,9 +549,8 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
       (long long)p.batch * ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
   // programmatic stream serialization: this grid may launch while the previous kernel of
   // the stream finishes (the kernel waits for it with pdl_wait before reading)
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2] = {};
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -52,6 +52,11 @@ struct TcGemmParams {
   int b_split;       // k chunks >= b_split load from map B1 (K coordinate restarts at 0)
   int b_batched0, b_batched1;
   int b_major1;      // major of the chunks read from map B1
+  int a_kdiag;       // 1: K-major A chunks < b_split are read at K = n0 + kc * chunk, where n0
+                     // is the tile's first output column (block-diagonal B: an N tile only
+                     // contracts with the same range of K)
+  int a_k1;          // K coordinate of A (elements) read by chunk b_split; later chunks follow
+                     // it. < 0: contiguous with the chunks before (b_split * chunk)
   uint32_t idesc;
   uint32_t idesc1;   // instruction descriptor of the chunks read from map B1
   uint32_t acc_cols;  // TMEM columns of one accumulator (power of two >= BN)

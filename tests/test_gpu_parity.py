@@ -53,7 +53,7 @@ def _check_forward(cfg, X, W, b, prep, layer, Y, ridge=0.0):
 # ---------------------------------------------------------------------------- reduced sizes
 
 REDUCED = [("c1", None, None), ("c2", 3, None), ("c2", 2, 61), ("c3_fc1", 2, None),
-           ("c3_fc2", 2, 300), ("c5", 1, 1100)]
+           ("c3_fc2", 2, 300), ("c4", 2, None), ("c4", 3, 130), ("c5", 1, 1100)]
 
 
 @pytest.mark.parametrize("name,batch,n", REDUCED)
@@ -68,12 +68,13 @@ def test_forward_matches_oracle(name, batch, n):
     assert dy.workspace_status(layer, ws) == (0, 0)
 
 
-@pytest.mark.parametrize("name", ["c1", "c2"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c4"])
 def test_intermediates_match_oracle(name):
     """Each kernel's output in the workspace: [XU | L] (or L G^-1), G, C, G^-1, B."""
     import torch
     import input_adaptive_rank_dyra_b300 as dy
-    cfg = WL.reduced(WL.get_config(name), batch=2 if name == "c2" else None)
+    cfg = WL.reduced(WL.get_config(name), batch=None if name == "c1" else 2,
+                     n=300 if name == "c4" else None)
     W, b, prep = weights_and_prep(name)
     X = WL.make_inputs(cfg)
     layer = make_layer(cfg, prep, W, b)
@@ -85,8 +86,16 @@ def test_intermediates_match_oracle(name):
     ft = torch.bfloat16 if bf else torch.float32
     _, ldT = layer.workspace_tensor(B_, n, "T")
     T = to_host(dy.workspace_view(layer, ws, B_, n, "T", (B_, n, ldT), ft))
-    XU = X @ prep["F1"]
-    assert rel(T[:, :, :k], XU) <= t
+    if cfg.kind == "monarch":
+        # the static columns hold Zp[:, c*nb + a] = (X BD1)[:, a*nb + c]
+        nb = k
+        B1 = prep["F1"]
+        Z = np.einsum("bnai,aic->bnac", X.reshape(B_, n, nb, d // nb), B1)
+        assert rel(T[:, :, :d], Z.transpose(0, 1, 3, 2).reshape(B_, n, d)) <= t
+        k = d
+    else:
+        XU = X @ prep["F1"]
+        assert rel(T[:, :, :k], XU) <= t
     Lo = np.stack(inter["L"])
     Go = np.stack(inter["G"])
     Gi_o = np.linalg.inv(Go)
@@ -241,7 +250,7 @@ def test_library_fit_end_to_end():
 
 # ---------------------------------------------------------------------------- full sizes
 
-FULL = ["c2", "c3_fc1", "c3_fc2", "c5"]
+FULL = ["c2", "c3_fc1", "c3_fc2", "c4", "c5"]
 
 
 @pytest.mark.parametrize("name", FULL)

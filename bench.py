@@ -35,11 +35,13 @@ import workloads as WL  # noqa: E402
 METRIC = "DyRA layer tokens/s and latency vs dense cuBLAS XW; % bf16 TC peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 L2_BYTES = 126 * 1024 * 1024
-KERNEL_SOURCES = ["input_adaptive_rank_dyra_b300/csrc/tc_gemm.cu",
-                  "input_adaptive_rank_dyra_b300/csrc/tc_gemm.cuh",
-                  "input_adaptive_rank_dyra_b300/csrc/ptx.cuh",
-                  "input_adaptive_rank_dyra_b300/csrc/solve.cu",
-                  "input_adaptive_rank_dyra_b300/csrc/api.cu"]
+_CSRC = "input_adaptive_rank_dyra_b300/csrc/"
+# the source files that define each kernel of the forward (a recorded DRAM-traffic figure is
+# used only while their hash matches the one recorded with it)
+GEMM_SOURCES = [_CSRC + "tc_gemm.cu", _CSRC + "tc_gemm.cuh", _CSRC + "ptx.cuh"]
+KERNEL_SOURCES = {"chol_solve_apply": [_CSRC + "solve.cu", _CSRC + "kernels.cuh"],
+                  "ns_prep": [_CSRC + "solve.cu"], "ns_finish": [_CSRC + "solve.cu"],
+                  "monarch_permute": [_CSRC + "monarch.cu", _CSRC + "monarch.cuh"]}
 
 
 # ---------------------------------------------------------------------------- helpers
@@ -53,9 +55,9 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES.get(kernel, GEMM_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
@@ -67,7 +69,7 @@ def recorded_traffic(workload: str, kernel: str):
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    cur = kernel_source_hash()
+    cur = kernel_source_hash(kernel)
     with open(p) as f:
         for line in f:
             parts = line.split()

@@ -139,9 +139,9 @@ dyra_status dyra_workspace_size(const dyra_layer *layer, int batch, int n, size_
 /* The online step. X: device [batch, n, d], Y: device [batch, n, m], both in the layer's
  * dtype, 16-byte aligned, rows densely packed. workspace: device, >= dyra_workspace_size
  * bytes, 256-byte aligned, owned by the caller; it must not be shared by two forwards that
- * may run at the same time. Enqueues every kernel on `stream` (the bf16 path also forks
- * the SPD solve onto an internal stream of the layer and joins it back before the output
- * kernel) and returns without waiting. batch == 0 or n == 0 is a no-op. A sample whose
+ * may run at the same time. Enqueues every kernel on `stream` (on the bf16 Cholesky path
+ * the SPD solve is forked onto an internal stream of the layer, beside B = C W_res, and
+ * joined back before the output kernel) and returns without waiting. batch == 0 or n == 0 is a no-op. A sample whose
  * L^T L + lambda I is not positive definite (e.g. an all-zero sample with lambda = 0) gets
  * R = 0 -- its rows of Y are the static branch plus b -- and is counted in the status word
  * that dyra_workspace_status reads. Errors (nothing launched): INVALID_ARG, WORKSPACE, CUDA. */

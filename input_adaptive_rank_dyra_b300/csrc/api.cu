@@ -411,7 +411,11 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.timeouts = status + 1;
     plan.steps.push_back(gemm_step(p, ax, al, al, al));
   }
-  {
+  // The Cholesky branch is one kernel and runs on the auxiliary stream beside B = C W_res.
+  // The Newton-Schulz branch is a chain of small kernels: beside the persistent B GEMM they
+  // would wait for SMs, so it runs on the main stream, before it.
+  const bool fork = L->solver == DYRA_SOLVE_CHOLESKY;
+  if (fork) {
     Step f;
     f.kind = Step::FORK;
     plan.steps.push_back(f);
@@ -443,7 +447,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     {
       Step st;
       st.kind = Step::NS_PREP;
-      st.aux = true;
+      st.aux = false;
       st.G = G;
       st.batch = batch;
       st.r = r;
@@ -483,7 +487,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
       p.rows_valid = r;
       p.cols_valid = r;
       p.timeouts = status + 1;
-      plan.steps.push_back(gemm_step(p, a, a, b, b, true));   // P^T = (G_hat X)^T
+      plan.steps.push_back(gemm_step(p, a, a, b, b));   // P^T = (G_hat X)^T
       DY_MAP(make_map(&a, Xa, 4, r, r, batch, r, (long long)r * r, 128));
       DY_MAP(make_map(&b, Pt, 4, r, r, batch, r, (long long)r * r, BN / kCluster));
       p.epi = EPI_ROW_F32;
@@ -495,12 +499,12 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
       p.aux_ld = r;
       p.alpha = -1.f;
       p.beta = 2.f;
-      plan.steps.push_back(gemm_step(p, a, a, b, b, true));   // X' = 2X - X P
+      plan.steps.push_back(gemm_step(p, a, a, b, b));   // X' = 2X - X P
       std::swap(Xa, Xb);
     }
     Step st;
     st.kind = Step::NS_FINISH;
-    st.aux = true;
+    st.aux = false;
     st.Xf = Xa;
     st.dinv = dinv;
     st.batch = batch;
@@ -541,7 +545,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
         p.out_bstride = (long long)n * ldT;
         p.out_ld = ldT;
       }
-      Step st = gemm_step(p, a, a, b, b, true);
+      Step st = gemm_step(p, a, a, b, b);
       st.out = o;
       plan.steps.push_back(st);
     }
@@ -573,7 +577,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     st.out = o;
     plan.steps.push_back(st);
   }
-  {
+  if (fork) {
     Step j;
     j.kind = Step::JOIN;
     plan.steps.push_back(j);

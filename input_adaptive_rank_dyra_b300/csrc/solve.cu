@@ -5,13 +5,14 @@
 // the L columns of T as L~ = L G^-1 and lets the output GEMM multiply L~ by B. These kernels
 // produce G^-1 from G = L^T L (fp32) and, for small r, apply it:
 //   * r <= 64 (the Cholesky branch): chol_apply. Every CTA takes one sample and a block of
-//     128 of its token rows. It inverts G + lambda I in place by Gauss-Jordan elimination
-//     without pivoting -- for an SPD matrix the pivots are the successive Schur complements,
-//     i.e. the squared diagonal of its Cholesky factor, so this is the Cholesky solve
-//     organised as one elimination step per column -- with the r x r matrix padded to R x R
-//     by the identity and held in registers (256 threads, R*R/256 entries each), one barrier
-//     per step. It then multiplies its rows of L by the inverse (fp32 FMA) and writes L~
-//     over them in T. CTAs of the first row block also store G^-1 (bf16).
+//     128 of its token rows. It inverts G + lambda I in place by block Gauss-Jordan
+//     elimination without pivoting, on 8 x 8 pivot blocks -- for an SPD matrix the pivot
+//     blocks are SPD Schur complements, whose scalar pivots are the squared diagonal of the
+//     Cholesky factor, so this is the Cholesky solve organised as r / 8 block steps -- with
+//     the r x r matrix padded to R x R (R = 32 or 64) by the identity and double-buffered in
+//     shared memory. It then multiplies its rows of L (staged in shared memory) by the
+//     inverse (fp32 FMA) and writes L~ over them in T. CTAs of the first row block also
+//     store G^-1 (bf16).
 //   * larger r: Newton-Schulz. ns_prep scales G symmetrically to unit diagonal and sets
 //     X0 = I / ||G_hat||_inf; the iterations X <- X (2I - G_hat X) run as tf32 tensor-core
 //     GEMMs (tc_gemm); ns_finish undoes the scaling; a bf16 tensor-core GEMM applies the
@@ -28,132 +29,155 @@ namespace {
 
 constexpr int kApplyRows = 128;   // token rows per chol_apply CTA
 
+constexpr int kPivot = 8;       // pivot block of the block elimination
+
+// threads of chol_apply: four matrix entries per thread
 template <int R>
-__global__ void __launch_bounds__(256)
+__host__ __device__ constexpr int apply_threads() { return R * R / 4; }
+
+// In-place block Gauss-Jordan on the SPD matrix A = G + ridge I padded to R x R by the
+// identity, in shared memory. For each pivot block K (kPivot columns starting at K0):
+//   P = A[K][K]^-1 (8 x 8, SPD), RK = P A[K][:], CK = A[:][K] (before the step),
+//   A[i][c] <- A[i][c] - CK[i][:] RK[:, c]   (i, c outside K),
+//   A[i][K] <- -CK[i][:] P,  A[K][c] <- RK[:, c],  A[K][K] <- P.
+// After R / kPivot steps A holds A^-1. Warp 0 forms P (two entries per lane, exchanged by
+// shuffles) while the other threads copy CK; then every thread forms one entry of RK; then
+// every thread rewrites its own entries of A. Three barriers per step.
+template <int R>
+__global__ void __launch_bounds__(apply_threads<R>())
     chol_apply_kernel(const float *__restrict__ G, int r, float ridge, __nv_bfloat16 *T, int n,
                       int ldT, int l0, long long sTb, __nv_bfloat16 *__restrict__ Ginv,
                       int *status) {
-  constexpr int TPR = 256 / R;   // threads per matrix row
-  constexpr int E = R / TPR;     // entries per thread: row i, columns p + TPR * e
-  __shared__ float rowk[2][R];   // row k of the matrix before step k
-  __shared__ float colk[2][R];   // column k of the matrix before step k
-  __shared__ __align__(16) float Gi[R][R];
-  const int tid = threadIdx.x, b = blockIdx.y;
-  const int i = tid / TPR, p = tid % TPR;
+  constexpr int NT = apply_threads<R>();
+  constexpr int E = R * R / NT;       // matrix entries per thread (4)
+  __shared__ __align__(16) float A[R][R];
+  __shared__ __align__(16) float RK[kPivot][R];
+  __shared__ float CK[R][kPivot];
+  __shared__ float Pm[kPivot][kPivot];
+  __shared__ __align__(16) __nv_bfloat16 Ls[kApplyRows][R];   // this CTA's rows of L
+  __shared__ int bad_s;
+  const int tid = threadIdx.x, b = blockIdx.y, lane = tid & 31, warp = tid >> 5;
   const float *g = G + (size_t)b * r * r;
-  float a[E];
+  // this CTA's rows of L, staged now (every read of L happens before any write below)
+  const int row0 = blockIdx.x * kApplyRows;
+  for (int t = tid; t < kApplyRows * (R / 8); t += NT) {
+    const int rr = t / (R / 8), c8 = (t % (R / 8)) * 8;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (row0 + rr < n && c8 < r)
+      w = *reinterpret_cast<const uint4 *>(T + (size_t)b * sTb + (size_t)(row0 + rr) * ldT + l0 + c8);
+    *reinterpret_cast<uint4 *>(&Ls[rr][c8]) = w;
+  }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const int c = p + TPR * e;
-    a[e] = (i < r && c < r) ? g[i * r + c] + (i == c ? ridge : 0.f) : (i == c ? 1.f : 0.f);
+    const int idx = tid + NT * e, i = idx / R, c = idx % R;
+    A[i][c] = (i < r && c < r) ? g[i * r + c] + (i == c ? ridge : 0.f) : (i == c ? 1.f : 0.f);
   }
-  if (i == 0) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) rowk[0][p + TPR * e] = a[e];
-  }
-  if (p == 0) colk[0][i] = a[0];
+  if (tid == 0) bad_s = 0;
   __syncthreads();
-  // Branch-free elimination step: every thread computes the pivot-row and the other-row
-  // update and selects, so no warp diverges between the barriers.
-  bool bad = false;
-  for (int k = 0; k < r; ++k) {
-    const int kb = k & 1;
-    const float piv = rowk[kb][k];
-    if (!(piv > 0.f) || !isfinite(piv)) bad = true;   // same decision in every thread
-    const float inv = bad ? 0.f : __frcp_rn(piv);
-    const bool prow = (i == k);
-    const float f = prow ? 0.f : colk[kb][i] * inv;
-    float rc[E];
+  const int steps = (r + kPivot - 1) / kPivot;
+  for (int kb = 0; kb < steps; ++kb) {
+    const int K0 = kb * kPivot;
+    if (warp == 0) {
+      // P = A[K][K]^-1: lane holds (x0, y) and (x0 + 4, y), x0 = lane / 8, y = lane % 8
+      const int x0 = lane >> 3, y = lane & 7;
+      float q0 = A[K0 + x0][K0 + y], q1 = A[K0 + x0 + 4][K0 + y];
+      bool bad = false;
 #pragma unroll
-    for (int e = 0; e < E; ++e) rc[e] = rowk[kb][p + TPR * e];
+      for (int k = 0; k < kPivot; ++k) {
+        const int src = ((k & 3) << 3);   // lanes holding row k, slot k >> 2
+        const float piv = __shfl_sync(0xffffffffu, (k >> 2) ? q1 : q0, src + k);
+        const float ky = __shfl_sync(0xffffffffu, (k >> 2) ? q1 : q0, src + y);   // A[k][y]
+        const float xk0 = __shfl_sync(0xffffffffu, q0, (x0 << 3) + k);           // A[x0][k]
+        const float xk1 = __shfl_sync(0xffffffffu, q1, (x0 << 3) + k);           // A[x0+4][k]
+        if (!(piv > 0.f) || !isfinite(piv)) bad = true;
+        const float inv = bad ? 0.f : __frcp_rn(piv);
+        const float f0 = xk0 * inv, f1 = xk1 * inv;
+        const float u0 = (x0 == k) ? ((y == k) ? inv : q0 * inv) : ((y == k) ? -f0 : fmaf(-f0, ky, q0));
+        const float u1 = (x0 + 4 == k) ? ((y == k) ? inv : q1 * inv) : ((y == k) ? -f1 : fmaf(-f1, ky, q1));
+        q0 = u0;
+        q1 = u1;
+      }
+      Pm[x0][y] = q0;
+      Pm[x0 + 4][y] = q1;
+      if (bad && lane == 0) bad_s = 1;
+    }
+    // CK = A[:][K] before the step, by the warps other than warp 0
+    for (int t = tid - 32; t >= 0 && t < R * kPivot; t += NT - 32)
+      CK[t / kPivot][t % kPivot] = A[t / kPivot][K0 + t % kPivot];
+    __syncthreads();
+    // RK = P A[K][:] (one entry per thread)
+    if (tid < kPivot * R) {
+      const int x = tid / R, c = tid % R;
+      float v = 0.f;
+#pragma unroll
+      for (int yy = 0; yy < kPivot; ++yy) v = fmaf(Pm[x][yy], A[K0 + yy][c], v);
+      RK[x][c] = v;
+    }
+    __syncthreads();
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const bool pcol = (p + TPR * e == k);
-      const float v = prow ? a[e] * inv : fmaf(-f, rc[e], a[e]);
-      a[e] = pcol ? (prow ? inv : -f) : v;
-    }
-    const int kn = k + 1;
-    if (i == kn) {
+      const int idx = tid + NT * e, i = idx / R, c = idx % R;
+      const bool in_i = (unsigned)(i - K0) < (unsigned)kPivot;
+      const bool in_c = (unsigned)(c - K0) < (unsigned)kPivot;
+      float v;
+      if (in_i) {
+        v = in_c ? Pm[i - K0][c - K0] : RK[i - K0][c];
+      } else if (in_c) {
+        v = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) rowk[kn & 1][p + TPR * e] = a[e];
-    }
-    float v = a[0];
+        for (int x = 0; x < kPivot; ++x) v = fmaf(-CK[i][x], Pm[x][c - K0], v);
+      } else {
+        v = A[i][c];
 #pragma unroll
-    for (int e = 1; e < E; ++e) v = (e == kn / TPR) ? a[e] : v;
-    if (p == kn % TPR) colk[kn & 1][i] = v;
+        for (int x = 0; x < kPivot; ++x) v = fmaf(-CK[i][x], RK[x][c], v);
+      }
+      A[i][c] = v;
+    }
     __syncthreads();
   }
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int c = p + TPR * e;
-    const float v = (bad || !isfinite(a[e])) ? 0.f : a[e];
-    Gi[i][c] = (i < r && c < r) ? v : 0.f;
-  }
-  if (blockIdx.x == 0 && i < r) {
-    __nv_bfloat16 *out = Ginv + (size_t)b * r * r + (size_t)i * r;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int c = p + TPR * e;
-      if (c < r) out[c] = __float2bfloat16_rn(bad ? 0.f : a[e]);
+  const bool bad = bad_s != 0;
+  if (blockIdx.x == 0) {
+    for (int idx = tid; idx < r * r; idx += NT) {
+      const int i = idx / r, c = idx % r;
+      const float v = A[i][c];
+      Ginv[(size_t)b * r * r + idx] = __float2bfloat16_rn((bad || !isfinite(v)) ? 0.f : v);
     }
+    if (tid == 0 && bad) atomicAdd(status, 1);
   }
-  if (blockIdx.x == 0 && tid == 0 && bad) atomicAdd(status, 1);
-  __syncthreads();
-  // L~ = L G^-1 for this CTA's rows: two threads per row, each producing R/2 columns
-  const int row = blockIdx.x * kApplyRows + (tid >> 1);
-  const int half = tid & 1;
-  const bool active = row < n;   // the same for both threads of a pair
-  __nv_bfloat16 *Lrow = T + (size_t)b * sTb + (size_t)(active ? row : 0) * ldT + l0;
-  constexpr int H = R / 2;
+  // L~ = L G^-1 for this CTA's rows: TR threads per row, H columns each
+  constexpr int TR = NT / kApplyRows, H = R / TR;
+  const int rr = tid / TR, c0 = (tid % TR) * H;
+  const int row = row0 + rr;
+  if (row >= n || c0 >= r) return;
   float acc[H];
 #pragma unroll
   for (int c = 0; c < H; ++c) acc[c] = 0.f;
-  if (active) {
-    float x[R];
+  for (int k = 0; k < r; ++k) {
+    const float xk = __bfloat162float(Ls[rr][k]);
+    const float4 *gk = reinterpret_cast<const float4 *>(&A[k][c0]);
 #pragma unroll
-    for (int k = 0; k < R; k += 8) {
-      if (k < r) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(Lrow + k);
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&w);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f2 = __bfloat1622float2(h[j]);
-          x[k + 2 * j] = f2.x;
-          x[k + 2 * j + 1] = f2.y;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[k + j] = 0.f;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < R; ++k) {
-      const float4 *gk = reinterpret_cast<const float4 *>(&Gi[k][half * H]);
-#pragma unroll
-      for (int c4 = 0; c4 < H / 4; ++c4) {
-        const float4 gg = gk[c4];
-        acc[4 * c4 + 0] = fmaf(x[k], gg.x, acc[4 * c4 + 0]);
-        acc[4 * c4 + 1] = fmaf(x[k], gg.y, acc[4 * c4 + 1]);
-        acc[4 * c4 + 2] = fmaf(x[k], gg.z, acc[4 * c4 + 2]);
-        acc[4 * c4 + 3] = fmaf(x[k], gg.w, acc[4 * c4 + 3]);
-      }
+    for (int c4 = 0; c4 < H / 4; ++c4) {
+      const float4 gg = gk[c4];
+      acc[4 * c4 + 0] = fmaf(xk, gg.x, acc[4 * c4 + 0]);
+      acc[4 * c4 + 1] = fmaf(xk, gg.y, acc[4 * c4 + 1]);
+      acc[4 * c4 + 2] = fmaf(xk, gg.z, acc[4 * c4 + 2]);
+      acc[4 * c4 + 3] = fmaf(xk, gg.w, acc[4 * c4 + 3]);
     }
   }
-  // both threads of a pair (adjacent lanes) have read the whole row of L before either
-  // overwrites its half of it
-  __syncwarp();
-  if (active) {
+  if (bad) {
 #pragma unroll
-    for (int c = 0; c < H; c += 8) {
-      const int col = half * H + c;
-      if (col < r) {
-        uint4 w;
-        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+    for (int c = 0; c < H; ++c) acc[c] = 0.f;
+  }
+  __nv_bfloat16 *Lrow = T + (size_t)b * sTb + (size_t)row * ldT + l0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          h[j] = __floats2bfloat162_rn(acc[c + 2 * j], acc[c + 2 * j + 1]);
-        *reinterpret_cast<uint4 *>(Lrow + col) = w;
-      }
+  for (int c = 0; c < H; c += 8) {
+    if (c0 + c < r) {
+      uint4 w;
+      __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        h[j] = __floats2bfloat162_rn(acc[c + 2 * j], acc[c + 2 * j + 1]);
+      *reinterpret_cast<uint4 *>(Lrow + c0 + c) = w;
     }
   }
 }
@@ -234,9 +258,11 @@ cudaError_t launch_chol_apply(const float *G, int batch, int r, float ridge, __n
   if (batch <= 0 || n <= 0) return cudaSuccess;
   dim3 grid((n + kApplyRows - 1) / kApplyRows, batch);
   if (r <= 32)
-    chol_apply_kernel<32><<<grid, 256, 0, s>>>(G, r, ridge, T, n, ldT, l0, sTb, Ginv, status);
+    chol_apply_kernel<32><<<grid, apply_threads<32>(), 0, s>>>(G, r, ridge, T, n, ldT, l0, sTb,
+                                                              Ginv, status);
   else
-    chol_apply_kernel<64><<<grid, 256, 0, s>>>(G, r, ridge, T, n, ldT, l0, sTb, Ginv, status);
+    chol_apply_kernel<64><<<grid, apply_threads<64>(), 0, s>>>(G, r, ridge, T, n, ldT, l0, sTb,
+                                                              Ginv, status);
   return cudaGetLastError();
 }
 

@@ -197,6 +197,18 @@ bool make_store_map(CUtensorMap *map, const void *base, long long inner, long lo
 // epilogue's stores and launch latency, not by L2 reads of B), so single CTAs are the default.
 constexpr int kCluster = 1;
 
+// GEMMs whose operands are both K-major run as cta_group::2 pair MMAs (M = 256 per CTA pair,
+// B split between the pair), which cuts each SM's shared-memory traffic per MMA by a third.
+constexpr bool kPairMma = true;
+constexpr int kBDiv = kPairMma ? 2 : kCluster;   // K-major B box rows = BN / kBDiv
+
+void set_pair(dyra::TcGemmParams &p, int elem_bytes, int b_major1) {
+  if (!kPairMma) return;
+  p.pair_mma = 1;
+  p.idesc = dyra::tc_idesc(elem_bytes, 0, 0, p.BN, 256);
+  p.idesc1 = dyra::tc_idesc(elem_bytes, 0, b_major1, p.BN, 256);
+}
+
 dyra::TcGemmParams base_params() {
   dyra::TcGemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -262,7 +274,7 @@ dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, in
     CUtensorMap a, b, o;
     const int BN = 256;
     DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
-    DY_MAP(make_map(&b, L->bd1, 2, 256, d, 1, 256, 0, BN / kCluster));
+    DY_MAP(make_map(&b, L->bd1, 2, 256, d, 1, 256, 0, BN / kBDiv));
     DY_MAP(make_store_map(&o, T, d, n, batch, ldT, (long long)n * ldT));
     TcGemmParams p = base_params();
     p.m_tiles = (int)cdiv(n, 128);
@@ -276,6 +288,7 @@ dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, in
     p.a_kdiag = 1;
     p.b_split = p.k_chunks;
     p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    set_pair(p, 2, 0);
     p.epi = EPI_ROW_BF16;
     p.tma_store = 1;
     p.out_batched = 1;
@@ -289,9 +302,9 @@ dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, in
   // L = X P into T[:, d:d+r]
   {
     CUtensorMap a, b, o;
-    const int BN = roundup(r, 16);
+    const int BN = roundup(r, kPairMma ? 32 : 16);
     DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
-    DY_MAP(make_map(&b, L->w1, 2, d, r, 1, d, 0, BN / kCluster));
+    DY_MAP(make_map(&b, L->w1, 2, d, r, 1, d, 0, BN / kBDiv));
     TcGemmParams p = base_params();
     p.m_tiles = (int)cdiv(n, 128);
     p.n_tiles = 1;
@@ -303,6 +316,7 @@ dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, in
     p.a_batched0 = 1;
     p.b_split = p.k_chunks;
     p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    set_pair(p, 2, 0);
     p.epi = EPI_ROW_BF16;
     p.rows_valid = n;
     p.cols_valid = r;
@@ -355,7 +369,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     const int nt = (int)cdiv(N, 256);
     const int BN = roundup((int)cdiv(N, nt), 32);
     DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
-    DY_MAP(make_map(&b, L->w1, 2, d, N, 1, d, 0, BN / kCluster));
+    DY_MAP(make_map(&b, L->w1, 2, d, N, 1, d, 0, BN / kBDiv));
     DY_MAP(make_store_map(&o, T, N, n, batch, ldT, (long long)n * ldT));
     TcGemmParams p = base_params();
     p.m_tiles = (int)cdiv(n, 128);
@@ -368,6 +382,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.a_batched0 = 1;
     p.b_split = p.k_chunks;
     p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    set_pair(p, 2, 0);
     p.epi = EPI_ROW_BF16;
     p.tma_store = 1;
     p.out_batched = 1;
@@ -461,11 +476,11 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     // Both GEMMs of an iteration read K-major operands only. X_t stays symmetric (a
     // polynomial in G_hat), so its rows serve as the columns of the B operand of
     // P = G_hat X_t; P is stored transposed so X_{t+1} = 2 X_t - X_t P reads it K-major too.
-    const int BN = roundup(r, 16);
+    const int BN = roundup(r, kPairMma ? 32 : 16);
     for (int it = 0; it < L->ns_iters; ++it) {
       CUtensorMap a, b;
       DY_MAP(make_map(&a, Gh, 4, r, r, batch, r, (long long)r * r, 128));
-      DY_MAP(make_map(&b, Xa, 4, r, r, batch, r, (long long)r * r, BN / kCluster));
+      DY_MAP(make_map(&b, Xa, 4, r, r, batch, r, (long long)r * r, BN / kBDiv));
       TcGemmParams p = base_params();
       p.m_tiles = (int)cdiv(r, 128);
       p.n_tiles = 1;
@@ -478,6 +493,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
       p.b_split = p.k_chunks;
       p.b_batched0 = 1;
       p.idesc = tc_idesc(4, 0, 0, BN);
+      set_pair(p, 4, 0);
       p.epi = EPI_TRANS_F32;
       p.out = Pt;
       p.out_bstride = (long long)r * r;
@@ -489,7 +505,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
       p.timeouts = status + 1;
       plan.steps.push_back(gemm_step(p, a, a, b, b));   // P^T = (G_hat X)^T
       DY_MAP(make_map(&a, Xa, 4, r, r, batch, r, (long long)r * r, 128));
-      DY_MAP(make_map(&b, Pt, 4, r, r, batch, r, (long long)r * r, BN / kCluster));
+      DY_MAP(make_map(&b, Pt, 4, r, r, batch, r, (long long)r * r, BN / kBDiv));
       p.epi = EPI_ROW_F32;
       p.out = Xb;
       p.out_bstride = (long long)r * r;
@@ -516,9 +532,9 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     // L~ = L G^-1, in place over the L columns of T (auxiliary stream)
     {
       CUtensorMap a, b, o;
-      const int BN = roundup(r, 16);
+      const int BN = roundup(r, kPairMma ? 32 : 16);
       DY_MAP(make_map(&a, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 128));
-      DY_MAP(make_map(&b, Ginv, 2, r, r, batch, r, (long long)r * r, BN / kCluster));
+      DY_MAP(make_map(&b, Ginv, 2, r, r, batch, r, (long long)r * r, BN / kBDiv));
       TcGemmParams p = base_params();
       p.m_tiles = (int)cdiv(n, 128);
       p.n_tiles = 1;
@@ -531,6 +547,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
       p.b_split = p.k_chunks;
       p.b_batched0 = 1;
       p.idesc = tc_idesc(2, 0, 0, BN);
+      set_pair(p, 2, 0);
       p.epi = EPI_ROW_BF16;
       p.rows_valid = n;
       p.cols_valid = r;
@@ -556,7 +573,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     const long long rows = (long long)batch * r;
     const int BN = pick_bn(rows, m, 32);
     DY_MAP(make_map(&a, C, 2, d, rows, 1, d, 0, 128));
-    DY_MAP(make_map(&b, L->wres, 2, d, m, 1, d, 0, BN / kCluster));
+    DY_MAP(make_map(&b, L->wres, 2, d, m, 1, d, 0, BN / kBDiv));
     DY_MAP(make_store_map(&o, Bm, m, rows, 1, m, 0));
     TcGemmParams p = base_params();
     p.m_tiles = (int)cdiv(rows, 128);
@@ -568,6 +585,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.a_split = p.m_tiles;
     p.b_split = p.k_chunks;
     p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    set_pair(p, 2, 0);
     p.epi = EPI_ROW_BF16;
     p.tma_store = 1;
     p.rows_valid = (int)rows;
@@ -590,7 +608,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     const int BN = 256;
     DY_MAP(make_map(&a, T, 2, ldT, n, batch, ldT, (long long)n * ldT, 128));
     DY_MAP(make_map(&b1, Bm, 2, m, r, batch, m, (long long)r * m, 64));
-    DY_MAP(make_map(&b0, L->bd2, 2, 256, m, 1, 256, 0, BN / kCluster));
+    DY_MAP(make_map(&b0, L->bd2, 2, 256, m, 1, 256, 0, BN / kBDiv));
     DY_MAP(make_store_map(&o, Y, m, n, batch, m, (long long)n * m));
     TcGemmParams p = base_params();
     p.m_tiles = (int)cdiv(n, 128);
@@ -609,6 +627,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.b_major1 = 1;
     p.idesc = tc_idesc(2, 0, 0, BN);
     p.idesc1 = tc_idesc(2, 0, 1, BN);
+    set_pair(p, 2, 1);
     p.epi = EPI_ROW_BF16;
     p.tma_store = 1;
     p.out_batched = 1;
@@ -623,11 +642,11 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
   }
   {
     CUtensorMap a, b0, b1, o;
-    const int BN = pick_bn((long long)batch * cdiv(n, 128) * 128, m, 64);
+    const int BN = pick_bn((long long)batch * cdiv(n, 128) * 128, m, kPairMma ? 128 : 64);
     DY_MAP(make_map(&a, T, 2, ldT, n, batch, ldT, (long long)n * ldT, 128));
     DY_MAP(make_map(&b1, Bm, 2, m, r, batch, m, (long long)r * m, 64));
     if (kp > 0)
-      DY_MAP(make_map(&b0, L->v, 2, kp, m, 1, kp, 0, BN / kCluster));
+      DY_MAP(make_map(&b0, L->v, 2, kp, m, 1, kp, 0, BN / kBDiv));
     else
       b0 = b1;
     DY_MAP(make_store_map(&o, Y, m, n, batch, m, (long long)n * m));
@@ -646,6 +665,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.b_major1 = 1;
     p.idesc = tc_idesc(2, 0, 0, BN);
     p.idesc1 = tc_idesc(2, 0, 1, BN);
+    set_pair(p, 2, 1);
     p.epi = EPI_ROW_BF16;
     p.tma_store = 1;
     p.out_batched = 1;

@@ -5,6 +5,7 @@
 
 #include <cuda_bf16.h>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 namespace dyra {
@@ -106,6 +107,9 @@ constexpr int kWarpLoadA = 0, kWarpMma = 1, kWarpLoadB = 2;
 constexpr int kEpiWarp0 = 4, kEpiWarps = 8;      // warps 4..11: two per TMEM lane quarter
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 
+// PMMA: cta_group::2 pair MMAs. A kernel holding pair instructions may only be launched as a
+// cluster, so the single-CTA engine is a separate instantiation without them.
+template <bool PMMA>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
@@ -118,8 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw_addr);
   const uint32_t S = (uint32_t)p.stages;
+  constexpr bool pmma = PMMA;
   const uint32_t a_bytes = 16384u;
-  const uint32_t b_bytes = (uint32_t)p.BN * 128u;
+  // B bytes in this CTA's shared memory per stage (half the tile for pair MMAs)
+  const uint32_t b_bytes = (uint32_t)p.BN * 128u / (pmma ? 2u : 1u);
   const uint32_t stage_bytes = a_bytes + b_bytes;
   const uint32_t staging = base + p.staging_off;
   const uint32_t bar_base =
@@ -133,8 +139,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = 128 / p.elem_bytes;   // elements in one 128-byte row
-  const bool pair = p.cluster == 2;
-  const int crank = pair ? (int)ptx::cluster_ctarank() : 0;
+  const bool pair = p.cluster == 2 && !pmma;     // multicast pairs
+  const int crank = p.cluster == 2 ? (int)ptx::cluster_ctarank() : 0;
+  const bool leader = crank == 0;
   const int cid = (int)blockIdx.x / p.cluster, ncl = (int)gridDim.x / p.cluster;
   const int mp_tiles = (p.m_tiles + p.cluster - 1) / p.cluster;
   const int total = p.batch * mp_tiles * p.n_tiles;
@@ -142,12 +149,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpLoadA && lane == 0) {
     for (uint32_t s = 0; s < S; ++s) {
       ptx::mbar_init(full_bar + 8u * s, 2);    // the A and the B issuer
-      ptx::mbar_init(empty_bar + 8u * s, (uint32_t)p.cluster);   // the MMA of every CTA
-                                                                  // reading this stage
+      // the MMA of every CTA reading this stage (multicast pairs: both; pair MMAs: the one
+      // issuing CTA)
+      ptx::mbar_init(empty_bar + 8u * s, pair ? 2u : 1u);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar + 8u * a, 1);
-      ptx::mbar_init(tempty_bar + 8u * a, kEpiWarps);
+      // pair MMAs: the even CTA's MMA waits for the epilogues of both CTAs
+      ptx::mbar_init(tempty_bar + 8u * a, (uint32_t)(kEpiWarps * (pmma ? 2 : 1)));
     }
     ptx::mbar_init_fence();
     ptx::tma_prefetch_desc(&tmA0);
@@ -159,13 +168,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.b_split < p.k_chunks) ptx::tma_prefetch_desc(&tmB1);
   }
   if (warp == kWarpMma) {
-    ptx::tmem_alloc(tmem_slot, 2u * p.acc_cols);
-    ptx::tmem_relinquish();
+    if constexpr (PMMA) {
+      ptx::tmem_alloc_pair(tmem_slot, 2u * p.acc_cols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, 2u * p.acc_cols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
   // the peer's barriers must be initialised before its multicasts and commits reach them
-  if (pair) ptx::cluster_sync_all();
+  if (p.cluster == 2) ptx::cluster_sync_all();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_ptr;
   // set-up above overlaps the previous kernel; its outputs are read only after this
@@ -192,11 +206,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t full = full_bar + 8u * s;
-          ptx::mbar_arrive_expect_tx(full, a_bytes);
-          if (p.a_major == 0) {
+          if constexpr (PMMA) {
+            // both CTAs' A land on the even CTA's full barrier, which expects them all
+            if (leader) ptx::mbar_arrive_expect_tx(full, 2u * a_bytes);
+            const int ka = kc < p.b_split ? a_k0 + kc * chunk : a_k1 + (kc - p.b_split) * chunk;
+            ptx::tma_load_3d_pair(sa, ma, ptx::mapa_shared(full, 0), ka, m0, a_b);
+          } else if (p.a_major == 0) {
+            ptx::mbar_arrive_expect_tx(full, a_bytes);
             const int ka = kc < p.b_split ? a_k0 + kc * chunk : a_k1 + (kc - p.b_split) * chunk;
             ptx::tma_load_3d(sa, ma, full, ka, m0, a_b);
           } else {
+            ptx::mbar_arrive_expect_tx(full, a_bytes);
             for (int i = 0; i < 128 / chunk; ++i)
               ptx::tma_load_3d(sa + (uint32_t)(i * chunk * 128), ma, full, m0 + i * chunk,
                                kc * chunk, a_b);
@@ -226,11 +246,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t full = full_bar + 8u * s;
-          ptx::mbar_arrive_expect_tx(full, b_bytes);
           const bool b_second = kc >= p.b_split;
           const CUtensorMap *mb = b_second ? &tmB1 : &tmB0;
           const int kk = b_second ? kc - p.b_split : kc;
           const int b_b = b_second ? b_b1 : b_b0;
+          if constexpr (PMMA) {
+            if (leader) ptx::mbar_arrive_expect_tx(full, 2u * b_bytes);
+            const uint32_t fb = ptx::mapa_shared(full, 0);
+            const int half = p.BN / 2;
+            if ((b_second ? p.b_major1 : p.b_major) == 0) {
+              ptx::tma_load_3d_pair(sb, mb, fb, kk * chunk, n0 + crank * half, b_b);
+            } else {
+              for (int i = 0; i < half / chunk; ++i)
+                ptx::tma_load_3d_pair(sb + (uint32_t)(i * chunk * 128), mb, fb,
+                                      n0 + crank * half + i * chunk, kk * chunk, b_b);
+            }
+          } else {
+          ptx::mbar_arrive_expect_tx(full, b_bytes);
           if (!pair) {
             if ((b_second ? p.b_major1 : p.b_major) == 0) {
               ptx::tma_load_3d(sb, mb, full, kk * chunk, n0, b_b);
@@ -249,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tma_load_3d_mc(sb + (uint32_t)(i * chunk * 128), mb, full, n0 + i * chunk,
                                   kk * chunk, b_b, (uint16_t)3);
           }
+          }
           if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -261,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
+    // (pair MMAs: only the even CTA issues, for both CTAs of the pair)
+    if (lane == 0 && (!pmma || leader)) {
       // K-major SW128: rows of 128 B, 8-row groups 1024 B apart (SBO), K advance inside the row.
       // MN-major SW128: 128-byte rows hold `chunk` MN elements; MN groups LBO apart, 8-row K
       // groups 1024 B apart; one MMA consumes 32 bytes of K = 32/elem rows.
@@ -293,20 +327,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = (b_second ? b_desc1 : b_desc0) + soff;
           const uint32_t bk = b_second ? b_k16_1 : b_k16_0;
           const uint32_t idesc = b_second ? p.idesc1 : p.idesc;
-          if (f16) {
+          if constexpr (PMMA) {
+            if (f16) {
 #pragma unroll
-            for (uint32_t ks = 0; ks < 4; ++ks)
-              ptx::tc_mma_f16(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
+              for (uint32_t ks = 0; ks < 4; ++ks)
+                ptx::tc_mma_f16_pair(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (uint32_t ks = 0; ks < 4; ++ks)
+                ptx::tc_mma_tf32_pair(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
+            }
+            // frees the stage in both CTAs when these MMAs finish
+            ptx::tc_commit_pair_mc(empty_bar + 8u * s, (uint16_t)3);
           } else {
+            if (f16) {
 #pragma unroll
-            for (uint32_t ks = 0; ks < 4; ++ks)
-              ptx::tc_mma_tf32(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
+              for (uint32_t ks = 0; ks < 4; ++ks)
+                ptx::tc_mma_f16(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (uint32_t ks = 0; ks < 4; ++ks)
+                ptx::tc_mma_tf32(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
+            }
+            // frees the smem stage (in both CTAs of a multicast pair) when these MMAs finish
+            if (pair)
+              ptx::tc_commit_mc(empty_bar + 8u * s, (uint16_t)3);
+            else
+              ptx::tc_commit(empty_bar + 8u * s);
           }
-          // frees the smem stage (in both CTAs of a pair) when these MMAs finish
-          if (pair)
-            ptx::tc_commit_mc(empty_bar + 8u * s, (uint16_t)3);
-          else
-            ptx::tc_commit(empty_bar + 8u * s);
           if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -315,7 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             soff += st16;
           }
         }
-        if (ok) ptx::tc_commit(tfull_bar + 8u * acc);   // accumulator ready
+        if (ok) {   // accumulator ready (in both CTAs of a pair)
+          if constexpr (PMMA)
+            ptx::tc_commit_pair_mc(tfull_bar + 8u * acc, (uint16_t)3);
+          else
+            ptx::tc_commit(tfull_bar + 8u * acc);
+        }
       }
     }
   } else if (warp >= kEpiWarp0) {
@@ -340,7 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tc.m_tile >= p.m_tiles) {   // a pair's tile past the last M tile: nothing to store
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(tempty_bar + 8u * acc);
+        if (lane == 0) {
+          if (pmma && !leader)
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar + 8u * acc, 0));
+          else
+            ptx::mbar_arrive(tempty_bar + 8u * acc);
+        }
         continue;
       }
       const bool second = tc.m_tile >= p.a_split;
@@ -423,7 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(tempty_bar + 8u * acc);
+      if (lane == 0) {   // this accumulator may be overwritten (pair MMAs: by the even CTA)
+        if (pmma && !leader)
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar + 8u * acc, 0));
+        else
+          ptx::mbar_arrive(tempty_bar + 8u * acc);
+      }
     }
     if (p.tma_store && lane == 0) ptx::bulk_wait<0>();
   }
@@ -431,10 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   // neither CTA of a pair leaves while the other may still write its shared memory or
   // arrive on its barriers
-  if (pair) ptx::cluster_sync_all();
+  if (p.cluster == 2) ptx::cluster_sync_all();
   if (warp == kWarpMma) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, 2u * p.acc_cols);
+    if constexpr (PMMA)
+      ptx::tmem_dealloc_pair(tmem_base, 2u * p.acc_cols);
+    else
+      ptx::tmem_dealloc(tmem_base, 2u * p.acc_cols);
   }
 }
 
@@ -490,7 +556,7 @@ int num_sms() {
 
 }  // namespace
 
-uint32_t tc_idesc(int elem_bytes, int a_major, int b_major, int n) {
+uint32_t tc_idesc(int elem_bytes, int a_major, int b_major, int n, int m) {
   const uint32_t fmt = elem_bytes == 2 ? 1u : 2u;   // BF16 = 1, TF32 = 2
   uint32_t d = 0;
   d |= 1u << 4;                          // D format: F32
@@ -499,7 +565,7 @@ uint32_t tc_idesc(int elem_bytes, int a_major, int b_major, int n) {
   d |= (uint32_t)(a_major & 1) << 15;    // A major (1 = MN)
   d |= (uint32_t)(b_major & 1) << 16;    // B major
   d |= ((uint32_t)n >> 3) << 17;         // N / 8
-  d |= (128u >> 4) << 24;                // M / 16
+  d |= ((uint32_t)m >> 4) << 24;         // M / 16
   return d;
 }
 
@@ -512,14 +578,41 @@ bool tc_make_store_map(CUtensorMap *map, const TcOperand &op) {
   return encode(map, op, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// Co-resident 2-CTA clusters for this kernel and shared-memory size (a persistent grid larger
+// than that would run a second, mostly idle wave). Queried once per (kernel, size) and cached;
+// a failed query is cleared and falls back to one pair per two SMs.
+static int max_active_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                                         CUtensorMap, TcGemmParams),
+                            cudaLaunchConfig_t cfg, bool pmma) {
+  static std::mutex mu;
+  static std::map<std::pair<int, uint64_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_pair(dev, ((uint64_t)cfg.dynamicSmemBytes << 1) | (pmma ? 1u : 0u));
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cfg.gridDim = dim3(2, 1, 1);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = num_sms() / 2;
+  }
+  cache[key] = n;
+  return n;
+}
+
 cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensorMap &a1,
                            const CUtensorMap &b0, const CUtensorMap &b1,
                            const CUtensorMap &out_map, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, []() {
-    attr_err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    232448);
+    attr_err = cudaFuncSetAttribute(tc_gemm_kernel<false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(tc_gemm_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
   });
   if (attr_err != cudaSuccess) return attr_err;
   if (p.m_tiles <= 0 || p.n_tiles <= 0 || p.batch <= 0 || p.k_chunks <= 0) return cudaSuccess;
@@ -531,7 +624,13 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
   if ((p.b_major || p.b_major1) && p.BN % 64) return cudaErrorInvalidValue;
   p.acc_cols = 32;
   while (p.acc_cols < (uint32_t)p.BN) p.acc_cols <<= 1;
-  const uint32_t stage = 16384u + (uint32_t)p.BN * 128u;
+  if (p.pair_mma) {
+    p.cluster = 2;
+    if (p.BN % 32) return cudaErrorInvalidValue;                   // halves of whole 8-row groups
+    if ((p.b_major || p.b_major1) && p.BN % 128) return cudaErrorInvalidValue;
+    if (p.a_major) return cudaErrorNotSupported;
+  }
+  const uint32_t stage = 16384u + (uint32_t)p.BN * 128u / (p.pair_mma ? 2u : 1u);
   const uint32_t staging = p.tma_store ? (uint32_t)kEpiWarps * kStagingBytesPerWarp : 0u;
   const uint32_t fixed = 1024u + staging + 256u;   // alignment slack, staging, barriers
   int S = (int)((232448u - fixed) / stage);
@@ -560,22 +659,20 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
   cfg.numAttrs = 1;
   if (p.cluster == 1) {
     cfg.gridDim = dim3((unsigned)(units < num_sms() ? units : num_sms()), 1, 1);
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, a0, a1, b0, b1, out_map, p);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<false>, a0, a1, b0, b1, out_map, p);
   }
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.numAttrs = 2;
-  int max_clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, tc_gemm_kernel, &cfg) != cudaSuccess ||
-      max_clusters <= 0)
-    max_clusters = num_sms() / 2;
+  // cluster launches go without the programmatic-serialization attribute; their pdl_wait
+  // then returns at once
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.numAttrs = 1;
+  auto kern = p.pair_mma ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+  const int max_clusters = max_active_pairs(kern, cfg, p.pair_mma != 0);
   const long long clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel, a0, a1, b0, b1, out_map, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, out_map, p);
 }
 
 }  // namespace dyra

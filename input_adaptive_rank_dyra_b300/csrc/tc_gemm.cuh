@@ -40,6 +40,11 @@ enum TcEpi : int {
 
 struct TcGemmParams {
   int m_tiles, n_tiles, batch;
+  int pair_mma;      // 1: CTA pairs run cta_group::2 MMAs (M = 256 per pair): each CTA holds
+                     // its 128 rows of A and half of the B tile (BN / 2 rows or columns), the
+                     // even CTA issues the MMAs, each CTA's TMEM receives its own 128 rows
+                     // (implies cluster = 2 without multicast; K-major B maps then need a
+                     // box of BN / 2 rows; MN-major B needs BN % 128 == 0)
   int cluster;       // 1, or 2: CTA pairs take adjacent M tiles of one (batch, N tile) and
                      // each loads half of the B tile, multicast to both (K-major B maps then
                      // need a box of BN / 2 rows)
@@ -90,8 +95,8 @@ struct TcOperand {
   long long row_stride, batch_stride;   // in bytes
 };
 
-// Build the instruction descriptor (M = 128).
-uint32_t tc_idesc(int elem_bytes, int a_major, int b_major, int n);
+// Build the instruction descriptor (M = 128, or 256 for pair MMAs).
+uint32_t tc_idesc(int elem_bytes, int a_major, int b_major, int n, int m = 128);
 
 // Creates a 3-D tensor map with 128-byte swizzle, box = {chunk, box_rows, 1}.
 bool tc_make_map(CUtensorMap *map, const TcOperand &op, int box_rows);

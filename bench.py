@@ -39,7 +39,7 @@ _CSRC = "input_adaptive_rank_dyra_b300/csrc/"
 # the source files that define each kernel of the forward (a recorded DRAM-traffic figure is
 # used only while their hash matches the one recorded with it)
 GEMM_SOURCES = [_CSRC + "tc_gemm.cu", _CSRC + "tc_gemm.cuh", _CSRC + "ptx.cuh"]
-KERNEL_SOURCES = {"chol_solve_apply": [_CSRC + "solve.cu", _CSRC + "kernels.cuh"],
+KERNEL_SOURCES = {"spd_solve_c": [_CSRC + "solve.cu", _CSRC + "kernels.cuh"],
                   "ns_prep": [_CSRC + "solve.cu"], "ns_finish": [_CSRC + "solve.cu"],
                   "monarch_permute": [_CSRC + "monarch.cu", _CSRC + "monarch.cuh"]}
 
@@ -98,11 +98,12 @@ def kernel_work(cfg, name: str):
     if name == "xproj_static_L":
         return 2.0 * B * n * d * (k + r), e * (B * n * d + (k + r) * d + B * n * (k + r))
     if name == "cg_c_gram":
-        return 2.0 * B * n * r * (d + r), e * (B * n * d + B * n * r + B * r * d) + 4 * B * r * r
-    if name == "chol_solve_apply":   # in-place elimination (r^3 FMA) + L~ = L G^-1
-        return B * (2.0 * r ** 3 + 2.0 * n * r * r), 4 * B * r * r + e * (2 * B * n * r + B * r * r)
-    if name == "lsolve_apply":
-        return 2.0 * B * n * r * r, e * (2 * B * n * r + B * r * r)
+        return 2.0 * B * n * r * (d + r), e * (B * n * d + B * n * r) + 4 * (B * r * d + B * r * r)
+    if name == "spd_solve_c":   # r sweeps (r^3 FMA) + G^-1 applied to d columns
+        return (B * (2.0 * r ** 3 + 2.0 * r * r * d),
+                4 * (B * r * r + B * r * d) + e * (B * r * d + B * r * r))
+    if name == "ginv_c":
+        return 2.0 * B * r * r * d, 4 * (B * r * r + B * r * d) + e * B * r * d
     if name == "residual_product":
         return 2.0 * B * r * d * m, e * (B * r * d + d * m + B * r * m)
     if name == "fused_output":

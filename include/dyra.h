@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define DYRA_ABI_VERSION 1
+#define DYRA_ABI_VERSION 2
 
 typedef enum dyra_status {
   DYRA_OK = 0,
@@ -139,9 +139,8 @@ dyra_status dyra_workspace_size(const dyra_layer *layer, int batch, int n, size_
 /* The online step. X: device [batch, n, d], Y: device [batch, n, m], both in the layer's
  * dtype, 16-byte aligned, rows densely packed. workspace: device, >= dyra_workspace_size
  * bytes, 256-byte aligned, owned by the caller; it must not be shared by two forwards that
- * may run at the same time. Enqueues every kernel on `stream` (on the bf16 Cholesky path
- * the SPD solve is forked onto an internal stream of the layer, beside B = C W_res, and
- * joined back before the output kernel) and returns without waiting. batch == 0 or n == 0 is a no-op. A sample whose
+ * may run at the same time. Enqueues every kernel on `stream` and returns without waiting.
+ * batch == 0 or n == 0 is a no-op. A sample whose
  * L^T L + lambda I is not positive definite (e.g. an all-zero sample with lambda = 0) gets
  * R = 0 -- its rows of Y are the static branch plus b -- and is counted in the status word
  * that dyra_workspace_status reads. Errors (nothing launched): INVALID_ARG, WORKSPACE, CUDA. */
@@ -160,8 +159,7 @@ dyra_status dyra_linear_forward_host(const dyra_layer *layer, const void *X_host
 
 /* The same forward (same streams, same kernels) that also records two events around every
  * kernel it launches: events[2i] just before kernel i and events[2i + 1] just after it, both
- * on the stream kernel i runs on (the caller's stream, or the layer's auxiliary stream for
- * the SPD-solve branch), so cudaEventElapsedTime(events[2i], events[2i + 1]) is kernel i's
+ * on `stream`, so cudaEventElapsedTime(events[2i], events[2i + 1]) is kernel i's
  * device time. count = kernels_per_forward; max_events must be >= 2 * count. *recorded
  * receives 2 * count. Called while `stream` is being captured into a CUDA graph, the records
  * become event-record nodes (cudaEventRecordExternal), so every replay of the graph times
@@ -183,14 +181,15 @@ dyra_status dyra_workspace_status(const dyra_layer *layer, const void *workspace
 
 /* Intermediates a forward leaves in its workspace, for tests that check each kernel. */
 typedef enum dyra_buffer {
-  DYRA_BUF_T = 0,      /* [batch, n, ld]. bf16 path: [X F1 | L (L^T L + lambda I)^-1] after
-                          the forward (the L columns are rewritten in place); f32 path:
-                          [X U | L]                                                         */
-  DYRA_BUF_C = 1,      /* C = L^T X, [batch, r, d] (bf16 / fp32)                           */
+  DYRA_BUF_T = 0,      /* [batch, n, ld] = [X F1 | L] (bf16: F1 columns padded to a multiple
+                          of 64; Monarch: the permuted X BD1 in place of X F1)              */
+  DYRA_BUF_C = 1,      /* bf16 path: C^T = X^T L, [batch, d, r] fp32; f32 path: C = L^T X,
+                          [batch, r, d] fp32                                                */
   DYRA_BUF_G = 2,      /* L^T L without lambda, [batch, r, r] (fp32 / fp64)                */
   DYRA_BUF_GINV = 3,   /* (L^T L + lambda I)^-1, [batch, r, r] (bf16 / fp64)               */
-  DYRA_BUF_B = 4,      /* B = C W_res, [batch, r, m] (bf16 / fp32)                          */
-  DYRA_BUF_R = 5       /* f32 path only: R = G^-1 B, [batch, r, m] fp32                    */
+  DYRA_BUF_B = 4,      /* f32 path only: B = C W_res, [batch, r, m] fp32                    */
+  DYRA_BUF_R = 5,      /* R = (L^T L + lambda I)^-1 C W_res, [batch, r, m] (bf16 / fp32)     */
+  DYRA_BUF_CS = 6      /* bf16 path only: (L^T L + lambda I)^-1 C, [batch, r, d] bf16       */
 } dyra_buffer;
 
 /* Byte offset of intermediate `which` inside the workspace for (batch, n) and its row

@@ -46,9 +46,7 @@ struct dyra_layer {
   // wres = W_res^T [m, d] (bf16); f32: w1 = [U | P] [d, k + r], v = V [k, m], wres = W_res [d, m]
   void *w1 = nullptr, *v = nullptr, *wres = nullptr, *bd1 = nullptr, *bd2 = nullptr;
   float *bias_d = nullptr;
-  cudaStream_t aux = nullptr;            // stream of the SPD-solve branch
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  mutable std::mutex mu;                 // plan cache and fork/join events
+  mutable std::mutex mu;                 // plan cache
   mutable std::vector<std::pair<std::array<uintptr_t, 5>, std::shared_ptr<void>>> plans;
 };
 
@@ -86,7 +84,7 @@ struct DeviceGuard {
 
 struct WsLayout {
   size_t T = 0, C = 0, G = 0, Ginv = 0, Gh = 0, X0 = 0, X1 = 0, Pt = 0, dinv = 0, flags = 0,
-         B = 0, R = 0, total = 0;
+         B = 0, R = 0, Cs = 0, total = 0;
   int ldT = 0;
 };
 
@@ -102,7 +100,7 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
   if (L->dtype == DYRA_BF16) {
     w.ldT = L->kp + L->r;
     w.T = take(B * N * (size_t)w.ldT * 2);
-    w.C = take(B * r * d * 2);
+    w.C = take(B * d * r * 4);   // C^T, fp32
     w.G = take(B * r * r * 4);
     w.Ginv = take(B * r * r * 2);
     if (L->solver == DYRA_SOLVE_NEWTON_SCHULZ) {
@@ -113,7 +111,8 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
       w.dinv = take(B * r * 4);
       w.flags = take(B * 4);
     }
-    w.B = take(B * m * r * 2);
+    w.Cs = take(B * r * d * 2);
+    w.R = take(B * r * m * 2);
   } else {
     w.ldT = L->k + L->r;
     w.T = take(B * N * (size_t)w.ldT * 4);
@@ -134,8 +133,7 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
 // same buffers, so a steady-state forward costs only its launches on the host.
 
 struct Step {
-  enum Kind { GEMM, CHOL_APPLY, NS_PREP, NS_FINISH, PERMUTE, FORK, JOIN } kind = GEMM;
-  bool aux = false;   // runs on the auxiliary stream
+  enum Kind { GEMM, SPD_SOLVE, NS_PREP, NS_FINISH, PERMUTE } kind = GEMM;
   dyra::TcGemmParams p;
   CUtensorMap a0, a1, b0, b1, out;
   const float *G = nullptr;
@@ -144,9 +142,12 @@ struct Step {
   int *flags = nullptr;
   __nv_bfloat16 *Ginv = nullptr;
   __nv_bfloat16 *T = nullptr;
+  const float *Ct = nullptr;
+  float *G32 = nullptr;
+  __nv_bfloat16 *Cs = nullptr;
   int *status = nullptr;
-  int batch = 0, r = 0, n = 0, ldT = 0, l0 = 0, nb = 0;
-  long long sTb = 0, rows = 0;
+  int batch = 0, r = 0, d = 0, ldT = 0, nb = 0;
+  long long rows = 0;
   float ridge = 0.f;
 };
 
@@ -209,6 +210,35 @@ void set_pair(dyra::TcGemmParams &p, int elem_bytes, int b_major1) {
   p.idesc1 = dyra::tc_idesc(elem_bytes, 0, b_major1, p.BN, 256);
 }
 
+// The output GEMM tiles the flat batch * n rows (its rank chunks then repeat for every
+// sample that a tile's rows touch) when per-sample tiles would leave part of each sample's
+// last tile empty. Below 64 rows per sample a tile would touch too many samples.
+bool use_flat_rows(int batch, int n) {
+  const int unit = kPairMma ? 256 : 128;
+  return batch > 1 && n >= 64 && n % unit != 0;
+}
+
+// Switches the output GEMM `p` (per-sample maps a0 / o over [batch][n]) to flat rows:
+// a0 and o become [batch * n] views, a1 keeps the per-sample view for the rank chunks.
+dyra_status set_flat_rows(dyra::TcGemmParams &p, CUtensorMap &a0, CUtensorMap &o,
+                          const void *T, int ldT, void *Y, int m, int batch, int n) {
+  const long long rows = (long long)batch * n;
+  if (!make_map(&a0, T, 2, ldT, rows, 1, ldT, 0, 128) ||
+      !make_store_map(&o, Y, m, rows, 1, m, 0)) {
+    g_last_error = "cuTensorMapEncodeTiled failed: flat output maps";
+    return DYRA_ERR_CUDA;
+  }
+  p.m_tiles = (int)cdiv(rows, 128);
+  p.batch = 1;
+  p.a_split = p.m_tiles;
+  p.a_batched0 = 0;
+  p.seg_n = n;
+  p.seg_count = batch;
+  p.out_batched = 0;
+  p.rows_valid = (int)rows;
+  return DYRA_OK;
+}
+
 dyra::TcGemmParams base_params() {
   dyra::TcGemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -220,10 +250,9 @@ dyra::TcGemmParams base_params() {
 }
 
 Step gemm_step(const dyra::TcGemmParams &p, const CUtensorMap &a0, const CUtensorMap &a1,
-               const CUtensorMap &b0, const CUtensorMap &b1, bool aux = false) {
+               const CUtensorMap &b0, const CUtensorMap &b1) {
   Step st;
   st.kind = Step::GEMM;
-  st.aux = aux;
   st.p = p;
   st.a0 = a0;
   st.a1 = a1;
@@ -354,10 +383,11 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
   const int d = L->d, m = L->m, r = L->r, kp = L->kp, ldT = w.ldT;
   int *status = reinterpret_cast<int *>(ws);
   __nv_bfloat16 *T = reinterpret_cast<__nv_bfloat16 *>(ws + w.T);
-  __nv_bfloat16 *C = reinterpret_cast<__nv_bfloat16 *>(ws + w.C);
+  float *Ct = reinterpret_cast<float *>(ws + w.C);   // C^T [batch, d, r]
   float *G = reinterpret_cast<float *>(ws + w.G);
   __nv_bfloat16 *Ginv = reinterpret_cast<__nv_bfloat16 *>(ws + w.Ginv);
-  __nv_bfloat16 *Bm = reinterpret_cast<__nv_bfloat16 *>(ws + w.B);
+  __nv_bfloat16 *Cs = reinterpret_cast<__nv_bfloat16 *>(ws + w.Cs);
+  __nv_bfloat16 *Rm = reinterpret_cast<__nv_bfloat16 *>(ws + w.R);
 
   // 1. T = X [U | P]   (Monarch: permuted X BD1 and L)
   if (L->kind == DYRA_STATIC_MONARCH) {
@@ -413,9 +443,9 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.b_batched0 = 1;
     p.idesc = tc_idesc(2, 1, 1, p.BN);
     p.epi = EPI_CG;
-    p.out = C;                       // C [batch, r, d] from the C^T rows
-    p.out_bstride = (long long)r * d;
-    p.out_ld = d;
+    p.out = Ct;                      // C^T [batch, d, r], fp32
+    p.out_bstride = (long long)d * r;
+    p.out_ld = r;
     p.rows_valid = d;
     p.cols_valid = r;
     p.out2 = G;
@@ -426,30 +456,19 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.timeouts = status + 1;
     plan.steps.push_back(gemm_step(p, ax, al, al, al));
   }
-  // The Cholesky branch is one kernel and runs on the auxiliary stream beside B = C W_res.
-  // The Newton-Schulz branch is a chain of small kernels: beside the persistent B GEMM they
-  // would wait for SMs, so it runs on the main stream, before it.
-  const bool fork = L->solver == DYRA_SOLVE_CHOLESKY;
-  if (fork) {
-    Step f;
-    f.kind = Step::FORK;
-    plan.steps.push_back(f);
-  }
-  // 4-5. G^-1 and L~ = L G^-1 over the L columns of T (auxiliary stream)
+  // 3. C~ = (G + lambda I)^-1 C: one kernel on the Cholesky branch; on the Newton-Schulz
+  //    branch a chain of small kernels and tf32 GEMMs forms G^-1, then a bf16 GEMM applies it.
   if (L->solver == DYRA_SOLVE_CHOLESKY) {
     Step st;
-    st.kind = Step::CHOL_APPLY;
-    st.aux = true;
+    st.kind = Step::SPD_SOLVE;
     st.G = G;
     st.batch = batch;
     st.r = r;
+    st.d = d;
     st.ridge = (float)L->ridge;
+    st.Ct = Ct;
+    st.Cs = Cs;
     st.Ginv = Ginv;
-    st.T = T;
-    st.n = n;
-    st.ldT = ldT;
-    st.l0 = kp;
-    st.sTb = (long long)n * ldT;
     st.status = status;
     plan.steps.push_back(st);
   } else {
@@ -462,7 +481,6 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     {
       Step st;
       st.kind = Step::NS_PREP;
-      st.aux = false;
       st.G = G;
       st.batch = batch;
       st.r = r;
@@ -520,61 +538,55 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     }
     Step st;
     st.kind = Step::NS_FINISH;
-    st.aux = false;
     st.Xf = Xa;
     st.dinv = dinv;
     st.batch = batch;
     st.r = r;
     st.flags = flags;
     st.Ginv = Ginv;
+    st.G32 = Pt;   // fp32 G^-1 for the apply GEMM (Pt is free after the iterations)
     st.status = status;
     plan.steps.push_back(st);
-    // L~ = L G^-1, in place over the L columns of T (auxiliary stream)
+    // C~ = G^-1 C as a tf32 GEMM: M = r rows of G^-1 (fp32, K-major), N = d, K = r, with
+    // B = C^T [d, r] (K-major); bf16 result [batch, r, d]
     {
       CUtensorMap a, b, o;
-      const int BN = roundup(r, kPairMma ? 32 : 16);
-      DY_MAP(make_map(&a, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 128));
-      DY_MAP(make_map(&b, Ginv, 2, r, r, batch, r, (long long)r * r, BN / kBDiv));
+      const int BN = pick_bn((long long)batch * cdiv(r, 128) * 128, d, 32);
+      DY_MAP(make_map(&a, Pt, 4, r, r, batch, r, (long long)r * r, 128));
+      DY_MAP(make_map(&b, Ct, 4, r, d, batch, r, (long long)d * r, BN / kBDiv));
+      DY_MAP(make_store_map(&o, Cs, d, r, batch, d, (long long)r * d));
       TcGemmParams p = base_params();
-      p.m_tiles = (int)cdiv(n, 128);
-      p.n_tiles = 1;
+      p.m_tiles = (int)cdiv(r, 128);
+      p.n_tiles = (int)cdiv(d, BN);
       p.batch = batch;
       p.BN = BN;
-      p.k_chunks = (int)cdiv(r, 64);
-      p.elem_bytes = 2;
+      p.k_chunks = (int)cdiv(r, 32);
+      p.elem_bytes = 4;
       p.a_split = p.m_tiles;
       p.a_batched0 = 1;
       p.b_split = p.k_chunks;
       p.b_batched0 = 1;
-      p.idesc = tc_idesc(2, 0, 0, BN);
-      set_pair(p, 2, 0);
+      p.idesc = p.idesc1 = tc_idesc(4, 0, 0, BN);
+      set_pair(p, 4, 0);
       p.epi = EPI_ROW_BF16;
-      p.rows_valid = n;
-      p.cols_valid = r;
+      p.tma_store = 1;
+      p.out_batched = 1;
+      p.rows_valid = r;
+      p.cols_valid = d;
       p.timeouts = status + 1;
-      if (BN % 32 == 0) {
-        DY_MAP(make_store_map(&o, T + kp, r, n, batch, ldT, (long long)n * ldT));
-        p.tma_store = 1;
-        p.out_batched = 1;
-      } else {
-        o = a;
-        p.out = T + kp;
-        p.out_bstride = (long long)n * ldT;
-        p.out_ld = ldT;
-      }
       Step st = gemm_step(p, a, a, b, b);
       st.out = o;
       plan.steps.push_back(st);
     }
   }
-  // 3. B = C W_res, row-major [batch * r, m] (main stream, beside the solve)
+  // 4. R = C~ W_res, row-major [batch * r, m]
   {
     CUtensorMap a, b, o;
     const long long rows = (long long)batch * r;
     const int BN = pick_bn(rows, m, 32);
-    DY_MAP(make_map(&a, C, 2, d, rows, 1, d, 0, 128));
+    DY_MAP(make_map(&a, Cs, 2, d, rows, 1, d, 0, 128));
     DY_MAP(make_map(&b, L->wres, 2, d, m, 1, d, 0, BN / kBDiv));
-    DY_MAP(make_store_map(&o, Bm, m, rows, 1, m, 0));
+    DY_MAP(make_store_map(&o, Rm, m, rows, 1, m, 0));
     TcGemmParams p = base_params();
     p.m_tiles = (int)cdiv(rows, 128);
     p.n_tiles = (int)cdiv(m, BN);
@@ -595,19 +607,14 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     st.out = o;
     plan.steps.push_back(st);
   }
-  if (fork) {
-    Step j;
-    j.kind = Step::JOIN;
-    plan.steps.push_back(j);
-  }
-  // 6. Y = [X U | L~] [V ; B] + b: K chunks of V^T (K-major, shared by all samples), then
-  //    the sample's B (MN-major, [r, m] with m contiguous). Monarch: the first chunks are
+  // 5. Y = [X U | L] [V ; R] + b: K chunks of V^T (K-major, shared by all samples), then
+  //    the sample's R (MN-major, [r, m] with m contiguous). Monarch: the first chunks are
   //    Zp BD2 on 256-column tiles (each contracting with its own 256 columns of Zp).
   if (L->kind == DYRA_STATIC_MONARCH) {
     CUtensorMap a, b0, b1, o;
     const int BN = 256;
     DY_MAP(make_map(&a, T, 2, ldT, n, batch, ldT, (long long)n * ldT, 128));
-    DY_MAP(make_map(&b1, Bm, 2, m, r, batch, m, (long long)r * m, 64));
+    DY_MAP(make_map(&b1, Rm, 2, m, r, batch, m, (long long)r * m, 64));
     DY_MAP(make_map(&b0, L->bd2, 2, 256, m, 1, 256, 0, BN / kBDiv));
     DY_MAP(make_store_map(&o, Y, m, n, batch, m, (long long)n * m));
     TcGemmParams p = base_params();
@@ -635,16 +642,23 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.cols_valid = m;
     p.bias = L->bias_d;
     p.timeouts = status + 1;
-    Step st = gemm_step(p, a, a, b0, b1);
+    CUtensorMap a0 = a;
+    if (use_flat_rows(batch, n)) {
+      const dyra_status fs = set_flat_rows(p, a0, o, T, ldT, Y, m, batch, n);
+      if (fs != DYRA_OK) return fs;
+    }
+    Step st = gemm_step(p, a0, a, b0, b1);
     st.out = o;
     plan.steps.push_back(st);
     return DYRA_OK;
   }
   {
     CUtensorMap a, b0, b1, o;
-    const int BN = pick_bn((long long)batch * cdiv(n, 128) * 128, m, kPairMma ? 128 : 64);
+    const bool flat = use_flat_rows(batch, n);
+    const int BN = pick_bn(flat ? (long long)batch * n : (long long)batch * cdiv(n, 128) * 128, m,
+                           kPairMma ? 128 : 64);
     DY_MAP(make_map(&a, T, 2, ldT, n, batch, ldT, (long long)n * ldT, 128));
-    DY_MAP(make_map(&b1, Bm, 2, m, r, batch, m, (long long)r * m, 64));
+    DY_MAP(make_map(&b1, Rm, 2, m, r, batch, m, (long long)r * m, 64));
     if (kp > 0)
       DY_MAP(make_map(&b0, L->v, 2, kp, m, 1, kp, 0, BN / kBDiv));
     else
@@ -673,7 +687,12 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.cols_valid = m;
     p.bias = L->bias_d;
     p.timeouts = status + 1;
-    Step st = gemm_step(p, a, a, b0, b1);
+    CUtensorMap a0 = a;
+    if (flat) {
+      const dyra_status fs = set_flat_rows(p, a0, o, T, ldT, Y, m, batch, n);
+      if (fs != DYRA_OK) return fs;
+    }
+    Step st = gemm_step(p, a0, a, b0, b1);
     st.out = o;
     plan.steps.push_back(st);
   }
@@ -683,31 +702,16 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
 dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream_t s,
                      Recorder &rec) {
   using namespace dyra;
-  const bool fork = L->aux != nullptr;
   DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
   for (const Step &st : plan.steps) {
-    if (st.kind == Step::FORK) {
-      if (fork) {
-        DY_CUDA(cudaEventRecord(L->ev_fork, s));
-        DY_CUDA(cudaStreamWaitEvent(L->aux, L->ev_fork, 0));
-      }
-      continue;
-    }
-    if (st.kind == Step::JOIN) {
-      if (fork) {
-        DY_CUDA(cudaEventRecord(L->ev_join, L->aux));
-        DY_CUDA(cudaStreamWaitEvent(s, L->ev_join, 0));
-      }
-      continue;
-    }
-    cudaStream_t ks = (fork && st.aux) ? L->aux : s;
+    const cudaStream_t ks = s;
     switch (st.kind) {
       case Step::GEMM:
         DY_TIMED(rec, ks, tc_gemm_launch(st.p, st.a0, st.a1, st.b0, st.b1, st.out, ks));
         break;
-      case Step::CHOL_APPLY:
-        DY_TIMED(rec, ks, launch_chol_apply(st.G, st.batch, st.r, st.ridge, st.T, st.n, st.ldT, st.l0,
-                                            st.sTb, st.Ginv, st.status, ks));
+      case Step::SPD_SOLVE:
+        DY_TIMED(rec, ks, launch_spd_solve(st.G, st.batch, st.r, st.ridge, st.Ct, st.d, st.Cs,
+                                            st.Ginv, st.status, ks));
         break;
       case Step::NS_PREP:
         DY_TIMED(rec, ks,
@@ -717,8 +721,8 @@ dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream
         DY_TIMED(rec, ks, launch_monarch_permute(st.T, st.rows, st.ldT, st.nb, ks));
         break;
       case Step::NS_FINISH:
-        DY_TIMED(rec, ks,
-                 launch_ns_finish(st.Xf, st.dinv, st.batch, st.r, st.flags, st.Ginv, st.status, ks));
+        DY_TIMED(rec, ks, launch_ns_finish(st.Xf, st.dinv, st.batch, st.r, st.flags, st.Ginv,
+                                           st.G32, st.status, ks));
         break;
       default:
         break;
@@ -770,7 +774,7 @@ dyra_status forward_f32(const dyra_layer *L, const float *X, int batch, int n, f
   return DYRA_OK;
 }
 
-const char *const kNamesChol[] = {"xproj_static_L", "cg_c_gram", "chol_solve_apply",
+const char *const kNamesChol[] = {"xproj_static_L", "cg_c_gram", "spd_solve_c",
                                   "residual_product", "fused_output"};
 const char *const kNamesMonarchFront[] = {"monarch_bd1", "xproj_L", "monarch_permute"};
 const char *const kNamesF32[] = {"f32_xproj", "f32_gram_f64", "f32_c", "f32_b",
@@ -796,7 +800,7 @@ const char *kernel_name(const dyra_layer *L, int i) {
   if (i == 2) return "ns_prep";
   if (i < 3 + it2) return ((i - 3) % 2 == 0) ? "ns_gemm_gx" : "ns_gemm_update";
   if (i == 3 + it2) return "ns_finish";
-  if (i == 4 + it2) return "lsolve_apply";
+  if (i == 4 + it2) return "ginv_c";
   return kNamesChol[i - it2 - 2];   // residual_product, fused_output
 }
 
@@ -860,13 +864,8 @@ void free_device(dyra_layer *L) {
   if (L->bd1) cudaFree(L->bd1);
   if (L->bd2) cudaFree(L->bd2);
   if (L->bias_d) cudaFree(L->bias_d);
-  if (L->ev_fork) cudaEventDestroy(L->ev_fork);
-  if (L->ev_join) cudaEventDestroy(L->ev_join);
-  if (L->aux) cudaStreamDestroy(L->aux);
   L->w1 = L->v = L->wres = L->bd1 = L->bd2 = nullptr;
   L->bias_d = nullptr;
-  L->ev_fork = L->ev_join = nullptr;
-  L->aux = nullptr;
 }
 
 // Monarch fit: each (a, c) block of W gets its leading singular triplet.
@@ -1089,12 +1088,6 @@ dyra_status upload_layer(const dyra_prepare_args *a, dyra_layer *L) {
     if (st == DYRA_OK) st = upload(&L->v, vv);
     if (st == DYRA_OK) st = upload(&L->wres, wr);
   }
-  if (a->dtype == DYRA_BF16 && st == DYRA_OK) {
-    cudaError_t e = cudaStreamCreateWithFlags(&L->aux, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming);
-    if (e != cudaSuccess) st = cuda_fail(e, "auxiliary stream / events");
-  }
   if (st == DYRA_OK) {
     void *bp = nullptr;
     st = upload(&bp, bias32);
@@ -1213,7 +1206,7 @@ void dyra_layer_destroy(dyra_layer *layer) {
   if (!layer) return;
   {
     DeviceGuard guard(layer->device);
-    if (layer->aux) cudaStreamSynchronize(layer->aux);
+    cudaDeviceSynchronize();   // no forward of this layer may still read its weights
     free_device(layer);
   }
   delete layer;
@@ -1318,8 +1311,9 @@ dyra_status dyra_workspace_tensor(const dyra_layer *L, int batch, int n, int whi
     case DYRA_BUF_C: off = w.C; l = L->d; break;
     case DYRA_BUF_G: off = w.G; l = L->r; break;
     case DYRA_BUF_GINV: off = w.Ginv; l = L->r; break;
-    case DYRA_BUF_B: off = w.B; l = L->m; break;
-    case DYRA_BUF_R: if (bf) return DYRA_ERR_UNSUPPORTED; off = w.R; l = L->m; break;
+    case DYRA_BUF_B: if (bf) return DYRA_ERR_UNSUPPORTED; off = w.B; l = L->m; break;
+    case DYRA_BUF_R: off = w.R; l = L->m; break;
+    case DYRA_BUF_CS: if (!bf) return DYRA_ERR_UNSUPPORTED; off = w.Cs; l = L->d; break;
     default: return DYRA_ERR_INVALID_ARG;
   }
   *offset_bytes = off;

@@ -6,15 +6,18 @@
 namespace dyra {
 
 // bf16 path, SPD solves (solve.cu)
-// (G + ridge I)^-1 for r <= 64, and L~ = L (G + ridge I)^-1 written over the L columns
-// [l0, l0 + r) of T [batch][n][ldT] (batch stride sTb elements); G^-1 also to Ginv (bf16).
-cudaError_t launch_chol_apply(const float *G, int batch, int r, float ridge, __nv_bfloat16 *T,
-                              int n, int ldT, int l0, long long sTb, __nv_bfloat16 *Ginv,
-                              int *status, cudaStream_t s);
+// C~ = (G + ridge I)^-1 C for r <= 64 (r % 4 == 0): G [batch][r][r] fp32, C given as
+// C^T [batch][d][r] fp32, C~ to Cs [batch][r][d] bf16; G^-1 also to Ginv [batch][r][r] bf16.
+cudaError_t launch_spd_solve(const float *G, int batch, int r, float ridge, const float *Ct,
+                             int d, __nv_bfloat16 *Cs, __nv_bfloat16 *Ginv, int *status,
+                             cudaStream_t s);
+// Newton-Schulz start: dinv = diag(G + ridge I)^-1/2, Gh = D (G + ridge I) D,
+// X0 = I / ||Gh||_inf; flags[b] marks a sample whose diagonal is not positive and finite.
 cudaError_t launch_ns_prep(const float *G, int batch, int r, float ridge, float *Gh, float *X0,
                            float *dinv, int *flags, cudaStream_t s);
+// G^-1 from the Newton-Schulz iterate: to Ginv (bf16) and G32 (fp32), both [batch][r][r].
 cudaError_t launch_ns_finish(const float *X, const float *dinv, int batch, int r, const int *flags,
-                             __nv_bfloat16 *Ginv, int *status, cudaStream_t s);
+                             __nv_bfloat16 *Ginv, float *G32, int *status, cudaStream_t s);
 
 // fp32 path (f32_path.cu)
 cudaError_t launch_sgemm(int batch, int M, int N, int K, const float *A, long long sAb,

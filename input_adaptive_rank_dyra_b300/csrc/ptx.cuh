@@ -103,6 +103,11 @@ __device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *
       : "memory");
 }
 
+// Brings the 128-byte line holding `ptr` into L1 (no register result, nothing waits on it).
+__device__ __forceinline__ void prefetch_l1(const void *ptr) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -36,6 +36,21 @@ __device__ __forceinline__ TileCoord decode_tile(int u, const TcGemmParams &p, i
   return c;
 }
 
+// K chunks of the tile (segmented mode: b_split plus one group of rank chunks per segment
+// that the unit's rows touch) and the first segment it touches.
+__device__ __forceinline__ int tile_chunks(const TcGemmParams &p, const TileCoord &tc, int crank,
+                                           int &s_lo) {
+  if (p.seg_n <= 0) {
+    s_lo = 0;
+    return p.k_chunks;
+  }
+  const int urow0 = (tc.m_tile - crank) * 128;   // first row of the CTA pair's unit
+  s_lo = urow0 / p.seg_n;
+  int s_hi = (urow0 + 128 * p.cluster - 1) / p.seg_n;
+  if (s_hi > p.seg_count - 1) s_hi = p.seg_count - 1;
+  return p.b_split + (s_hi - s_lo + 1) * (p.k_chunks - p.b_split);
+}
+
 // Epilogue of 16 accumulator columns [col0, col0 + 16) of row g, direct global stores
 // (the modes without a TMA store: C / G of the Gram kernel, fp32 Newton-Schulz products).
 __device__ __forceinline__ void epilogue16(const TcGemmParams &p, const float *f, long long g,
@@ -54,10 +69,10 @@ __device__ __forceinline__ void epilogue16(const TcGemmParams &p, const float *f
   } else if (p.epi == EPI_CG) {
     if (!second) {
       if (g < p.rows_valid) {
-        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + bz * p.out_bstride + g;
+        float *dst = reinterpret_cast<float *>(p.out) + bz * p.out_bstride + g * p.out_ld + col0;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (j < valid) dst[(long long)(col0 + j) * p.out_ld] = __float2bfloat16_rn(f[j]);
+          if (j < valid) dst[j] = f[j];
       }
     } else if (g < p.rows2_valid) {
       float *dst = reinterpret_cast<float *>(p.out2) + bz * p.out2_bstride + g * p.out2_ld + col0;
@@ -200,21 +215,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a_b = (a_second ? p.a_batched1 : p.a_batched0) ? tc.bz : 0;
         const int a_k0 = p.a_kdiag ? tc.n_tile * p.BN : 0;
         const int a_k1 = p.a_k1 >= 0 ? p.a_k1 : p.b_split * chunk;
-        for (int kc = 0; kc < p.k_chunks; ++kc) {
+        int s_lo;
+        const int kct = tile_chunks(p, tc, crank, s_lo);
+        const int rc = p.k_chunks - p.b_split;
+        int seg = 0, sc = 0;   // segmented mode: segment and chunk within it
+        for (int kc = 0; kc < kct; ++kc) {
           if (!ptx::mbar_wait(empty_bar + 8u * s, ph ^ 1u, p.timeouts)) {
             ok = false;
             break;
           }
           const uint32_t full = full_bar + 8u * s;
+          // K / row / batch coordinates and map of this chunk of A
+          const CUtensorMap *mk = ma;
+          int ka, arow = m0, ab = a_b;
+          if (kc < p.b_split) {
+            ka = a_k0 + kc * chunk;
+          } else if (p.seg_n > 0) {
+            const int sg = s_lo + seg;
+            mk = &tmA1;
+            ka = a_k1 + sc * chunk;
+            arow = tc.m_tile * 128 - sg * p.seg_n;
+            ab = sg;
+            if (++sc == rc) {
+              sc = 0;
+              ++seg;
+            }
+          } else {
+            ka = a_k1 + (kc - p.b_split) * chunk;
+          }
           if constexpr (PMMA) {
             // both CTAs' A land on the even CTA's full barrier, which expects them all
             if (leader) ptx::mbar_arrive_expect_tx(full, 2u * a_bytes);
-            const int ka = kc < p.b_split ? a_k0 + kc * chunk : a_k1 + (kc - p.b_split) * chunk;
-            ptx::tma_load_3d_pair(sa, ma, ptx::mapa_shared(full, 0), ka, m0, a_b);
+            ptx::tma_load_3d_pair(sa, mk, ptx::mapa_shared(full, 0), ka, arow, ab);
           } else if (p.a_major == 0) {
             ptx::mbar_arrive_expect_tx(full, a_bytes);
-            const int ka = kc < p.b_split ? a_k0 + kc * chunk : a_k1 + (kc - p.b_split) * chunk;
-            ptx::tma_load_3d(sa, ma, full, ka, m0, a_b);
+            ptx::tma_load_3d(sa, mk, full, ka, arow, ab);
           } else {
             ptx::mbar_arrive_expect_tx(full, a_bytes);
             for (int i = 0; i < 128 / chunk; ++i)
@@ -240,7 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileCoord tc = decode_tile(t, p, mp_tiles, crank);
         const int n0 = tc.n_tile * p.BN;
         const int b_b0 = p.b_batched0 ? tc.bz : 0, b_b1 = p.b_batched1 ? tc.bz : 0;
-        for (int kc = 0; kc < p.k_chunks; ++kc) {
+        int s_lo;
+        const int kct = tile_chunks(p, tc, crank, s_lo);
+        const int rc = p.k_chunks - p.b_split;
+        int seg = 0, sc = 0;
+        for (int kc = 0; kc < kct; ++kc) {
           if (!ptx::mbar_wait(empty_bar + 8u * s, ph ^ 1u, p.timeouts)) {
             ok = false;
             break;
@@ -248,8 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full = full_bar + 8u * s;
           const bool b_second = kc >= p.b_split;
           const CUtensorMap *mb = b_second ? &tmB1 : &tmB0;
-          const int kk = b_second ? kc - p.b_split : kc;
-          const int b_b = b_second ? b_b1 : b_b0;
+          int kk = b_second ? kc - p.b_split : kc;
+          int b_b = b_second ? b_b1 : b_b0;
+          if (b_second && p.seg_n > 0) {
+            kk = sc;
+            b_b = s_lo + seg;
+            if (++sc == rc) {
+              sc = 0;
+              ++seg;
+            }
+          }
           if constexpr (PMMA) {
             if (leader) ptx::mbar_arrive_expect_tx(full, 2u * b_bytes);
             const uint32_t fb = ptx::mapa_shared(full, 0);
@@ -316,7 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ptx::mbar_wait(tempty_bar + 8u * acc, ((i >> 1) & 1u) ^ 1u, p.timeouts)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * p.acc_cols;
-        for (int kc = 0; kc < p.k_chunks; ++kc) {
+        int s_lo;
+        const int kct = p.seg_n > 0 ? tile_chunks(p, decode_tile(t, p, mp_tiles, crank), crank, s_lo)
+                                    : p.k_chunks;
+        for (int kc = 0; kc < kct; ++kc) {
           if (!ptx::mbar_wait(full_bar + 8u * s, ph, p.timeouts)) {
             ok = false;
             break;
@@ -384,12 +434,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t buf_i = 0, i = 0;
     for (int t = cid; t < total; t += ncl, ++i) {
       const uint32_t acc = i & 1u;
+      const TileCoord tc = decode_tile(t, p, mp_tiles, crank);
+      if (p.bias && p.tma_store) {
+        // the bias lines of this warp's columns (at most 4 x 128 B) reach L1 while the
+        // accumulator is still being computed
+        const int pc = tc.n_tile * p.BN + c_lo + lane * 32;
+        if (lane < 4 && pc < p.cols_valid && c_lo + lane * 32 < c_hi) ptx::prefetch_l1(p.bias + pc);
+      }
       int got = 0;
       if (lane == 0) got = ptx::mbar_wait(tfull_bar + 8u * acc, (i >> 1) & 1u, p.timeouts) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       ptx::tc_fence_after();
-      const TileCoord tc = decode_tile(t, p, mp_tiles, crank);
       if (tc.m_tile >= p.m_tiles) {   // a pair's tile past the last M tile: nothing to store
         ptx::tc_fence_before();
         __syncwarp();
@@ -433,11 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               f[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + bb.z;
               f[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + bb.w;
             }
+          } else if (!p.bias) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) f[j] = __uint_as_float(v[j]);
           } else {
 #pragma unroll
             for (int j = 0; j < 64; ++j)
-              f[j] = __uint_as_float(v[j]) +
-                     ((p.bias && col0 + j < cols_lim) ? __ldg(p.bias + col0 + j) : 0.f);
+              f[j] = __uint_as_float(v[j]) + (col0 + j < cols_lim ? __ldg(p.bias + col0 + j) : 0.f);
           }
           if (lane == 0) ptx::bulk_wait_read<1>();   // this pair's previous stores have read it
           __syncwarp();
@@ -592,6 +650,14 @@ static int max_active_pairs(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, 
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
+  // the query takes the cluster shape alone
+  cudaLaunchAttribute cl = {};
+  cl.id = cudaLaunchAttributeClusterDimension;
+  cl.val.clusterDim.x = 2;
+  cl.val.clusterDim.y = 1;
+  cl.val.clusterDim.z = 1;
+  cfg.attrs = &cl;
+  cfg.numAttrs = 1;
   cfg.gridDim = dim3(2, 1, 1);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
@@ -624,6 +690,8 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
   if ((p.b_major || p.b_major1) && p.BN % 64) return cudaErrorInvalidValue;
   p.acc_cols = 32;
   while (p.acc_cols < (uint32_t)p.BN) p.acc_cols <<= 1;
+  if (p.seg_n > 0 && (p.batch != 1 || p.a_major || p.seg_count <= 0 || p.k_chunks <= p.b_split))
+    return cudaErrorInvalidValue;
   if (p.pair_mma) {
     p.cluster = 2;
     if (p.BN % 32) return cudaErrorInvalidValue;                   // halves of whole 8-row groups
@@ -661,13 +729,11 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
     cfg.gridDim = dim3((unsigned)(units < num_sms() ? units : num_sms()), 1, 1);
     return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<false>, a0, a1, b0, b1, out_map, p);
   }
-  // cluster launches go without the programmatic-serialization attribute; their pdl_wait
-  // then returns at once
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.numAttrs = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.numAttrs = 2;
   auto kern = p.pair_mma ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
   const int max_clusters = max_active_pairs(kern, cfg, p.pair_mma != 0);
   const long long clusters = units < max_clusters ? units : max_clusters;

@@ -32,8 +32,8 @@ namespace dyra {
 
 enum TcEpi : int {
   EPI_ROW_BF16 = 0,    // out[b][g][c] = bf16(acc + bias[c]); TMA store when tma_store is set
-  EPI_CG = 2,          // m tiles < a_split: out[b*bs + c*ld + g] = bf16(acc)   (C from C^T)
-                       // m tiles >= a_split: out2[b*bs2 + g*ld2 + c] = acc    (G, fp32)
+  EPI_CG = 2,          // m tiles < a_split: out[b*bs + g*ld + c] = acc     (C^T, fp32)
+                       // m tiles >= a_split: out2[b*bs2 + g*ld2 + c] = acc  (G, fp32)
   EPI_ROW_F32 = 3,     // out[b][g][c] = alpha*acc + beta*aux[b][g][c]   (fp32)
   EPI_TRANS_F32 = 4    // out[b*bs + (g/rb)*gs + g%rb + c*ld] = alpha*acc (fp32)
 };
@@ -62,6 +62,13 @@ struct TcGemmParams {
                      // contracts with the same range of K)
   int a_k1;          // K coordinate of A (elements) read by chunk b_split; later chunks follow
                      // it. < 0: contiguous with the chunks before (b_split * chunk)
+  int seg_n;         // > 0: flat M over `seg_count` segments (samples) of seg_n rows each.
+                     // Chunks >= b_split then repeat once per segment that the rows of the
+                     // tile (of the CTA pair, for pair MMAs) touch: A from map A1 as
+                     // [segment][seg_n][inner] at row (first row of the tile - segment start),
+                     // whose rows outside the segment read as zeros, and B from map B1 with
+                     // the segment as its batch coordinate. Needs batch = 1, K-major A.
+  int seg_count;
   uint32_t idesc;
   uint32_t idesc1;   // instruction descriptor of the chunks read from map B1
   uint32_t acc_cols;  // TMEM columns of one accumulator (power of two >= BN)

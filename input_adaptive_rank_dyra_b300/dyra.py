@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "OOM"
 KINDS = {"lowrank": 0, "monarch": 1}
 DTYPES = {"f32": 0, "bf16": 1}
 SOLVERS = {"auto": 0, "cholesky": 1, "newton_schulz": 2}
-BUFFERS = {"T": 0, "C": 1, "G": 2, "GINV": 3, "B": 4, "R": 5}
+BUFFERS = {"T": 0, "C": 1, "G": 2, "GINV": 3, "B": 4, "R": 5, "CS": 6}
 
 _c_double_p = ctypes.POINTER(ctypes.c_double)
 

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for name in declared:
         assert hasattr(lib, name), name
     assert set(declared) <= set(D.EXPORTED)
-    assert lib.dyra_abi_version() == 1
+    assert lib.dyra_abi_version() == 2
 
 
 def test_status_strings():

@@ -70,7 +70,8 @@ def test_forward_matches_oracle(name, batch, n):
 
 @pytest.mark.parametrize("name", ["c1", "c2", "c4"])
 def test_intermediates_match_oracle(name):
-    """Each kernel's output in the workspace: [XU | L] (or L G^-1), G, C, G^-1, B."""
+    """Each kernel's output in the workspace: [XU | L], G, C, G^-1, then G^-1 C (bf16) or
+    B = C W_res (fp32), and R = G^-1 C W_res."""
     import torch
     import input_adaptive_rank_dyra_b300 as dy
     cfg = WL.reduced(WL.get_config(name), batch=None if name == "c1" else 2,
@@ -104,27 +105,38 @@ def test_intermediates_match_oracle(name):
     assert rel(G, Go) <= t
     Gi = to_host(dy.workspace_view(layer, ws, B_, n, "GINV", (B_, r, r), ft if bf else gdt))
     assert rel(Gi, Gi_o) <= t
-    C = to_host(dy.workspace_view(layer, ws, B_, n, "C", (B_, r, d), ft))
-    assert rel(C, np.stack(inter["C"])) <= t
-    Bo = np.stack(inter["B"])
-    if bf:
-        kp = ldT - r
-        assert rel(T[:, :, kp:kp + r], Lo @ Gi_o) <= t      # L G^-1 over the L columns
-        Bm = to_host(dy.workspace_view(layer, ws, B_, n, "B", (B_, r, m), ft))
-        assert rel(Bm, Bo) <= t
+    if bf:   # C^T [batch, d, r], fp32
+        C = to_host(dy.workspace_view(layer, ws, B_, n, "C", (B_, d, r), torch.float32))
+        C = C.transpose(0, 2, 1)
     else:
-        assert rel(T[:, :, k:k + r], Lo) <= t
+        C = to_host(dy.workspace_view(layer, ws, B_, n, "C", (B_, r, d), ft))
+    assert rel(C, np.stack(inter["C"])) <= t
+    kl = ldT - r   # first L column of T
+    assert rel(T[:, :, kl:kl + r], Lo) <= t
+    if bf:
+        # the solve runs on C before the residual product: C~ = G^-1 C, then R = C~ W_res
+        Cs = to_host(dy.workspace_view(layer, ws, B_, n, "CS", (B_, r, d), ft))
+        assert rel(Cs, Gi_o @ np.stack(inter["C"])) <= t
+    else:
         Bm = to_host(dy.workspace_view(layer, ws, B_, n, "B", (B_, r, m), ft))
-        assert rel(Bm, Bo) <= t
-        R = to_host(dy.workspace_view(layer, ws, B_, n, "R", (B_, r, m), ft))
-        assert rel(R, np.stack(inter["R"])) <= t
+        assert rel(Bm, np.stack(inter["B"])) <= t
+    R = to_host(dy.workspace_view(layer, ws, B_, n, "R", (B_, r, m), ft))
+    assert rel(R, np.stack(inter["R"])) <= t
 
 
 # ---------------------------------------------------------------------------- edge cases
 
-@pytest.mark.parametrize("n", [1, 5, 64, 127, 128, 129, 200])
-def test_token_counts_spanning_tiles(n):
-    cfg = WL.reduced(WL.get_config("c2"), batch=2, n=n)
+# (batch, n): token counts around the 128-row tile and the 256-row CTA-pair unit. With more
+# than one sample and n not a multiple of 256 the output GEMM tiles the flat batch * n rows,
+# so a unit can hold the tail of one sample and the head of the next (or, for n < 128,
+# parts of up to five samples); 256 and 512 keep the per-sample tiles.
+TOKEN_CASES = [(2, 1), (2, 5), (2, 64), (2, 127), (2, 128), (2, 129), (2, 200), (7, 70),
+               (5, 100), (3, 256), (4, 600), (2, 512)]
+
+
+@pytest.mark.parametrize("batch,n", TOKEN_CASES)
+def test_token_counts_spanning_tiles(batch, n):
+    cfg = WL.reduced(WL.get_config("c2"), batch=batch, n=n)
     W, b, prep = weights_and_prep("c2")
     X = WL.make_inputs(cfg)
     layer = make_layer(cfg, prep, W, b)
@@ -132,6 +144,9 @@ def test_token_counts_spanning_tiles(n):
     Yg = to_host(Y)
     Yo = O.forward(X, prep)
     assert rel(Yg, Yo) <= BF16_TOL
+    # every sample on its own: a wrong segment would corrupt one sample's rows only
+    for s in range(batch):
+        assert rel(Yg[s], Yo[s]) <= BF16_TOL, f"sample {s}"
 
 
 @pytest.mark.parametrize("name", ["c1", "c2"])

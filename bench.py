@@ -56,10 +56,15 @@ def peaks():
 
 
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the kernel's source files with // comments and blank space removed, so that
+    editing a comment does not invalidate a recorded capture."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES.get(kernel, GEMM_SOURCES):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:12]
 
 

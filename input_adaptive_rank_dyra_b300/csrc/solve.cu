@@ -7,10 +7,10 @@
 // count.
 //   * r <= 64 (the Cholesky branch): spd_solve. Every CTA takes one sample and 128 columns
 //     of C. It inverts G + lambda I (padded to R x R, R = 32 or 64, by the identity) in place
-//     by symmetric sweeps -- Gauss-Jordan without pivoting, whose pivots on an SPD matrix are
-//     the squared diagonal of the Cholesky factor -- with the matrix spread over the CTA's
-//     registers, then forms its columns of C~ (fp32 FMA). CTAs of the first column block also
-//     store G^-1 (bf16).
+//     by block sweeps on 4 x 4 pivot blocks -- Gauss-Jordan without pivoting, whose scalar
+//     pivots on an SPD matrix are the squared diagonal of the Cholesky factor -- with the
+//     matrix spread over the CTA's registers, then forms its columns of C~ (fp32 FMA). CTAs
+//     of the first column block also store G^-1 (bf16).
 //   * larger r: Newton-Schulz. ns_prep scales G symmetrically to unit diagonal and sets
 //     X0 = I / ||G_hat||_inf; the iterations X <- X (2I - G_hat X) run as tf32 tensor-core
 //     GEMMs (tc_gemm); ns_finish undoes the scaling; a bf16 tensor-core GEMM then forms
@@ -28,34 +28,75 @@ namespace {
 
 constexpr int kSolveCols = 128;   // columns of C per spd_solve CTA
 
-// Threads of spd_solve for the padded size R: each holds a BR x BC block of the matrix.
+// Threads of spd_solve for the padded size R (the elimination uses (R / 4)^2 of them).
 template <int R>
 __host__ __device__ constexpr int solve_threads() { return R == 32 ? 128 : 256; }
 
-// (G + ridge I)^-1 for one sample by in-place symmetric sweeps (Gauss-Jordan without
-// pivoting; on an SPD matrix the pivots are the positive Schur complements that a Cholesky
-// factorisation squares), then C~ = G^-1 C for kSolveCols columns of C. With s_i = a_ik / a_kk
-// the sweep on pivot k is
-//   a_ij -= s_i a_kj  (i, j != k),   a_ik = a_ki = s_i,   a_kk = -1 / a_kk,
-// and after the sweeps on k = 0 .. r-1 the matrix holds -(G + ridge I)^-1. Every thread
-// keeps its BR x BC block in registers; the pivot column (= pivot row, by symmetry) goes
-// through a double-buffered shared-memory vector, so each sweep costs one barrier. The
-// inverse then goes to shared memory and every thread forms rows of C~ for its column as
-// dot products with broadcast rows of the inverse.
+// p = -(m^-1) of an SPD 4 x 4 block by four scalar sweeps; false if a pivot is not positive
+// and finite.
+__device__ __forceinline__ bool sweep4(const float (&m)[4][4], float (&p)[4][4]) {
+  float w[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[i][j] = m[i][j];
+  bool ok = true;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float dk = w[k][k];
+    ok = ok && dk > 0.f && dk < INFINITY;
+    const float di = 1.f / dk;
+    float c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = w[i][k];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[i][j] = fmaf(-c[i] * di, c[j], w[i][j]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[k][i] = c[i] * di;
+      w[i][k] = c[i] * di;
+    }
+    w[k][k] = -di;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) p[i][j] = w[i][j];
+  return ok;
+}
+
+// (G + ridge I)^-1 for one sample by in-place block sweeps on 4 x 4 pivot blocks (block
+// Gauss-Jordan without pivoting; on an SPD matrix the pivot blocks are SPD Schur complements,
+// whose scalar pivots are the squared diagonal of the Cholesky factor), then
+// C~ = G^-1 C for kSolveCols columns of C. With K the pivot block, P = A_KK^-1 and
+// S_i = A_iK P, one block sweep is
+//   A_ij -= S_i A_Kj  (i, j outside K),  A_iK = S_i,  A_Kj = P A_Kj,  A_KK = -P,
+// and after the sweeps over all blocks the matrix holds -(G + ridge I)^-1 (the identity
+// padding up to R x R is never swept). Each of (R/4)^2 threads keeps one 4 x 4 block in
+// registers. The pivot columns of the next step (rows of 4, = its pivot rows by symmetry) and
+// the inverse of its pivot block, which the owner of that block forms after its update, go
+// through double-buffered shared memory: one barrier per step, r / 4 steps. The inverse then
+// goes to shared memory and every thread forms rows of C~ for its column as dot products with
+// broadcast rows of the inverse.
 template <int R>
 __global__ void __launch_bounds__(solve_threads<R>())
     spd_solve_kernel(const float *__restrict__ G, int r, float ridge,
                      const float *__restrict__ Ct, int d, __nv_bfloat16 *__restrict__ Cs,
                      __nv_bfloat16 *__restrict__ Ginv, int *status) {
   constexpr int NT = solve_threads<R>();
-  constexpr int BR = R == 32 ? 2 : 4, BC = 4, QC = R / BC;
-  static_assert((R / BR) * QC == NT, "thread blocks must tile the matrix");
+  constexpr int Q = R / 4, NS = Q * Q;   // 4 x 4 blocks per side, elimination threads
+  static_assert(NS <= NT, "every block needs a thread");
   constexpr int TPC = NT / kSolveCols;   // threads per column in the apply
-  __shared__ __align__(16) float colbuf[2][R];
+  __shared__ __align__(16) float colbuf[2][R][4];   // the step's pivot columns A_iK
+  __shared__ __align__(16) float pinv[2][4][4];     // P of the step
   __shared__ __align__(16) float Ai[R][R + 4];
+  __shared__ int bad_s;
   const int tid = threadIdx.x, b = blockIdx.y;
-  const int i0 = (tid / QC) * BR, j0 = (tid % QC) * BC;
-  // this thread's column of C (row of C^T), loaded first so the loads overlap the sweeps
+  const bool el = tid < NS;   // takes part in the elimination
+  const int i0 = (tid / Q) * 4, j0 = (tid % Q) * 4;
+  // this thread's column of C (row of C^T), loaded first so the loads overlap the elimination
   const int col = blockIdx.x * kSolveCols + tid % kSolveCols;
   float x[R];
   {
@@ -69,74 +110,112 @@ __global__ void __launch_bounds__(solve_threads<R>())
       x[i4 + 3] = v.w;
     }
   }
-  float a[BR][BC];
-  const float *g = G + (size_t)b * r * r;
+  float a[4][4];
+  if (el) {
+    const float *g = G + (size_t)b * r * r;
 #pragma unroll
-  for (int u = 0; u < BR; ++u)
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
-    for (int v = 0; v < BC; ++v) {
-      const int i = i0 + u, j = j0 + v;
-      a[u][v] = (i < r && j < r) ? g[i * r + j] + (i == j ? ridge : 0.f) : (i == j ? 1.f : 0.f);
-    }
-  if (j0 == 0) {
+      for (int v = 0; v < 4; ++v) {
+        const int i = i0 + u, j = j0 + v;
+        a[u][v] = (i < r && j < r) ? g[i * r + j] + (i == j ? ridge : 0.f) : (i == j ? 1.f : 0.f);
+      }
+  }
+  if (tid == 0) bad_s = 0;
+  __syncthreads();
+  if (el && j0 == 0) {
 #pragma unroll
-    for (int u = 0; u < BR; ++u) colbuf[0][i0 + u] = a[u][0];
+    for (int u = 0; u < 4; ++u)
+      *reinterpret_cast<float4 *>(colbuf[0][i0 + u]) = make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
+  }
+  if (tid == 0) {   // owner of the first pivot block
+    float p[4][4];
+    if (!sweep4(a, p)) bad_s = 1;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) pinv[0][u][v] = -p[u][v];
   }
   __syncthreads();
-  bool bad = false;   // the same in every thread: every pivot is read from shared memory
-  for (int k = 0; k < r; ++k) {
-    const float *cur = colbuf[k & 1];
-    const float piv = cur[k];
-    if (!(piv > 0.f && piv < INFINITY)) bad = true;
-    const float dinv = 1.f / piv;
-    float ci[BR], cj[BC];
+  const int steps = r / 4;
+  for (int kb = 0; kb < steps; ++kb) {
+    const int k0 = kb * 4, cur = kb & 1;
+    if (el) {
+      float P[4][4], crow[4][4], ccol[4][4];
 #pragma unroll
-    for (int u = 0; u < BR; ++u) ci[u] = cur[i0 + u];
-    {
-      const float4 c4 = *reinterpret_cast<const float4 *>(cur + j0);
-      cj[0] = c4.x;
-      cj[1] = c4.y;
-      cj[2] = c4.z;
-      cj[3] = c4.w;
-    }
+      for (int u = 0; u < 4; ++u) {
+        const float4 pp = *reinterpret_cast<const float4 *>(pinv[cur][u]);
+        const float4 cr = *reinterpret_cast<const float4 *>(colbuf[cur][i0 + u]);
+        const float4 cc = *reinterpret_cast<const float4 *>(colbuf[cur][j0 + u]);
+        P[u][0] = pp.x; P[u][1] = pp.y; P[u][2] = pp.z; P[u][3] = pp.w;
+        crow[u][0] = cr.x; crow[u][1] = cr.y; crow[u][2] = cr.z; crow[u][3] = cr.w;
+        ccol[u][0] = cc.x; ccol[u][1] = cc.y; ccol[u][2] = cc.z; ccol[u][3] = cc.w;
+      }
+      const bool rowsK = i0 == k0, colsK = j0 == k0;
+      if (rowsK && colsK) {
 #pragma unroll
-    for (int u = 0; u < BR; ++u) {
-      const float si = ci[u] * dinv;
+        for (int u = 0; u < 4; ++u)
 #pragma unroll
-      for (int v = 0; v < BC; ++v) a[u][v] = fmaf(-si, cj[v], a[u][v]);
-    }
-    if ((unsigned)(k - i0) < (unsigned)BR) {   // row k: a_kj = a_kj / a_kk
+          for (int v = 0; v < 4; ++v) a[u][v] = -P[u][v];
+      } else if (rowsK) {   // A_Kj = P A_Kj = (A_jK P)^T
 #pragma unroll
-      for (int u = 0; u < BR; ++u)
-        if (i0 + u == k) {
+        for (int v = 0; v < 4; ++v)
 #pragma unroll
-          for (int v = 0; v < BC; ++v) a[u][v] = cj[v] * dinv;
+          for (int u = 0; u < 4; ++u) {
+            float t = 0.f;
+#pragma unroll
+            for (int l = 0; l < 4; ++l) t = fmaf(ccol[v][l], P[l][u], t);
+            a[u][v] = t;
+          }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float S[4];   // S_i = A_iK P
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            float t = 0.f;
+#pragma unroll
+            for (int l = 0; l < 4; ++l) t = fmaf(crow[u][l], P[l][m], t);
+            S[m] = t;
+          }
+          if (colsK) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) a[u][v] = S[v];
+          } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+#pragma unroll
+              for (int m = 0; m < 4; ++m) a[u][v] = fmaf(-S[m], ccol[v][m], a[u][v]);
+          }
         }
-    }
-    if ((unsigned)(k - j0) < (unsigned)BC) {   // column k: a_ik = a_ik / a_kk; a_kk = -1 / a_kk
+      }
+      const int kn = k0 + 4;   // the next pivot block, after this step
+      if (kn < r) {
+        if (j0 == kn) {
 #pragma unroll
-      for (int v = 0; v < BC; ++v)
-        if (j0 + v == k) {
-#pragma unroll
-          for (int u = 0; u < BR; ++u) a[u][v] = (i0 + u == k) ? -dinv : ci[u] * dinv;
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<float4 *>(colbuf[cur ^ 1][i0 + u]) =
+                make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
         }
-    }
-    const int kn = k + 1;   // the next pivot column, after this sweep
-    if (kn < r && (unsigned)(kn - j0) < (unsigned)BC) {
-      float *nxt = colbuf[kn & 1];
+        if (i0 == kn && j0 == kn) {
+          float p[4][4];
+          if (!sweep4(a, p)) bad_s = 1;
 #pragma unroll
-      for (int v = 0; v < BC; ++v)
-        if (j0 + v == kn) {
+          for (int u = 0; u < 4; ++u)
 #pragma unroll
-          for (int u = 0; u < BR; ++u) nxt[i0 + u] = a[u][v];
+            for (int v = 0; v < 4; ++v) pinv[cur ^ 1][u][v] = -p[u][v];
         }
+      }
     }
     __syncthreads();
   }
+  const bool bad = bad_s != 0;
+  if (el) {
 #pragma unroll
-  for (int u = 0; u < BR; ++u)
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
-    for (int v = 0; v < BC; ++v) Ai[i0 + u][j0 + v] = bad ? 0.f : -a[u][v];
+      for (int v = 0; v < 4; ++v) Ai[i0 + u][j0 + v] = bad ? 0.f : -a[u][v];
+  }
   __syncthreads();
   if (blockIdx.x == 0) {
     for (int t = tid; t < r * r; t += NT)
@@ -144,20 +223,21 @@ __global__ void __launch_bounds__(solve_threads<R>())
     if (tid == 0 && bad) atomicAdd(status, 1);
   }
   if (col >= d) return;
-  // C~[i][col] = sum_j G^-1[i][j] C[j][col]; the TPC threads of a column split the rows
+  // C~[i][col] = sum_j G^-1[i][j] C[j][col]; the TPC threads of a column split the rows, four
+  // independent partial sums per row
   __nv_bfloat16 *op = Cs + (size_t)b * r * d + col;
   for (int i = tid / kSolveCols; i < r; i += TPC) {
     const float4 *ar = reinterpret_cast<const float4 *>(&Ai[i][0]);
-    float acc = 0.f;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
     for (int j4 = 0; j4 < R / 4; ++j4) {
       const float4 w = ar[j4];
-      acc = fmaf(w.x, x[4 * j4], acc);
-      acc = fmaf(w.y, x[4 * j4 + 1], acc);
-      acc = fmaf(w.z, x[4 * j4 + 2], acc);
-      acc = fmaf(w.w, x[4 * j4 + 3], acc);
+      s0 = fmaf(w.x, x[4 * j4], s0);
+      s1 = fmaf(w.y, x[4 * j4 + 1], s1);
+      s2 = fmaf(w.z, x[4 * j4 + 2], s2);
+      s3 = fmaf(w.w, x[4 * j4 + 3], s3);
     }
-    op[(size_t)i * d] = __float2bfloat16_rn(acc);
+    op[(size_t)i * d] = __float2bfloat16_rn((s0 + s1) + (s2 + s3));
   }
 }
 

@@ -2,24 +2,30 @@
 // stored K-contiguous ("K-major") or MN-contiguous, fp32 accumulation in TMEM.
 //
 // Persistent kernel: a grid of at most one CTA per SM walks the tiles (batch, m tile,
-// n tile), n fastest, in a static round-robin. With cluster = 2 the unit of that walk is a
-// pair of M tiles handled by the two CTAs of a cluster, which share the B tile: each loads
-// half of it and multicasts it to both, which halves the L2 reads of B. Each CTA has
-// these warps:
-//   warp 0      TMA producer (one lane): 128-byte K chunks of A (128 rows) and B (BN rows)
-//               into a ring of smem stages; it runs ahead across tile boundaries
+// n tile), n fastest, in a static round-robin. Two cluster modes pair CTAs on adjacent M
+// tiles of one (batch, N tile):
+//   * pair MMA (cta_group::2): a 256-row unit; each CTA loads its 128 rows of A and half of
+//     the B tile, the even CTA issues the MMAs for both, and each CTA's TMEM receives its own
+//     128 rows;
+//   * multicast: each CTA loads half of the B tile and multicasts it to both.
+// Each CTA has these warps:
+//   warp 0      TMA issuer for A (one lane): 128-byte K chunks (128 rows) into a ring of
+//               shared-memory stages; it runs ahead across tile boundaries
 //   warp 1      TMEM allocation and MMA issue (one lane): 4 MMAs (32 bytes of K each) per
 //               chunk into one of two TMEM accumulators, so the epilogue of tile i overlaps
 //               the main loop of tile i+1
-//   warps 2..5  epilogue: tcgen05.ld of the 128 x BN accumulator (one TMEM lane quarter per
-//               warp, one row per thread), then the epilogue mode below; row-major bf16
-//               results go through swizzled smem staging buffers and TMA bulk stores
+//   warp 2      TMA issuer for B (one lane)
+//   warps 4..11 epilogue, two warps per TMEM lane quarter (each a column half): tcgen05.ld
+//               of the accumulator (one row per thread), then the epilogue mode below;
+//               row-major bf16 results go through 64-byte-swizzled shared-memory staging
+//               tiles and TMA bulk stores
 // Operands are bf16 (kind::f16, K-major or MN-major) or fp32 read as tf32 (kind::tf32,
 // K-major only), always in the 128-byte swizzled layout that TMA writes. The B operand
 // may switch major-ness at the K chunk b_split (e.g. a K-major weight followed by an
-// MN-major per-sample factor).
+// MN-major per-sample factor). In segmented mode (seg_n) the M rows are the flat rows of
+// several samples and the chunks from b_split on repeat once per sample a unit touches.
 //
-// The two issuing threads run short dependent instruction chains, so their loops keep
+// The issuing threads run short dependent instruction chains, so their loops keep
 // everything precomputed: shared-memory descriptors are built once and advanced by adding
 // to their address field, the ring position advances by increment and wrap, and no
 // division happens inside the K loop.

@@ -242,72 +242,82 @@ __global__ void __launch_bounds__(solve_threads<R>())
 }
 
 // Jacobi scaling and start of Newton-Schulz: dinv = diag(G + lambda I)^-1/2,
-// G_hat = D (G + lambda I) D, X0 = I / max_i sum_j |G_hat_ij|.
-__global__ void __launch_bounds__(256)
+// G_hat = D (G + lambda I) D, X0 = I / max_i sum_j |G_hat_ij|. One CTA of kNsThreads per
+// sample; a warp per row, so every load and store is coalesced and row sums are warp
+// reductions.
+constexpr int kNsThreads = 1024;
+
+__global__ void __launch_bounds__(kNsThreads)
     ns_prep_kernel(const float *__restrict__ G, int r, float ridge, float *__restrict__ Gh,
                    float *__restrict__ X0, float *__restrict__ dinv, int *__restrict__ flags) {
   __shared__ float sd[256];
-  __shared__ float red[256];
-  __shared__ int bad;
-  const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  __shared__ float red[kNsThreads / 32];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kNsThreads / 32;
   const float *g = G + (size_t)b * r * r;
-  if (tid == 0) bad = 0;
-  __syncthreads();
-  for (int i = tid; i < r; i += nt) {
-    const float gii = g[(size_t)i * r + i] + ridge;
-    float v = 0.f;
-    if (gii > 0.f && isfinite(gii)) v = rsqrtf(gii);
-    else bad = 1;
-    sd[i] = v;
+  bool bad = false;
+  if (tid < r) {
+    const float gii = g[(size_t)tid * r + tid] + ridge;
+    bad = !(gii > 0.f && gii < INFINITY);
+    sd[tid] = bad ? 0.f : rsqrtf(gii);
   }
-  __syncthreads();
+  bad = __syncthreads_or(bad) != 0;
   float mx = 0.f;
-  for (int i = tid; i < r; i += nt) {
+  for (int i = warp; i < r; i += NW) {
     float rs = 0.f;
-    for (int j = 0; j < r; ++j) {
+    for (int j = lane; j < r; j += 32) {
       float v = (g[(size_t)i * r + j] + (i == j ? ridge : 0.f)) * sd[i] * sd[j];
-      if (bad) v = 0.f;
+      v = bad ? 0.f : v;
       Gh[(size_t)b * r * r + (size_t)i * r + j] = v;
       rs += fabsf(v);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
     mx = fmaxf(mx, rs);
   }
-  red[tid] = mx;
+  if (lane == 0) red[warp] = mx;
   __syncthreads();
-  for (int s = nt / 2; s > 0; s >>= 1) {
-    if (tid < s) red[tid] = fmaxf(red[tid], red[tid + s]);
-    __syncthreads();
+  if (warp == 0) {
+    float m = red[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[0] = m;
   }
+  __syncthreads();
   const float alpha = (bad || !(red[0] > 0.f)) ? 0.f : 1.f / red[0];
-  for (int t = tid; t < r * r; t += nt) {
-    const int i = t / r, j = t % r;
+  for (int t = tid; t < r * r; t += kNsThreads) {
+    const int i = t / r, j = t - i * r;
     X0[(size_t)b * r * r + t] = (i == j) ? alpha : 0.f;
   }
-  for (int i = tid; i < r; i += nt) dinv[(size_t)b * r + i] = bad ? 0.f : sd[i];
-  if (tid == 0) flags[b] = bad;
+  if (tid < r) dinv[(size_t)b * r + tid] = bad ? 0.f : sd[tid];
+  if (tid == 0) flags[b] = bad ? 1 : 0;
 }
 
-__global__ void __launch_bounds__(256)
+// G^-1 = D X_t D, to bf16 (workspace) and fp32 (operand of the apply GEMM). A sample whose
+// iterate is not finite, or whose start was already flagged, gets G^-1 = 0.
+__global__ void __launch_bounds__(kNsThreads)
     ns_finish_kernel(const float *__restrict__ X, const float *__restrict__ dinv, int r,
                      const int *__restrict__ flags, __nv_bfloat16 *__restrict__ Ginv,
                      float *__restrict__ G32, int *status) {
-  __shared__ int bad;
-  const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
-  if (tid == 0) bad = flags[b];
-  __syncthreads();
-  for (int t = tid; t < r * r; t += nt) {
-    const float v = X[(size_t)b * r * r + t];
-    if (!isfinite(v)) bad = 1;
-  }
-  __syncthreads();
+  const int b = blockIdx.x, tid = threadIdx.x;
   const float *dv = dinv + (size_t)b * r;
-  for (int t = tid; t < r * r; t += nt) {
-    const int i = t / r, j = t % r;
-    const float v = bad ? 0.f : X[(size_t)b * r * r + t] * dv[i] * dv[j];
-    Ginv[(size_t)b * r * r + t] = __float2bfloat16_rn(v);
-    G32[(size_t)b * r * r + t] = v;
+  const size_t base = (size_t)b * r * r;
+  bool bad = flags[b] != 0;
+  for (int t = tid; t < r * r; t += kNsThreads) {
+    const int i = t / r, j = t - i * r;
+    const float x = X[base + t];
+    bad = bad || !(fabsf(x) < INFINITY);
+    const float v = x * dv[i] * dv[j];
+    Ginv[base + t] = __float2bfloat16_rn(v);
+    G32[base + t] = v;
   }
-  if (tid == 0 && bad) atomicAdd(status, 1);
+  if (__syncthreads_or(bad)) {   // rare: overwrite the sample with zeros
+    for (int t = tid; t < r * r; t += kNsThreads) {
+      Ginv[base + t] = __float2bfloat16_rn(0.f);
+      G32[base + t] = 0.f;
+    }
+    if (tid == 0) atomicAdd(status, 1);
+  }
 }
 
 }  // namespace
@@ -317,6 +327,7 @@ cudaError_t launch_spd_solve(const float *G, int batch, int r, float ridge, cons
                              cudaStream_t s) {
   if (r <= 0 || r > 64 || r % 4 || d <= 0) return cudaErrorInvalidValue;
   if (batch <= 0) return cudaSuccess;
+  // a plain launch: the GEMM after it reads C~ through TMA only once this grid has completed
   dim3 grid((d + kSolveCols - 1) / kSolveCols, batch);
   if (r <= 32)
     spd_solve_kernel<32><<<grid, solve_threads<32>(), 0, s>>>(G, r, ridge, Ct, d, Cs, Ginv, status);
@@ -328,13 +339,13 @@ cudaError_t launch_spd_solve(const float *G, int batch, int r, float ridge, cons
 cudaError_t launch_ns_prep(const float *G, int batch, int r, float ridge, float *Gh, float *X0,
                            float *dinv, int *flags, cudaStream_t s) {
   if (r > 256) return cudaErrorInvalidValue;
-  ns_prep_kernel<<<batch, 256, 0, s>>>(G, r, ridge, Gh, X0, dinv, flags);
+  ns_prep_kernel<<<batch, kNsThreads, 0, s>>>(G, r, ridge, Gh, X0, dinv, flags);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ns_finish(const float *X, const float *dinv, int batch, int r, const int *flags,
                              __nv_bfloat16 *Ginv, float *G32, int *status, cudaStream_t s) {
-  ns_finish_kernel<<<batch, 256, 0, s>>>(X, dinv, r, flags, Ginv, G32, status);
+  ns_finish_kernel<<<batch, kNsThreads, 0, s>>>(X, dinv, r, flags, Ginv, G32, status);
   return cudaGetLastError();
 }
 

@@ -13,6 +13,7 @@ namespace dyra {
 namespace {
 
 constexpr uint32_t kStagingBytesPerWarp = 4 * 2048;   // two pairs of 32 x 32 bf16 buffers
+constexpr uint32_t kBiasBytesPerWarp = 512;            // the bias of a warp's (<= 128) columns
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -99,17 +100,17 @@ __device__ __forceinline__ void epilogue16(const TcGemmParams &p, const float *f
   }
 }
 
-// 32 fp32 values of one row -> bf16 into a 32 x 32 staging tile (64-byte rows, 64-byte
-// swizzle: 16-byte chunk c of row l lands at chunk c ^ ((l >> 1) & 3)).
-__device__ __forceinline__ void stage_row32(uint32_t buf, int lane, const float *f) {
+// 32 fp32 accumulator values (raw bits) of one row -> bf16 into a 32 x 32 staging tile
+// (64-byte rows, 64-byte swizzle: 16-byte chunk c of row l lands at chunk c ^ ((l >> 1) & 3)).
+__device__ __forceinline__ void stage_bits32(uint32_t buf, int lane, const uint32_t *v) {
   const uint32_t dst = buf + (uint32_t)lane * 64u;
   const uint32_t sw = (uint32_t)((lane >> 1) & 3);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const uint32_t w0 = pack_bf16x2(f[8 * c + 0], f[8 * c + 1]);
-    const uint32_t w1 = pack_bf16x2(f[8 * c + 2], f[8 * c + 3]);
-    const uint32_t w2 = pack_bf16x2(f[8 * c + 4], f[8 * c + 5]);
-    const uint32_t w3 = pack_bf16x2(f[8 * c + 6], f[8 * c + 7]);
+    const uint32_t w0 = pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1]));
+    const uint32_t w1 = pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3]));
+    const uint32_t w2 = pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5]));
+    const uint32_t w3 = pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7]));
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (((uint32_t)c ^ sw) << 4)),
                  "r"(w0), "r"(w1), "r"(w2), "r"(w3)
                  : "memory");
@@ -431,15 +432,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int u_hi = (e < 4) ? (units + 1) / 2 : units;
     const int c_lo = u_lo * 32, c_hi = u_hi * 32 < p.BN ? u_hi * 32 : p.BN;
     const uint32_t stg = staging + (uint32_t)e * kStagingBytesPerWarp;
+    // this warp's slice of the bias, staged in shared memory once per tile
+    float *bias_s = reinterpret_cast<float *>(
+        smem + (staging - base) + (uint32_t)kEpiWarps * kStagingBytesPerWarp + (uint32_t)e * kBiasBytesPerWarp);
+    const bool stage_bias = p.tma_store && p.bias;
+    // bias[n_tile * BN + c_lo + 4 lane .. + 3] (zeros past the last column)
+    auto load_bias = [&](int n_tile) {
+      float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int c = n_tile * p.BN + c_lo + 4 * lane;
+      if (c_lo + 4 * lane < c_hi) {
+        if (c + 3 < p.cols_valid) {
+          bb = __ldg(reinterpret_cast<const float4 *>(p.bias + c));
+        } else {
+          if (c < p.cols_valid) bb.x = __ldg(p.bias + c);
+          if (c + 1 < p.cols_valid) bb.y = __ldg(p.bias + c + 1);
+          if (c + 2 < p.cols_valid) bb.z = __ldg(p.bias + c + 2);
+        }
+      }
+      return bb;
+    };
     uint32_t buf_i = 0, i = 0;
+    // the next tile's coordinates and bias are fetched one tile ahead
+    TileCoord tcn = decode_tile(cid < total ? cid : 0, p, mp_tiles, crank);
+    float4 bnext = (stage_bias && cid < total) ? load_bias(tcn.n_tile) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int t = cid; t < total; t += ncl, ++i) {
       const uint32_t acc = i & 1u;
-      const TileCoord tc = decode_tile(t, p, mp_tiles, crank);
-      if (p.bias && p.tma_store) {
-        // the bias lines of this warp's columns (at most 4 x 128 B) reach L1 while the
-        // accumulator is still being computed
-        const int pc = tc.n_tile * p.BN + c_lo + lane * 32;
-        if (lane < 4 && pc < p.cols_valid && c_lo + lane * 32 < c_hi) ptx::prefetch_l1(p.bias + pc);
+      const TileCoord tc = tcn;
+      const float4 bcur = bnext;
+      if (t + ncl < total) {
+        tcn = decode_tile(t + ncl, p, mp_tiles, crank);
+        if (stage_bias) bnext = load_bias(tcn.n_tile);
+      }
+      if (stage_bias) {
+        __syncwarp();   // the previous tile's reads of bias_s are done
+        reinterpret_cast<float4 *>(bias_s)[lane] = bcur;
+        __syncwarp();
       }
       int got = 0;
       if (lane == 0) got = ptx::mbar_wait(tfull_bar + 8u * acc, (i >> 1) & 1u, p.timeouts) ? 1 : 0;
@@ -463,54 +490,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem_base + acc * p.acc_cols + ((uint32_t)(q * 32) << 16);
       const int cols_lim = (p.epi == EPI_CG && second) ? p.cols2_valid : p.cols_valid;
       if (p.tma_store) {
-        // bf16 rows, 64 columns per step: two TMEM loads in flight, (+ bias), two 64B-swizzled
-        // 32 x 32 staging tiles, two TMA stores in one bulk group. The warp alternates two
-        // pairs of staging tiles and reuses a pair only after the group that last read it has
-        // finished reading.
+        // bf16 rows. A warp has at most 128 columns of a tile: up to four 32-column pieces,
+        // handled in pairs. Both TMEM loads of a pair complete (tcgen05.wait::ld) before any
+        // other instruction touches their registers -- the destination registers of an
+        // outstanding tcgen05.ld are not yet written, and the compiler does not know that.
+        // Each piece then gets the staged bias and is packed to bf16 into a 64B-swizzled
+        // 32 x 32 staging tile; a pair goes out as one bulk group of TMA stores. The warp
+        // alternates two pairs of staging tiles and reuses a pair only after the group that
+        // last read it has finished reading.
         const int row0 = m0 + q * 32;
-        for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
-          const int col0 = n0 + c0;
-          if (col0 >= cols_lim) break;   // uniform across the warp
-          const bool two = (c0 + 32 < c_hi) && (col0 + 32 < cols_lim);
-          uint32_t v[64];
-          ptx::tmem_ld32(taddr + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[32]>(v));
-          if (two) ptx::tmem_ld32(taddr + (uint32_t)c0 + 32u, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-          ptx::tmem_ld_wait();
-          if (row0 >= p.rows_valid) continue;   // whole 32-row slab outside the tensor
-          float f[64];
-          if (p.bias && col0 + 64 <= cols_lim) {
-            // every lane reads the same 256 bytes: a broadcast from L1
-            const float4 *b4 = reinterpret_cast<const float4 *>(p.bias + col0);
+        int npc = 0;   // pieces inside the tile's and the tensor's columns (uniform)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float4 bb = __ldg(b4 + j);
-              f[4 * j + 0] = __uint_as_float(v[4 * j + 0]) + bb.x;
-              f[4 * j + 1] = __uint_as_float(v[4 * j + 1]) + bb.y;
-              f[4 * j + 2] = __uint_as_float(v[4 * j + 2]) + bb.z;
-              f[4 * j + 3] = __uint_as_float(v[4 * j + 3]) + bb.w;
+        for (int s = 0; s < 4; ++s)
+          if (c_lo + 32 * s < c_hi && n0 + c_lo + 32 * s < cols_lim) npc = s + 1;
+        if (row0 < p.rows_valid) {   // else the 32-row slab is outside the tensor
+          const int zb = p.out_batched ? tc.bz : 0;
+#pragma unroll
+          for (int s0 = 0; s0 < 4; s0 += 2) {
+            if (s0 < npc) {
+              const bool two = s0 + 1 < npc;
+              uint32_t v[2][32];
+              ptx::tmem_ld32(taddr + (uint32_t)(c_lo + 32 * s0), v[0]);
+              if (two) ptx::tmem_ld32(taddr + (uint32_t)(c_lo + 32 * s0 + 32), v[1]);
+              ptx::tmem_ld_wait();
+              if (stage_bias) {   // every lane reads the same bytes: a shared-memory broadcast
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const float4 *b4 = reinterpret_cast<const float4 *>(bias_s + 32 * (s0 + h));
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    const float4 bb = b4[j];
+                    v[h][4 * j + 0] = __float_as_uint(__uint_as_float(v[h][4 * j + 0]) + bb.x);
+                    v[h][4 * j + 1] = __float_as_uint(__uint_as_float(v[h][4 * j + 1]) + bb.y);
+                    v[h][4 * j + 2] = __float_as_uint(__uint_as_float(v[h][4 * j + 2]) + bb.z);
+                    v[h][4 * j + 3] = __float_as_uint(__uint_as_float(v[h][4 * j + 3]) + bb.w);
+                  }
+                }
+              }
+              if (lane == 0) ptx::bulk_wait_read<1>();   // this pair was read by its last group
+              __syncwarp();
+              const uint32_t buf = stg + buf_i * 4096u;
+              stage_bits32(buf, lane, v[0]);
+              if (two) stage_bits32(buf + 2048u, lane, v[1]);
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::tma_store_3d(&tmOut, buf, n0 + c_lo + 32 * s0, row0, zb);
+                if (two) ptx::tma_store_3d(&tmOut, buf + 2048u, n0 + c_lo + 32 * s0 + 32, row0, zb);
+                ptx::bulk_commit();
+              }
+              buf_i ^= 1u;
             }
-          } else if (!p.bias) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) f[j] = __uint_as_float(v[j]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-              f[j] = __uint_as_float(v[j]) + (col0 + j < cols_lim ? __ldg(p.bias + col0 + j) : 0.f);
           }
-          if (lane == 0) ptx::bulk_wait_read<1>();   // this pair's previous stores have read it
-          __syncwarp();
-          const uint32_t buf = stg + buf_i * 4096u;
-          stage_row32(buf, lane, f);
-          if (two) stage_row32(buf + 2048u, lane, f + 32);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int zb = p.out_batched ? tc.bz : 0;
-            ptx::tma_store_3d(&tmOut, buf, col0, row0, zb);
-            if (two) ptx::tma_store_3d(&tmOut, buf + 2048u, col0 + 32, row0, zb);
-            ptx::bulk_commit();
-          }
-          buf_i ^= 1u;
         }
       } else {
         const long long g = (long long)m0 + q * 32 + lane;
@@ -699,7 +730,7 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
     if (p.a_major) return cudaErrorNotSupported;
   }
   const uint32_t stage = 16384u + (uint32_t)p.BN * 128u / (p.pair_mma ? 2u : 1u);
-  const uint32_t staging = p.tma_store ? (uint32_t)kEpiWarps * kStagingBytesPerWarp : 0u;
+  const uint32_t staging = p.tma_store ? (uint32_t)kEpiWarps * (kStagingBytesPerWarp + kBiasBytesPerWarp) : 0u;
   const uint32_t fixed = 1024u + staging + 256u;   // alignment slack, staging, barriers
   int S = (int)((232448u - fixed) / stage);
   if (S > 8) S = 8;

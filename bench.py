@@ -278,6 +278,14 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def weak_scaling_value(tokens_per_rank: int, ms_local: float, world: int):
+    """Whole-job throughput of `world` independent replicas: every rank processed
+    tokens_per_rank tokens per step; the step time is the slowest rank's. Returns
+    (tokens/s, the max-over-ranks ms)."""
+    ms = max_over_ranks(ms_local, world)
+    return world * tokens_per_rank / (ms * 1e-3), ms
+
+
 def workload_config(cfg):
     return {"workload": cfg.name, "batch": cfg.batch, "n_tokens": cfg.n, "d": cfg.d, "m": cfg.m,
             "static": cfg.kind, "k": cfg.k, "r": cfg.r,
@@ -449,9 +457,8 @@ def run_dyra(args, cfg):
     if tmo:
         raise RuntimeError(f"{tmo} bounded waits timed out in the forward")
     ms_local = float(np.mean(step_ms))
-    ms = max_over_ranks(ms_local, world)
     tokens = cfg.batch * cfg.n
-    value = world * tokens / (ms * 1e-3)
+    value, ms = weak_scaling_value(tokens, ms_local, world)
 
     # ---- dense cuBLAS XW + b on the same input, same flushing
     Wd = torch.from_numpy(WL.bf16_bits(W).view(np.int16)).view(torch.bfloat16).to(dev) \

@@ -1,17 +1,16 @@
 // C ABI of the DyRA linear layer (include/dyra.h): offline preparation and the online
 // forward, which enqueues the CUDA kernels of this library on the caller's stream.
 //
-// bf16 low-rank forward, per sample s (every contraction on tcgen05 through tc_gemm):
+// bf16 low-rank forward, per sample s (every contraction on tcgen05 through tc_gemm), as one
+// chain of kernels on the caller's stream:
 //   1. T = X [U | P]                     -> [X U | L]                 (static branch, L = X P)
-//   2. [C^T ; G] = [X | L]^T L           -> C = L^T X, G = L^T L      (one pass over X's tokens)
-//   then two independent branches, the second on the layer's auxiliary stream:
-//   3. B = C W_res                       -> B^T                      (main stream)
-//   4. G^-1 = (G + lambda I)^-1          (Cholesky for r <= 64, Newton-Schulz otherwise)
-//   5. L~ = L G^-1                       written over the L columns of T
-//   6. Y = [X U | L~] [V ; B] + b        (joins the two branches)
-// Since L R = L (G^-1 B) = (L G^-1) B, step 6 produces X W_hat + b + L R of the one-step
-// ALS update without materialising R, and the SPD solve runs beside the B = C W_res GEMM
-// instead of between the GEMMs.
+//   2. [C^T ; G] = [X | L]^T L           -> C^T = X^T L (fp32), G = L^T L
+//   3. C~ = (G + lambda I)^-1 C          (block sweeps for r <= 64, Newton-Schulz otherwise)
+//   4. R = C~ W_res                      one [batch r x d] [d x m] GEMM
+//   5. Y = [X U | L] [V ; R] + b         (the bias in the epilogue)
+// R = G^-1 (C W_res) = (G^-1 C) W_res is the R-update of the one-step ALS; solving on C
+// before the residual product keeps the solve at r x d per sample. The Monarch static branch
+// replaces step 1 by X BD1, X P and the stride permutation, and step 5's static chunks by BD2.
 #include "../../include/dyra.h"
 #include "fit.h"
 #include "kernels.cuh"

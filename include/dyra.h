@@ -64,8 +64,9 @@ typedef enum dyra_dtype {
 
 typedef enum dyra_solver {
   DYRA_SOLVE_AUTO = 0,        /* Cholesky if r <= 64, else Newton-Schulz                 */
-  DYRA_SOLVE_CHOLESKY = 1,
-  DYRA_SOLVE_NEWTON_SCHULZ = 2
+  DYRA_SOLVE_CHOLESKY = 1,    /* exact SPD solve, r <= 64 (bf16: elimination without
+                                 pivoting, whose pivots are Cholesky's; f32: fp64)       */
+  DYRA_SOLVE_NEWTON_SCHULZ = 2 /* ns_iters steps of X <- X (2I - G X) after Jacobi scaling */
 } dyra_solver;
 
 /* Arguments of dyra_prepare / dyra_fit. All pointers are HOST pointers to float64, read

@@ -191,16 +191,11 @@ bool make_store_map(CUtensorMap *map, const void *base, long long inner, long lo
   return dyra::tc_make_store_map(map, op);
 }
 
-// CTAs per cluster for every GEMM of the plan. With 2, CTA pairs share (multicast) the B
-// tile and K-major B maps are encoded with a box of BN / 2 rows. On the ViT-B fc1 layer the
-// pairs measured slightly slower than single CTAs (the kernels there are bound by the
-// epilogue's stores and launch latency, not by L2 reads of B), so single CTAs are the default.
-constexpr int kCluster = 1;
-
-// GEMMs whose operands are both K-major run as cta_group::2 pair MMAs (M = 256 per CTA pair,
-// B split between the pair), which cuts each SM's shared-memory traffic per MMA by a third.
+// GEMMs whose A operand is K-major run as cta_group::2 pair MMAs (M = 256 per CTA pair, B
+// split between the pair, each CTA loading its own half), which cuts each SM's shared-memory
+// traffic per MMA by a third.
 constexpr bool kPairMma = true;
-constexpr int kBDiv = kPairMma ? 2 : kCluster;   // K-major B box rows = BN / kBDiv
+constexpr int kBDiv = kPairMma ? 2 : 1;   // K-major B box rows = BN / kBDiv
 
 void set_pair(dyra::TcGemmParams &p, int elem_bytes, int b_major1) {
   if (!kPairMma) return;
@@ -243,7 +238,7 @@ dyra::TcGemmParams base_params() {
   std::memset(&p, 0, sizeof(p));
   p.rb = 1 << 30;
   p.alpha = 1.f;
-  p.cluster = kCluster;
+  p.cluster = 1;
   p.a_k1 = -1;
   return p;
 }

@@ -92,17 +92,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-// Same load, written to the same shared-memory offset of every CTA in `mask` (this cluster),
-// each copy signalling the mbarrier at the same offset in its own CTA.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                               int c0, int c1, int c2, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
-      : "memory");
-}
-
 // Brings the 128-byte line holding `ptr` into L1 (no register result, nothing waits on it).
 __device__ __forceinline__ void prefetch_l1(const void *ptr) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
@@ -172,15 +161,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)
                : "memory");
-}
-
-// Arrive on the mbarrier at offset `bar` of every CTA in `mask` once every tcgen05.mma issued
-// so far by this thread has completed.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(mask)
-      : "memory");
 }
 
 // ------------------------------------------------------------------ CTA pairs (cta_group::2)

@@ -24,9 +24,9 @@ struct TileCoord {
   int bz, m_tile, n_tile;
 };
 
-// Unit u of the persistent walk (n fastest); with cluster = 2 a unit is a pair of M tiles
-// and CTA rank `crank` of the cluster takes M tile 2 * pair + crank (possibly one past the
-// last M tile: then its loads read zeros and its epilogue stores nothing).
+// Unit u of the persistent walk (n fastest); with pair MMAs (cluster = 2) a unit is a pair
+// of M tiles and CTA rank `crank` of the cluster takes M tile 2 * pair + crank (possibly one
+// past the last M tile: then its loads read zeros and its epilogue stores nothing).
 __device__ __forceinline__ TileCoord decode_tile(int u, const TcGemmParams &p, int mp_tiles,
                                                  int crank) {
   TileCoord c;
@@ -155,7 +155,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = 128 / p.elem_bytes;   // elements in one 128-byte row
-  const bool pair = p.cluster == 2 && !pmma;     // multicast pairs
   const int crank = p.cluster == 2 ? (int)ptx::cluster_ctarank() : 0;
   const bool leader = crank == 0;
   const int cid = (int)blockIdx.x / p.cluster, ncl = (int)gridDim.x / p.cluster;
@@ -165,9 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpLoadA && lane == 0) {
     for (uint32_t s = 0; s < S; ++s) {
       ptx::mbar_init(full_bar + 8u * s, 2);    // the A and the B issuer
-      // the MMA of every CTA reading this stage (multicast pairs: both; pair MMAs: the one
-      // issuing CTA)
-      ptx::mbar_init(empty_bar + 8u * s, pair ? 2u : 1u);
+      // the MMA that reads this stage (pair MMAs: the one issuing CTA, whose commit arrives
+      // on the stage barrier of both CTAs)
+      ptx::mbar_init(empty_bar + 8u * s, 1u);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar + 8u * a, 1);
@@ -194,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
-  // the peer's barriers must be initialised before its multicasts and commits reach them
+  // the peer's barriers must be initialised before its loads and commits reach them
   if (p.cluster == 2) ptx::cluster_sync_all();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_ptr;
@@ -310,8 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       n0 + crank * half + i * chunk, kk * chunk, b_b);
             }
           } else {
-          ptx::mbar_arrive_expect_tx(full, b_bytes);
-          if (!pair) {
+            ptx::mbar_arrive_expect_tx(full, b_bytes);
             if ((b_second ? p.b_major1 : p.b_major) == 0) {
               ptx::tma_load_3d(sb, mb, full, kk * chunk, n0, b_b);
             } else {
@@ -319,16 +317,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_3d(sb + (uint32_t)(i * chunk * 128), mb, full, n0 + i * chunk,
                                  kk * chunk, b_b);
             }
-          } else if ((b_second ? p.b_major1 : p.b_major) == 0) {
-            // this CTA's half of the B rows, into both CTAs of the pair
-            const int half = p.BN / 2;
-            ptx::tma_load_3d_mc(sb + (uint32_t)(crank * half * 128), mb, full, kk * chunk,
-                                n0 + crank * half, b_b, (uint16_t)3);
-          } else {
-            for (int i = crank; i < p.BN / chunk; i += 2)
-              ptx::tma_load_3d_mc(sb + (uint32_t)(i * chunk * 128), mb, full, n0 + i * chunk,
-                                  kk * chunk, b_b, (uint16_t)3);
-          }
           }
           if (++s == S) {
             s = 0;
@@ -400,11 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (uint32_t ks = 0; ks < 4; ++ks)
                 ptx::tc_mma_tf32(d_tmem, ad + ks * a_k16, bd + ks * bk, idesc, (kc | ks) ? 1u : 0u);
             }
-            // frees the smem stage (in both CTAs of a multicast pair) when these MMAs finish
-            if (pair)
-              ptx::tc_commit_mc(empty_bar + 8u * s, (uint16_t)3);
-            else
-              ptx::tc_commit(empty_bar + 8u * s);
+            // frees the smem stage when these MMAs finish
+            ptx::tc_commit(empty_bar + 8u * s);
           }
           if (++s == S) {
             s = 0;
@@ -723,6 +708,7 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
   while (p.acc_cols < (uint32_t)p.BN) p.acc_cols <<= 1;
   if (p.seg_n > 0 && (p.batch != 1 || p.a_major || p.seg_count <= 0 || p.k_chunks <= p.b_split))
     return cudaErrorInvalidValue;
+  p.cluster = 1;
   if (p.pair_mma) {
     p.cluster = 2;
     if (p.BN % 32) return cudaErrorInvalidValue;                   // halves of whole 8-row groups
@@ -742,7 +728,6 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
   // one CTA per SM: the two accumulators may take all 512 TMEM columns
   if (smem < 116u * 1024u) smem = 116u * 1024u;
   p.smem_bytes = smem;
-  if (p.cluster != 2) p.cluster = 1;
   const long long units =
       (long long)p.batch * ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
   // programmatic stream serialization: this grid may launch while the previous kernel of
@@ -765,8 +750,8 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.numAttrs = 2;
-  auto kern = p.pair_mma ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
-  const int max_clusters = max_active_pairs(kern, cfg, p.pair_mma != 0);
+  auto kern = tc_gemm_kernel<true>;
+  const int max_clusters = max_active_pairs(kern, cfg, true);
   const long long clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, out_map, p);

@@ -2,12 +2,10 @@
 // stored K-contiguous ("K-major") or MN-contiguous, fp32 accumulation in TMEM.
 //
 // Persistent kernel: a grid of at most one CTA per SM walks the tiles (batch, m tile,
-// n tile), n fastest, in a static round-robin. Two cluster modes pair CTAs on adjacent M
-// tiles of one (batch, N tile):
-//   * pair MMA (cta_group::2): a 256-row unit; each CTA loads its 128 rows of A and half of
-//     the B tile, the even CTA issues the MMAs for both, and each CTA's TMEM receives its own
-//     128 rows;
-//   * multicast: each CTA loads half of the B tile and multicasts it to both.
+// n tile), n fastest, in a static round-robin. In pair-MMA mode (cta_group::2) a 2-CTA
+// cluster takes adjacent M tiles of one (batch, N tile) as a 256-row unit: each CTA loads its
+// own 128 rows of A and its own half of the B tile into its own shared memory, the even CTA
+// issues the MMAs for both, and each CTA's TMEM receives its own 128 rows.
 // Each CTA has these warps:
 //   warp 0      TMA issuer for A (one lane): 128-byte K chunks (128 rows) into a ring of
 //               shared-memory stages; it runs ahead across tile boundaries
@@ -49,11 +47,9 @@ struct TcGemmParams {
   int pair_mma;      // 1: CTA pairs run cta_group::2 MMAs (M = 256 per pair): each CTA holds
                      // its 128 rows of A and half of the B tile (BN / 2 rows or columns), the
                      // even CTA issues the MMAs, each CTA's TMEM receives its own 128 rows
-                     // (implies cluster = 2 without multicast; K-major B maps then need a
-                     // box of BN / 2 rows; MN-major B needs BN % 128 == 0)
-  int cluster;       // 1, or 2: CTA pairs take adjacent M tiles of one (batch, N tile) and
-                     // each loads half of the B tile, multicast to both (K-major B maps then
-                     // need a box of BN / 2 rows)
+                     // (K-major B maps then need a box of BN / 2 rows; MN-major B needs
+                     // BN % 128 == 0)
+  int cluster;       // set by tc_gemm_launch: 2 with pair_mma, else 1
   int BN;            // MMA N of a tile: multiple of 16 (of 64 for MN-major B), <= 256
   int k_chunks;      // K in 128-byte chunks
   int elem_bytes;    // 2 = bf16, 4 = fp32/tf32

@@ -288,6 +288,50 @@ def test_newton_schulz_converges_to_inverse():
 
 # -------------------------------------------------------------------- metric and workloads
 
+def test_relative_frobenius_hand_value():
+    """The parity metric ||a - b||_F / ||b||_F on values worked out by hand:
+    a - b = [[0, 0], [0, -1]] and ||b||_F^2 = 1 + 4 + 9 + 25 = 39, so the value is 1/sqrt(39).
+    With a = 2 b the two argument orders give 1 and 1/2, so a swapped numerator and
+    denominator, or a missing square root (1/39, or 1 and 1/4), fails."""
+    a = np.array([[1.0, 2.0], [3.0, 4.0]])
+    b = np.array([[1.0, 2.0], [3.0, 5.0]])
+    assert O.relative_frobenius(a, b) == pytest.approx(0.16012815380508713, rel=1e-15)
+    assert O.relative_frobenius(2 * b, b) == pytest.approx(1.0, rel=1e-15)
+    assert O.relative_frobenius(b, 2 * b) == pytest.approx(0.5, rel=1e-15)
+    assert O.relative_frobenius(b, b) == 0.0
+
+
+def test_monarch_forward_exact_when_residual_rank_at_most_r():
+    """Monarch branch end to end (Appendix B structure; blog rank-r objective and one-step
+    sections): with W = Monarch(B1, B2) + A R0, rank(A) <= r, the static factors (B1, B2) and
+    any R0 spanning the residual's row space, the residual is A R0 exactly, so P = A (R0
+    orthonormal), L = X A, R = R0 and Y = X W + b. A wrong permutation index, a dropped
+    static term or a transposed block would leave a residual the rank-r correction cannot
+    absorb."""
+    rng = _rng(16)
+    nb, bi, bo, r = 4, 3, 5, 3
+    Wm, B1, B2 = _planted_monarch(rng, nb, bi, bo)
+    d, m = nb * bi, nb * bo
+    A = rng.standard_normal((d, r))
+    R0 = _orth(rng, m, r).T
+    W = Wm + A @ R0
+    b = rng.standard_normal(m)
+    X = rng.standard_normal((2, 30, d))
+    prep = O.prepare(W, b, "monarch", nb, r, R0=R0, factors=(B1, B2))
+    assert np.allclose(prep["W_res"], A @ R0, atol=1e-12)
+    assert np.allclose(prep["P"], A, atol=1e-12)
+    Y, inter = O.forward(X, prep, keep=True)
+    assert np.allclose(Y, X @ W + b, atol=1e-10 * np.abs(X @ W).max())
+    # the library-side convention: the residual rank-r term alone is X W_res
+    for s in range(2):
+        assert np.allclose(inter["L"][s] @ inter["R"][s], X[s] @ (A @ R0), atol=1e-10)
+    # with R0 taken from the residual's own SVD (another basis of the same rows), the
+    # output is the same
+    prep2 = O.prepare(W, b, "monarch", nb, r, factors=(B1, B2))
+    assert not np.allclose(prep2["R0"], R0, atol=1e-6)
+    assert np.allclose(O.forward(X, prep2), X @ W + b, atol=1e-10 * np.abs(X @ W).max())
+
+
 def test_approximation_error_metric():
     rng = _rng(15)
     X = rng.standard_normal((2, 5, 4))

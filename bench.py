@@ -1,9 +1,13 @@
 """Benchmark of the DyRA linear layer (one forward = one step) on synthetic inputs.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl dyra|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5] [--impl dyra|reference]
+                    [--no-per-config] [--no-cpu-baseline]
 
-Prints ONE JSON line (rank 0). `value` is whole-job tokens/s = (tokens all ranks processed)
-/ (max over ranks of the summed device time of the K timed forwards). Every forward reads
+Prints ONE JSON line (rank 0). The headline workload is c5, the largest configuration (LLM
+prefill MLP up-projection, 4 x 2048 tokens, 4096 -> 12288, k 1024, r 256, Newton-Schulz);
+"per_config" holds the same numbers for the ViT-B fc1 (c2), DINOv3 fc1 / fc2 (c3) and Monarch
+(c4) layers. `value` is whole-job tokens/s = (tokens all ranks processed) / (max over ranks of
+the mean device time of the K timed forwards). Every forward reads
 its inputs from HBM: L2 is flushed (a write of 2x the L2 size) before each timed step,
 outside the events that time it. Under torchrun each rank runs an independent replica of
 the whole workload on its own GPU (the batch's samples are independent least-squares
@@ -35,6 +39,8 @@ import workloads as WL  # noqa: E402
 METRIC = "DyRA layer tokens/s and latency vs dense cuBLAS XW; % bf16 TC peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 L2_BYTES = 126 * 1024 * 1024
+# the workloads timed beside the headline one (each as its own entry of "per_config")
+PER_CONFIG = ["c2", "c3_fc1", "c3_fc2", "c4"]
 _CSRC = "input_adaptive_rank_dyra_b300/csrc/"
 # the source files that define each kernel of the forward (a recorded DRAM-traffic figure is
 # used only while their hash matches the one recorded with it)
@@ -296,61 +302,110 @@ def workload_config(cfg):
 
 # ---------------------------------------------------------------------------- CPU oracle
 
+# Samples of each workload that one CPU pass of the oracle forward covers: enough tokens for a
+# stable rate, few enough that a pass stays around a second on a many-core host.
+ORACLE_SAMPLES = {"c1_fp32_single_layer": 1, "c2_vitb16_fc1": 4, "c3_dinov3_vitl16_fc1": 1,
+                  "c3_dinov3_vitl16_fc2": 1, "c4_monarch32_attn_proj": 1, "c5_prefill_mlp_up": 1}
+
+
 @functools.lru_cache(maxsize=None)
 def _oracle_inputs(cfg):
-    """Oracle preparation (untimed) and the first few samples of the workload."""
+    """Oracle preparation (untimed) and the first samples of the workload."""
     import oracle as O
     W, b = WL.make_weights(cfg)
     prep = O.prepare(W, b, cfg.kind, cfg.k, cfg.r)
-    return prep, WL.make_inputs(cfg, range(min(cfg.batch, 4)))
+    ns = min(cfg.batch, ORACLE_SAMPLES.get(cfg.name, 1))
+    return prep, WL.make_inputs(cfg, range(ns))
 
 
-def oracle_baseline(cfg, seconds: float = 12.0):
-    """Times the fp64 oracle's forward (the offline fit excluded) on a bounded sample of the
-    workload: whole samples, repeated until `seconds` of CPU time have passed."""
-    import oracle as O
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
     except Exception:
-        cores = os.cpu_count()
+        return os.cpu_count() or 1
+
+
+def _solver_of(cfg) -> str:
+    return cfg.solver if cfg.solver != "auto" else ("cholesky" if cfg.r <= 64 else "newton_schulz")
+
+
+def oracle_pass(cfg):
+    """One timed pass of the fp64 oracle's forward (fit excluded) over the bounded sample.
+    Returns (tokens, seconds)."""
+    import oracle as O
     prep, X = _oracle_inputs(cfg)
-    solver = cfg.solver if cfg.solver != "auto" else ("cholesky" if cfg.r <= 64 else "newton_schulz")
-    nsamp = X.shape[0]
-    O.forward(X[:1], prep, solver=solver, ns_iters=cfg.ns_iters)   # warm-up
     t0 = time.perf_counter()
-    tokens = 0
-    reps = 0
-    while True:
-        O.forward(X, prep, solver=solver, ns_iters=cfg.ns_iters)
-        tokens += nsamp * cfg.n
+    O.forward(X, prep, solver=_solver_of(cfg), ns_iters=cfg.ns_iters)
+    return X.shape[0] * cfg.n, time.perf_counter() - t0
+
+
+def oracle_baseline(cfg, seconds: float = 10.0):
+    """Times the fp64 oracle's forward on the bounded sample, repeated until `seconds` have
+    passed, on all host threads; then one pass with the BLAS limited to one thread."""
+    prep, X = _oracle_inputs(cfg)
+    oracle_pass(cfg)   # warm-up
+    tokens, el, reps = 0, 0.0, 0
+    while el < seconds:
+        t, dt = oracle_pass(cfg)
+        tokens += t
+        el += dt
         reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": tokens / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    one = None
+    try:
+        from threadpoolctl import threadpool_limits
+        with threadpool_limits(limits=1):
+            t1, dt1 = oracle_pass(cfg)
+        one = {"value": t1 / dt1, "unit": "tokens/s", "cores": 1, "seconds": dt1}
+    except Exception as e:   # reported, never fatal
+        one = {"unavailable": f"{type(e).__name__}: {e}"}
+    nsamp = X.shape[0]
+    return {"value": tokens / el, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "cpu_model": _cpu_model(), "host_cpus": os.cpu_count(),
             "sample": f"{nsamp} of {cfg.batch} samples ({nsamp * cfg.n} tokens) x {reps} passes, "
-                      f"fp64 numpy/LAPACK forward, fit excluded, {el:.1f} s"}
+                      f"fp64 numpy/LAPACK forward, fit excluded, {el:.1f} s",
+            "single_thread": one}
 
 
 def run_reference(args, cfg):
+    """The reference arm: the fp64 oracle on the host cores, one pass over the bounded sample
+    per step (W untimed passes, then K timed ones); ms_per_step is the measured time of a
+    step's pass and value its tokens per second (median over the steps)."""
     rank, world, _ = dist_init(args.gpus)
     if rank != 0:
         return
-    per_step = []
-    cb = None
     for _ in range(args.warmup):
-        oracle_baseline(cfg, seconds=0.0)
+        oracle_pass(cfg)
+    per_ms, per_rate = [], []
+    tokens = 0
     for _ in range(args.steps):
-        cb = oracle_baseline(cfg, seconds=max(1.0, 20.0 / max(args.steps, 1)))
-        per_step.append(cb["value"])
-    value = statistics.median(per_step)
-    cb["value"] = value
+        tokens, dt = oracle_pass(cfg)
+        per_ms.append(dt * 1e3)
+        per_rate.append(tokens / dt)
+    value = statistics.median(per_rate)
+    nsamp = tokens // cfg.n
+    sample = (f"{nsamp} of {cfg.batch} samples ({tokens} tokens) per step, fp64 numpy/LAPACK "
+              "forward, fit excluded")
+    conf = dict(workload_config(cfg))
+    conf["sample"] = sample
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": cfg.batch * cfg.n / value * 1e3, "higher_is_better": True,
+            "ms_per_step": statistics.median(per_ms), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(cfg), "cpu_baseline": cb,
+            "config": conf,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _blas_threads(),
+                             "kind": "oracle", "cpu_model": _cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -358,28 +413,27 @@ def run_reference(args, cfg):
 
 # ---------------------------------------------------------------------------- GPU arm
 
-def run_dyra(args, cfg):
+def _torch_input(cfg, X):
+    import torch
+    if cfg.dtype == "bf16":
+        return torch.from_numpy(WL.bf16_bits(X).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(X.astype(np.float32))
+
+
+def measure_config(cfg, args, dev, world, pk, with_e2e: bool, clocks=None):
+    """Times one configuration on this rank's GPU: the DyRA forward (CUDA-graph replays of
+    one dyra_linear_forward call, L2 flushed before each step), its kernels one by one, the
+    dense cuBLAS X W + b on the same input and, if asked, the host-buffer entry point."""
     import torch
     import input_adaptive_rank_dyra_b300 as dy
-    rank, world, local = dist_init(args.gpus)
-    if not torch.cuda.is_available():
-        raise RuntimeError("bench.py needs a CUDA device (B300)")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dy.load()
-    pk, pk_kind = peaks()
-
     W, b = WL.make_weights(cfg)
     t0 = time.perf_counter()
-    layer = dy.prepare(W, b, kind=cfg.kind, k=cfg.k, r=cfg.r, dtype=cfg.dtype, device=local,
-                       solver=cfg.solver, ns_iters=cfg.ns_iters)
+    layer = dy.prepare(W, b, kind=cfg.kind, k=cfg.k, r=cfg.r, dtype=cfg.dtype,
+                       device=dev.index, solver=cfg.solver, ns_iters=cfg.ns_iters)
     prep_s = time.perf_counter() - t0
     X = WL.make_inputs(cfg)
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
-    if cfg.dtype == "bf16":
-        Xh = torch.from_numpy(WL.bf16_bits(X).view(np.int16)).view(torch.bfloat16)
-    else:
-        Xh = torch.from_numpy(X.astype(np.float32))
+    Xh = _torch_input(cfg, X)
     Xd = Xh.to(dev)
     Y = torch.empty((cfg.batch, cfg.n, cfg.m), dtype=tdt, device=dev)
     ws = dy.new_workspace(layer, cfg.batch, cfg.n)
@@ -389,12 +443,11 @@ def run_dyra(args, cfg):
     names = layer.kernel_names()
     K, Wm = args.steps, args.warmup
 
-    # ---- device-resident timed region. Each timed step replays a CUDA graph of one forward
-    # captured from the same C-ABI call (dyra_linear_forward), so the GPU runs the step's
-    # kernels back to back, with their programmatic-launch edges, instead of waiting on host
-    # launches. A second pass replays graphs of dyra_linear_forward_profiled, which carry a
-    # start/end event pair around every kernel on the stream that kernel runs on: it gives
-    # the per-kernel times (the event nodes sit between kernels, so it is not the step time).
+    # Each timed step replays a CUDA graph captured from one dyra_linear_forward call, so the
+    # GPU runs the step's kernels back to back with their programmatic-launch edges. A second
+    # pass replays graphs of dyra_linear_forward_profiled, which put an event pair around
+    # every kernel: the per-kernel times (the event nodes sit between kernels, so their sum
+    # is not the step time).
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(K)]
     st = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     en = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -416,14 +469,13 @@ def run_dyra(args, cfg):
             dy.linear_forward_profiled(layer, Xd, Y, ws, ev[i], stream=cap)
         graphs.append(g)
     torch.cuda.synchronize()
-    # host cost of one forward call (enqueue only), for reference
     t0 = time.perf_counter()
     for _ in range(20):
         dy.linear_forward(layer, Xd, Y, ws)
     host_us = (time.perf_counter() - t0) / 20 * 1e6
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.__enter__()
+    if clocks is not None:
+        clocks.__enter__()
     t_start = time.perf_counter()
     i = 0
     # W warm-up replays at least, and enough of them (about a second) for the clock sampler
@@ -443,7 +495,8 @@ def run_dyra(args, cfg):
         g_plain.replay()
         en[i].record(stream)
     torch.cuda.synchronize()
-    clocks.__exit__(None, None, None)
+    if clocks is not None:
+        clocks.__exit__(None, None, None)
     barrier(world)
     torch.cuda.synchronize()
     step_ms = [st[i].elapsed_time(en[i]) for i in range(K)]
@@ -455,12 +508,12 @@ def run_dyra(args, cfg):
                         for i in range(K)])
     nsp, tmo = dy.workspace_status(layer, ws)
     if tmo:
-        raise RuntimeError(f"{tmo} bounded waits timed out in the forward")
+        raise RuntimeError(f"{cfg.name}: {tmo} bounded waits timed out in the forward")
     ms_local = float(np.mean(step_ms))
     tokens = cfg.batch * cfg.n
     value, ms = weak_scaling_value(tokens, ms_local, world)
 
-    # ---- dense cuBLAS XW + b on the same input, same flushing
+    # dense cuBLAS X W + b on the same input, same flushing
     Wd = torch.from_numpy(WL.bf16_bits(W).view(np.int16)).view(torch.bfloat16).to(dev) \
         if cfg.dtype == "bf16" else torch.from_numpy(W.astype(np.float32)).to(dev)
     bd = torch.from_numpy(b.astype(np.float32)).to(dev).to(tdt)
@@ -478,26 +531,42 @@ def run_dyra(args, cfg):
         den[i].record(stream)
     torch.cuda.synchronize()
     dense_ms = float(np.mean([dst[i].elapsed_time(den[i]) for i in range(K)]))
+    del Wd, Yd
 
-    # ---- end to end through the host-buffer entry point (pinned host X and Y)
-    Xp = Xh.pin_memory()
-    Yp = torch.empty((cfg.batch, cfg.n, cfg.m), dtype=tdt).pin_memory()
-    Xs = torch.empty_like(Xd)
-    for _ in range(Wm):
-        dy.linear_forward_host(layer, Xp, Yp, Xs, Y, ws)
-    torch.cuda.synchronize()
-    est = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    een = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for i in range(K):
-        flush.fill_(float(i))
-        est[i].record(stream)
-        dy.linear_forward_host(layer, Xp, Yp, Xs, Y, ws)
-        een[i].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(float(np.mean([est[i].elapsed_time(een[i]) for i in range(K)])), world)
-    ebytes = 2 if cfg.dtype == "bf16" else 4
+    out = {"cfg": cfg, "value": value, "ms": ms, "ms_local": ms_local, "dense_ms": dense_ms,
+           "kern_ms": kern_ms, "names": names, "nk": nk, "host_us": host_us, "nsp": nsp,
+           "prep_s": prep_s, "tokens": tokens}
 
-    # ---- roofline of the dominant kernel
+    if with_e2e:
+        # end to end through the host-buffer entry point (pinned host X and Y)
+        Xp = Xh.pin_memory()
+        Yp = torch.empty((cfg.batch, cfg.n, cfg.m), dtype=tdt).pin_memory()
+        Xs = torch.empty_like(Xd)
+        for _ in range(Wm):
+            dy.linear_forward_host(layer, Xp, Yp, Xs, Y, ws)
+        torch.cuda.synchronize()
+        est = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        een = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for i in range(K):
+            flush.fill_(float(i))
+            est[i].record(stream)
+            dy.linear_forward_host(layer, Xp, Yp, Xs, Y, ws)
+            een[i].record(stream)
+        torch.cuda.synchronize()
+        out["e2e_ms"] = max_over_ranks(float(np.mean([est[i].elapsed_time(een[i])
+                                                      for i in range(K)])), world)
+    layer.close()
+    del flush, Xd, Y, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def summarize(res, pk, pk_kind):
+    """The per-configuration numbers: latency, dense reference, TC and roofline fractions,
+    per-kernel times (keyed by launch index) and the roofline of the dominant kernel."""
+    cfg = res["cfg"]
+    names, kern_ms, nk = res["names"], res["kern_ms"], res["nk"]
+    ms = res["ms"]
     mean_k = kern_ms.mean(axis=0)
     top = int(np.argmax(mean_k))
     top_name = names[top]
@@ -511,52 +580,95 @@ def run_dyra(args, cfg):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic(cfg.name, top_name)
     roof["kernel"] = top_name
+    roof["launch_index"] = top
     roof["kernel_us"] = mean_k[top] * 1e3
     roof["algorithmic_bytes"] = by
     roof["algorithmic_flops"] = fl
-    roof["peak_source"] = f"{pk_kind} (MEASURED_PEAKS.json burst)" if pk_kind == "measured" \
-        else "fallback"
-
+    roof["peak_source"] = (f"{pk_kind} (MEASURED_PEAKS.json burst: the kernel runs well under "
+                           "a millisecond)") if pk_kind == "measured" else "fallback"
     fl_layer = layer_flops(cfg)
     t_layer = ms * 1e-3
     t_roof = max(fl_layer / (tc_peak * 1e12), layer_bytes(cfg) / (hbm_peak * 1e9))
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded; no dataset)",
-        "config": workload_config(cfg),
-        "latency_us": ms * 1e3,
+    kernels = []
+    for j in range(nk):
+        f, b_ = kernel_work(cfg, names[j])
+        t = float(mean_k[j]) * 1e-3
+        kernels.append({"i": j, "name": names[j], "us": round(float(mean_k[j]) * 1e3, 3),
+                        "tflops": round(f / t / 1e12, 1) if f else 0.0,
+                        "gbs": round(b_ / t / 1e9, 1) if b_ else 0.0})
+    return {
+        "workload": cfg.name, "latency_us": ms * 1e3, "tokens_per_s": res["value"],
         "tc_frac_of_peak": fl_layer / t_layer / (tc_peak * 1e12),
         "layer_roofline_frac": t_roof / t_layer,
         "layer_tflops": fl_layer / t_layer / 1e12,
-        "dense_cublas": {"us": dense_ms * 1e3, "tokens_per_s": tokens / (dense_ms * 1e-3),
-                         "speedup_of_dyra": dense_ms / ms_local},
-        "kernels_us": {names[j]: round(float(mean_k[j]) * 1e3, 3) for j in range(nk)},
-        "roofline": roof,
-        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "dense_cublas": {"us": res["dense_ms"] * 1e3,
+                         "tokens_per_s": res["tokens"] / (res["dense_ms"] * 1e-3),
+                         "speedup_of_dyra": res["dense_ms"] / res["ms_local"]},
+        "kernels_us": kernels, "roofline": roof,
+        "not_spd_samples": res["nsp"], "prepare_s": res["prep_s"],
+    }
+
+
+def run_dyra(args, cfg):
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    rank, world, local = dist_init(args.gpus)
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device (B300)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dy.load()
+    pk, pk_kind = peaks()
+
+    clocks = ClockSampler(local)
+    head = measure_config(cfg, args, dev, world, pk, with_e2e=True, clocks=clocks)
+    h = summarize(head, pk, pk_kind)
+    others = []
+    if not args.no_per_config:
+        for name in PER_CONFIG:
+            c = WL.get_config(name)
+            if c.name == cfg.name:
+                continue
+            others.append(summarize(measure_config(c, args, dev, world, pk, with_e2e=False),
+                                    pk, pk_kind))
+    tokens = head["tokens"]
+    ebytes = 2 if cfg.dtype == "bf16" else 4
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded; no dataset)", "config": workload_config(cfg),
+        "latency_us": h["latency_us"], "tc_frac_of_peak": h["tc_frac_of_peak"],
+        "layer_roofline_frac": h["layer_roofline_frac"], "layer_tflops": h["layer_tflops"],
+        "dense_cublas": h["dense_cublas"], "kernels_us": h["kernels_us"],
+        "roofline": h["roofline"],
+        "e2e": {"value": world * tokens / (head["e2e_ms"] * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": tokens * cfg.d * ebytes,
                 "d2h_bytes_per_step": tokens * cfg.m * ebytes},
-        "gpu_launches": K * nk,
-        "host_enqueue_us": host_us,
+        "gpu_launches": args.steps * head["nk"],
+        "host_enqueue_us": head["host_us"],
         "clocks": clocks.summary(),
-        "not_spd_samples": nsp,
-        "prepare_s": prep_s,
+        "not_spd_samples": head["nsp"],
+        "prepare_s": head["prep_s"],
+        "per_config": others,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(cfg)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    layer.close()
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="c2", choices=sorted(WL.CONFIGS))
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="c5", choices=sorted(WL.CONFIGS),
+                    help="headline workload (default: c5, the largest)")
     ap.add_argument("--impl", default="dyra", choices=["dyra", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the headline workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

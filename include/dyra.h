@@ -94,7 +94,7 @@ typedef struct dyra_prepare_args {
   int fit_threads;      /* host threads for the fit, 0 => hardware concurrency           */
 } dyra_prepare_args;
 
-/* Read-only description of a prepared layer. */
+/* Read-only description of a prepared layer (the shapes and options of dyra_prepare). */
 typedef struct dyra_layer_desc {
   int d, m, k, r;
   dyra_static_kind kind;
@@ -110,12 +110,19 @@ typedef struct dyra_layer dyra_layer;   /* opaque; owns its device copies of the
 
 /* Offline preparation (synchronous, not meant for the timed path): static fit of W (unless
  * F1/F2 are given), W_res = W - W_hat, R0 (unless given), P = W_res R0^T (R0 R0^T)^-1, and
- * upload of the factors in the layer's dtype to `device`. On success *out owns the layer;
+ * upload of the factors in the layer's dtype to `device`.
+ * Passages: blog digest, section "没有训练时离线准备和在线计算是什么" (offline: static
+ * structured factors, residual, fixed initial right factor R0 = top right singular vectors of
+ * W_res, precomputed left projection, once per layer) and section "DyRA 的整体流程是怎样的"
+ * (the offline stage of the flow); section "静态分支与残差如何拆分" (W = W_hat + W_res);
+ * summary page Appendix B (truncated SVD; Monarch by a truncated SVD of each block of the
+ * rearranged weight, also the blog's section "已有结构化矩阵方法分工有何不同"). P is the
+ * least-squares L-update of the blog's section "残差乘积的低秩优化目标是什么" with R = R0. On success *out owns the layer;
  * free it with dyra_layer_destroy. Errors: INVALID_ARG (shapes, null W, r out of range,
  * R0 rank deficient), UNSUPPORTED (a shape the kernels do not take), NO_DEVICE, OOM, CUDA. */
 dyra_status dyra_prepare(const dyra_prepare_args *args, dyra_layer **out);
 
-/* The offline step alone, on the host (no device needed): the static fit (unless F1/F2
+/* The offline step alone, on the host (no device needed; same passages as dyra_prepare): the static fit (unless F1/F2
  * are given), W_res, R0 (unless given) and P, in float64, written to caller-owned host
  * buffers (any may be NULL; sizes as in dyra_export / dyra_export_factors). dtype, solver
  * and device are not used. Lets a CPU machine prepare factors that dyra_prepare later
@@ -123,21 +130,38 @@ dyra_status dyra_prepare(const dyra_prepare_args *args, dyra_layer **out);
 dyra_status dyra_fit(const dyra_prepare_args *args, double *W_hat, double *W_res, double *P,
                      double *R0, double *F1, double *F2);
 
+/* Frees a layer from dyra_prepare (waits for the layer's device to finish its work first).
+ * NULL is a no-op. Packaging: the pages have no counterpart. */
 void dyra_layer_destroy(dyra_layer *layer);
 
+/* Fills *out with the layer's shapes and resolved options. Errors: INVALID_ARG (NULL).
+ * Packaging: the pages have no counterpart. */
 dyra_status dyra_layer_info(const dyra_layer *layer, dyra_layer_desc *out);
 
-/* Host float64 copies of what dyra_prepare computed (before rounding to the device dtype).
+/* Host float64 copies of what dyra_prepare computed (before rounding to the device dtype):
+ * the offline quantities of the blog's section "没有训练时离线准备和在线计算是什么".
  * Any pointer may be NULL. Sizes: W_hat, W_res [d, m]; P [d, r]; R0 [r, m];
  * F1/F2 as in dyra_prepare_args. */
 dyra_status dyra_export(const dyra_layer *layer, double *W_hat, double *W_res, double *P,
                         double *R0);
 dyra_status dyra_export_factors(const dyra_layer *layer, double *F1, double *F2);
 
-/* Bytes of device workspace dyra_linear_forward needs for (batch, n). */
+/* Bytes of device workspace dyra_linear_forward needs for (batch, n): the per-sample
+ * rank-r intermediates of the online step (blog section "残差乘积的低秩优化目标是什么":
+ * every intermediate passes through a rank-r channel, never the full residual product).
+ * Errors: INVALID_ARG (null pointers, negative sizes). */
 dyra_status dyra_workspace_size(const dyra_layer *layer, int batch, int n, size_t *bytes);
 
-/* The online step. X: device [batch, n, d], Y: device [batch, n, m], both in the layer's
+/* The online step: Y = X W_hat + b + L R per sample, with L = X P (L-update from R0) and
+ * R = (L^T L + lambda I)^-1 (L^T X) W_res (R-update), one least-squares system per sample.
+ * Passages: blog digest, section "一次迭代的近似形式与额外代价" (one ALS iteration, L then R,
+ * XW ~ X W_hat + L(1) R(1)), section "残差乘积的低秩优化目标是什么" (the objective
+ * min ||X W_res - L R||_F^2 and the order of operations: input projected to r first, then
+ * multiplied by the residual), section "DyRA 的整体流程是怎样的" (online stage: static branch,
+ * thin product for L, least-squares R, fused accumulation; Cholesky for small r and
+ * Newton-Schulz for large r; the residual product never written to memory); summary page
+ * 2.2 (ridge) and 2.4 (solver choice).
+ * X: device [batch, n, d], Y: device [batch, n, m], both in the layer's
  * dtype, 16-byte aligned, rows densely packed. workspace: device, >= dyra_workspace_size
  * bytes, 256-byte aligned, owned by the caller; it must not be shared by two forwards that
  * may run at the same time. Enqueues every kernel on `stream` and returns without waiting.
@@ -149,7 +173,7 @@ dyra_status dyra_linear_forward(const dyra_layer *layer, const void *X, int batc
                                 void *Y, void *workspace, size_t workspace_bytes,
                                 cudaStream_t stream);
 
-/* Same step from HOST buffers: copies X_host -> X_dev, runs the forward, copies Y_dev ->
+/* Same step (same passages as dyra_linear_forward) from HOST buffers: copies X_host -> X_dev, runs the forward, copies Y_dev ->
  * Y_host, all enqueued on `stream` (use page-locked host memory for asynchronous copies;
  * synchronise the stream before reading Y_host). X_dev / Y_dev are device staging buffers
  * owned by the caller. */
@@ -158,8 +182,9 @@ dyra_status dyra_linear_forward_host(const dyra_layer *layer, const void *X_host
                                      void *workspace, size_t workspace_bytes,
                                      cudaStream_t stream);
 
-/* The same forward (same streams, same kernels) that also records two events around every
- * kernel it launches: events[2i] just before kernel i and events[2i + 1] just after it, both
+/* The same forward (same streams, same kernels; same passages as dyra_linear_forward) that
+ * also records two events around every kernel it launches (the pages time only whole
+ * models, summary page 3.2; this is the per-kernel measurement): events[2i] just before kernel i and events[2i + 1] just after it, both
  * on `stream`, so cudaEventElapsedTime(events[2i], events[2i + 1]) is kernel i's
  * device time. count = kernels_per_forward; max_events must be >= 2 * count. *recorded
  * receives 2 * count. Called while `stream` is being captured into a CUDA graph, the records
@@ -170,17 +195,22 @@ dyra_status dyra_linear_forward_profiled(const dyra_layer *layer, const void *X,
                                          size_t workspace_bytes, cudaStream_t stream,
                                          cudaEvent_t *events, int max_events, int *recorded);
 
-/* Name of kernel `i` of the forward (static string), or NULL. */
+/* Name of kernel `i` of the forward (static string), or NULL for an index out of range or a
+ * NULL layer. Packaging: the pages have no counterpart. */
 const char *dyra_kernel_name(const dyra_layer *layer, int i);
 
-/* Synchronises `stream`, then reads the status word the last forward on `workspace` left:
+/* Per-sample solve status (summary page 2.2: the R-update is a least-squares solve with an
+ * optional ridge; a sample whose L^T L + lambda I is not positive definite has no Cholesky
+ * factor, this library's reading is R = 0 for it).
+ * Synchronises `stream`, then reads the status word the last forward on `workspace` left:
  * *not_spd_samples = samples that fell back to the static branch, *timeouts = bounded
  * in-kernel waits that gave up. Returns DYRA_ERR_TIMEOUT if *timeouts > 0, else
  * DYRA_ERR_NOT_SPD if *not_spd_samples > 0, else DYRA_OK. */
 dyra_status dyra_workspace_status(const dyra_layer *layer, const void *workspace,
                                   cudaStream_t stream, int *not_spd_samples, int *timeouts);
 
-/* Intermediates a forward leaves in its workspace, for tests that check each kernel. */
+/* Intermediates a forward leaves in its workspace, for tests that check each kernel: the
+ * quantities of the blog's section "残差乘积的低秩优化目标是什么" (L, L^T L, L^T X, R). */
 typedef enum dyra_buffer {
   DYRA_BUF_T = 0,      /* [batch, n, ld] = [X F1 | L] (bf16: F1 columns padded to a multiple
                           of 64; Monarch: the permuted X BD1 in place of X F1)              */
@@ -211,7 +241,8 @@ dyra_status dyra_workspace_tensor(const dyra_layer *layer, int batch, int n, int
  * cudaFree or other device-allocating routine. X, Y: as in dyra_linear_forward (device,
  * caller-owned). The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with the layer's device current); make that first call before any
- * stream capture. All calls share the one array and it keeps the previous call's contents;
+ * stream capture. The address is cached together with the device's current CUDA context and
+ * looked up again when that context changes (after cudaDeviceReset, say). All calls share the one array and it keeps the previous call's contents;
  * the forward clears its own status words, so the layer's samples that were not positive
  * definite are not readable afterwards through this entry point. Two calls whose work can
  * overlap on the GPU (different streams, or different layers on one device) race on the
@@ -221,9 +252,22 @@ dyra_status dyra_workspace_tensor(const dyra_layer *layer, int batch, int n, int
 dyra_status dyra_linear_forward_static(const dyra_layer *layer, const void *X, int batch, int n,
                                        void *Y, cudaStream_t stream);
 
+/* Self-test of the failure path (packaging: the pages have no counterpart). Launches one
+ * CTA whose bounded mbarrier wait -- the same wait every kernel of the forward uses, with
+ * its limit set to limit_us microseconds instead of 2 s -- runs on a barrier that nothing
+ * arrives on. The wait gives up, counts itself in status_words[1] and the kernel returns.
+ * status_words: device, at least 2 ints, 4-byte aligned, caller-owned; zeroed by this call.
+ * Synchronises `stream`. Returns DYRA_ERR_TIMEOUT when the wait gave up (the designed
+ * outcome), DYRA_OK if it did not, INVALID_ARG for limit_us outside [1, 2000000] or a bad
+ * pointer, CUDA on a launch error. */
+dyra_status dyra_selftest_bounded_wait(int limit_us, int *status_words, cudaStream_t stream);
+
+/* Text of a status code (static string). Packaging: the pages have no counterpart. */
 const char *dyra_status_string(dyra_status status);
-/* Text of the last CUDA/driver error seen by this thread inside the library ("" if none). */
+/* Text of the last CUDA/driver error seen by this thread inside the library ("" if none).
+ * Packaging: the pages have no counterpart. */
 const char *dyra_last_error(void);
+/* DYRA_ABI_VERSION of the loaded library. */
 int dyra_abi_version(void);
 
 #ifdef __cplusplus

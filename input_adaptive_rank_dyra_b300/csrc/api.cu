@@ -1137,16 +1137,43 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 void *g_static_ptr[kMaxDevices] = {};
+void *g_static_ctx[kMaxDevices] = {};   // the context g_static_ptr[device] belongs to
 
-// Device address of g_static_scratch on the current device (set up on first use).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+// The current CUDA context of the calling thread (the device's primary context once the
+// runtime has used it), or nullptr if the driver entry point is unavailable.
+void *current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) == CUDA_SUCCESS) return c;
+  return nullptr;
+}
+
+// Device address of g_static_scratch on the current device. Looked up on the first call on a
+// device and again whenever the device's context has changed since (a cudaDeviceReset
+// destroys the primary context and the module image that holds the array).
 dyra_status static_scratch(int device, void **out) {
   if (device < 0 || device >= kMaxDevices) return DYRA_ERR_NO_DEVICE;
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[device]) {
-    void *ptr = nullptr;
+  // cudaSetDevice (the caller's DeviceGuard) has made the device's primary context current
+  void *ptr = g_static_ptr[device];
+  void *ctx = current_context();
+  if (!ptr || !ctx || ctx != g_static_ctx[device]) {
+    ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(g_static_scratch)");
     g_static_ptr[device] = ptr;
+    g_static_ctx[device] = current_context();
   }
   *out = g_static_ptr[device];
   return DYRA_OK;
@@ -1333,6 +1360,18 @@ dyra_status dyra_linear_forward_static(const dyra_layer *L, const void *X, int b
   if (ss != DYRA_OK) return ss;
   Recorder rec;
   return forward_impl(L, X, batch, n, Y, ws, (size_t)DYRA_STATIC_SCRATCH_BYTES, stream, rec);
+}
+
+dyra_status dyra_selftest_bounded_wait(int limit_us, int *status_words, cudaStream_t stream) {
+  if (!status_words || limit_us < 1 || limit_us > 2000000) return DYRA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(status_words) & 3) return DYRA_ERR_INVALID_ARG;
+  DY_CUDA(cudaMemsetAsync(status_words, 0, 2 * sizeof(int), stream));
+  DY_CUDA(dyra::launch_bounded_wait_probe(status_words, 1000ull * (unsigned long long)limit_us,
+                                          stream));
+  DY_CUDA(cudaStreamSynchronize(stream));
+  int h[2] = {0, 0};
+  DY_CUDA(cudaMemcpy(h, status_words, sizeof(h), cudaMemcpyDeviceToHost));
+  return h[1] > 0 ? DYRA_ERR_TIMEOUT : DYRA_OK;
 }
 
 const char *dyra_status_string(dyra_status s) {

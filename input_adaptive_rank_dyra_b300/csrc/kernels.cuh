@@ -19,6 +19,10 @@ cudaError_t launch_ns_prep(const float *G, int batch, int r, float ridge, float 
 cudaError_t launch_ns_finish(const float *X, const float *dinv, int batch, int r, const int *flags,
                              __nv_bfloat16 *Ginv, float *G32, int *status, cudaStream_t s);
 
+// failure-path self-test (probe.cu): one CTA whose bounded mbarrier wait, limited to
+// limit_ns, runs out on a barrier nothing arrives on; counted in status[1]
+cudaError_t launch_bounded_wait_probe(int *status, unsigned long long limit_ns, cudaStream_t s);
+
 // fp32 path (f32_path.cu)
 cudaError_t launch_sgemm(int batch, int M, int N, int K, const float *A, long long sAb,
                          long long sAi, long long sAk, const float *B, long long sBb, long long sBk,

@@ -68,13 +68,16 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 constexpr uint32_t kSuspendNs = 100000;   // 0.1 ms per suspended try
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *timeouts) {
+// Bounded wait for the phase with the given parity to complete: gives up after `limit_ns`
+// of global time, counts the event in *timeouts and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *timeouts,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer();
+  const uint32_t sleep_ns = limit_ns < kSuspendNs ? (uint32_t)limit_ns : kSuspendNs;
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
-    if (global_timer() - t0 > kWaitLimitNs) {
+    if (mbar_try_wait_sleep(bar, parity, sleep_ns)) return true;
+    if (global_timer() - t0 > limit_ns) {
       if (timeouts) atomicAdd(timeouts, 1);
       return false;
     }

@@ -50,7 +50,7 @@ EXPORTED = [
     "dyra_export_factors", "dyra_workspace_size", "dyra_linear_forward",
     "dyra_linear_forward_host", "dyra_linear_forward_profiled", "dyra_kernel_name",
     "dyra_workspace_status", "dyra_workspace_tensor", "dyra_status_string", "dyra_last_error",
-    "dyra_abi_version", "dyra_linear_forward_static",
+    "dyra_abi_version", "dyra_linear_forward_static", "dyra_selftest_bounded_wait",
 ]
 
 _lib = None
@@ -100,6 +100,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.dyra_last_error.restype = ctypes.c_char_p
     lib.dyra_abi_version.argtypes = []
     lib.dyra_linear_forward_static.argtypes = [vp, vp, i, i, vp, vp]
+    lib.dyra_selftest_bounded_wait.argtypes = [i, vp, vp]
     for name in EXPORTED:   # raises AttributeError if the library lacks an entry point
         getattr(lib, name)
     if path is None:
@@ -315,6 +316,16 @@ def linear_forward_profiled(layer: Layer, X, Y, workspace, events, stream=None) 
                                              len(events), ctypes.byref(rec))
     _check(st, "dyra_linear_forward_profiled")
     return rec.value
+
+
+def selftest_bounded_wait(limit_us: int, status_words, stream=None) -> int:
+    """dyra_selftest_bounded_wait: runs the failure-path probe (a bounded wait that runs out)
+    and returns its status code (TIMEOUT = 6 is the designed outcome). status_words: a CUDA
+    tensor of at least 8 bytes; its first two int32 words receive the status counters."""
+    if status_words.numel() * status_words.element_size() < 8:
+        raise ValueError("status_words needs at least two 32-bit words")
+    return load().dyra_selftest_bounded_wait(int(limit_us), ctypes.c_void_p(status_words.data_ptr()),
+                                            _stream_handle(stream))
 
 
 def workspace_status(layer: Layer, workspace, stream=None):

@@ -80,6 +80,10 @@ def test_forward_rejects_bad_arguments_without_device():
     assert lib.dyra_workspace_size(None, 1, 1, None) == 1
     assert lib.dyra_workspace_status(None, None, None, None, None) == 1
     assert lib.dyra_kernel_name(None, 0) is None
+    # the failure-path self-test checks its arguments before any CUDA call
+    assert lib.dyra_selftest_bounded_wait(1000, None, None) == 1
+    assert lib.dyra_selftest_bounded_wait(0, ctypes.c_void_p(4096), None) == 1
+    assert lib.dyra_selftest_bounded_wait(3000000, ctypes.c_void_p(4096), None) == 1
 
 
 def test_fit_lowrank_matches_oracle():

@@ -295,3 +295,8 @@ def test_full_size_sampled_rows(name):
     e_gpu = O.approximation_error(Ys, Xs, W, b)
     e_or = O.approximation_error(Yo, Xs, W, b)
     assert e_close(e_gpu, e_or), f"{name}: E gpu {e_gpu:.5f} vs oracle {e_or:.5f}"
+    if layer.solver == "newton_schulz":
+        # the iteration must also reach the explicit least-squares solution's error
+        Yc = np.concatenate(O.forward(X, prep, solver="cholesky", rows=rows))
+        e_chol = O.approximation_error(Yc, Xs, W, b)
+        assert e_close(e_gpu, e_chol), f"{name}: E gpu {e_gpu:.5f} vs explicit {e_chol:.5f}"

@@ -45,8 +45,10 @@ _CSRC = "input_adaptive_rank_dyra_b300/csrc/"
 # the source files that define each kernel of the forward (a recorded DRAM-traffic figure is
 # used only while their hash matches the one recorded with it)
 GEMM_SOURCES = [_CSRC + "tc_gemm.cu", _CSRC + "tc_gemm.cuh", _CSRC + "ptx.cuh"]
-KERNEL_SOURCES = {"spd_solve_c": [_CSRC + "solve.cu", _CSRC + "kernels.cuh"],
-                  "ns_prep": [_CSRC + "solve.cu"], "ns_finish": [_CSRC + "solve.cu"],
+KERNEL_SOURCES = {"spd_invert": [_CSRC + "solve.cu", _CSRC + "kernels.cuh"],
+                  "spd_apply_c": [_CSRC + "solve.cu", _CSRC + "kernels.cuh"],
+                  "ns_prep": [_CSRC + "solve.cu"],
+                  "ns_iterate": [_CSRC + "ns.cu", _CSRC + "ptx.cuh", _CSRC + "kernels.cuh"],
                   "monarch_permute": [_CSRC + "monarch.cu", _CSRC + "monarch.cuh"]}
 
 
@@ -110,17 +112,24 @@ def kernel_work(cfg, name: str):
         return 2.0 * B * n * d * (k + r), e * (B * n * d + (k + r) * d + B * n * (k + r))
     if name == "cg_c_gram":
         return 2.0 * B * n * r * (d + r), e * (B * n * d + B * n * r) + 4 * (B * r * d + B * r * r)
-    if name == "spd_solve_c":   # r sweeps (r^3 FMA) + G^-1 applied to d columns
-        return (B * (2.0 * r ** 3 + 2.0 * r * r * d),
-                4 * (B * r * r + B * r * d) + e * (B * r * d + B * r * r))
+    if name == "spd_invert":    # r / 4 block sweeps: about r^3 FMA; G in, G^-1 out (fp32, bf16)
+        return B * 2.0 * r ** 3, 4 * B * r * r + (4 + e) * B * r * r
+    if name == "spd_apply_c":   # C~ = G^-1 C: G^-1 and C^T (fp32) in, C~ (bf16) out
+        return B * 2.0 * r * r * d, 4 * (B * r * r + B * r * d) + e * B * r * d
     if name == "ginv_c":
         return 2.0 * B * r * r * d, 4 * (B * r * r + B * r * d) + e * B * r * d
     if name == "residual_product":
         return 2.0 * B * r * d * m, e * (B * r * d + d * m + B * r * m)
     if name == "fused_output":
         return 2.0 * B * n * (k + r) * m, e * (B * n * (k + r) + k * m + B * r * m + B * n * m) + 4 * m
-    if name.startswith("ns_"):
-        return 2.0 * B * r * r * r, 4 * 3 * B * r * r
+    if name == "ns_prep":       # G in, [E0 ; X0] out
+        return 3.0 * B * r * r, 4 * (B * r * r + 2 * B * r * r)
+    if name == "ns_iterate":    # [E ; X] E per iteration (the last one X E only), then
+        #                         G^-1 = D X D; the iterates stay in L2: [E0 ; X0] in,
+        #                         G^-1 out (fp32 and bf16)
+        t = cfg.ns_iters
+        return (B * (4.0 * (t - 1) + 2.0) * r ** 3,
+                4 * 2 * B * r * r + (4 + e) * B * r * r)
     return 0.0, 0.0
 
 
@@ -329,12 +338,68 @@ def _cpu_model() -> str:
     return "unknown"
 
 
+def _openblas():
+    """(get, set) thread-count functions of the OpenBLAS that numpy has loaded, found by its
+    exported names, or None (used when threadpoolctl is not installed)."""
+    import ctypes
+    import re
+    np.ones(2) @ np.ones(2)   # make sure the BLAS is loaded
+    try:
+        maps = open("/proc/self/maps").read()
+    except OSError:
+        return None
+    for path in sorted(set(re.findall(r"(/\S*openblas\S*\.so\S*)", maps))):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for pre in ("scipy_openblas", "openblas"):
+            for suf in ("64_", "_64_", ""):
+                g = getattr(lib, f"{pre}_get_num_threads{suf}", None)
+                st = getattr(lib, f"{pre}_set_num_threads{suf}", None)
+                if g is not None and st is not None:
+                    g.restype = ctypes.c_int
+                    st.argtypes = [ctypes.c_int]
+                    return g, st
+    return None
+
+
 def _blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
         return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
     except Exception:
+        ob = _openblas()
+        if ob is not None:
+            return int(ob[0]())
         return os.cpu_count() or 1
+
+
+class _one_blas_thread:
+    """Limits numpy's BLAS to one thread inside the block (threadpoolctl, else OpenBLAS's own
+    thread-count calls)."""
+
+    def __enter__(self):
+        self._ctx, self._ob, self._prev = None, None, None
+        try:
+            from threadpoolctl import threadpool_limits
+            self._ctx = threadpool_limits(limits=1)
+            self._ctx.__enter__()
+            return self
+        except ImportError:
+            pass
+        self._ob = _openblas()
+        if self._ob is None:
+            raise RuntimeError("no way to limit the BLAS thread count")
+        self._prev = int(self._ob[0]())
+        self._ob[1](1)
+        return self
+
+    def __exit__(self, *exc):
+        if self._ctx is not None:
+            self._ctx.__exit__(*exc)
+        elif self._ob is not None:
+            self._ob[1](self._prev)
 
 
 def _solver_of(cfg) -> str:
@@ -364,8 +429,7 @@ def oracle_baseline(cfg, seconds: float = 10.0):
         reps += 1
     one = None
     try:
-        from threadpoolctl import threadpool_limits
-        with threadpool_limits(limits=1):
+        with _one_blas_thread():
             t1, dt1 = oracle_pass(cfg)
         one = {"value": t1 / dt1, "unit": "tokens/s", "cores": 1, "seconds": dt1}
     except Exception as e:   # reported, never fatal
@@ -480,7 +544,7 @@ def measure_config(cfg, args, dev, world, pk, with_e2e: bool, clocks=None):
     i = 0
     # W warm-up replays at least, and enough of them (about a second) for the clock sampler
     # to see the GPU under load before the timed region
-    while i < Wm or time.perf_counter() - t_start < 1.0:
+    while i < Wm or time.perf_counter() - t_start < args.clock_warmup_s:
         flush.fill_(1.0)
         g_plain.replay()
         i += 1
@@ -669,6 +733,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only the headline workload")
+    ap.add_argument("--clock-warmup-s", type=float, default=1.0,
+                    help="seconds of warm-up replays before the timed region (0: only W of "
+                         "them, e.g. under a profiler)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -2,4 +2,4 @@
 correction, behind a C ABI (include/dyra.h) and this thin ctypes binding."""
 from .dyra import (DyraError, Layer, fit, linear_forward, linear_forward_host,  # noqa: F401
                    linear_forward_profiled, linear_forward_static, load, new_workspace,
-                   prepare, workspace_status, workspace_view)
+                   prepare, selftest_bounded_wait, workspace_status, workspace_view)

@@ -82,7 +82,7 @@ struct DeviceGuard {
 // ------------------------------------------------------------------------ workspace
 
 struct WsLayout {
-  size_t T = 0, C = 0, G = 0, Ginv = 0, Gh = 0, X0 = 0, X1 = 0, Pt = 0, dinv = 0, flags = 0,
+  size_t T = 0, C = 0, G = 0, Ginv = 0, EX0 = 0, EX1 = 0, G32 = 0, dinv = 0, flags = 0,
          B = 0, R = 0, Cs = 0, total = 0;
   int ldT = 0;
 };
@@ -102,11 +102,10 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
     w.C = take(B * d * r * 4);   // C^T, fp32
     w.G = take(B * r * r * 4);
     w.Ginv = take(B * r * r * 2);
+    w.G32 = take(B * r * r * 4);         // fp32 G^-1, read by the apply step
     if (L->solver == DYRA_SOLVE_NEWTON_SCHULZ) {
-      w.Gh = take(B * r * r * 4);
-      w.X0 = take(B * r * r * 4);
-      w.X1 = take(B * r * r * 4);
-      w.Pt = take(B * r * r * 4);
+      w.EX0 = take(B * 3 * r * r * 4);   // [E ; X ; I + E] iterate, two buffers
+      w.EX1 = take(B * 3 * r * r * 4);
       w.dinv = take(B * r * 4);
       w.flags = take(B * 4);
     }
@@ -132,12 +131,12 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
 // same buffers, so a steady-state forward costs only its launches on the host.
 
 struct Step {
-  enum Kind { GEMM, SPD_SOLVE, NS_PREP, NS_FINISH, PERMUTE } kind = GEMM;
+  enum Kind { GEMM, SPD_INVERT, SPD_APPLY, NS_PREP, NS_FUSED, PERMUTE } kind = GEMM;
   dyra::TcGemmParams p;
   CUtensorMap a0, a1, b0, b1, out;
+  CUtensorMap ns_maps[2][3];
   const float *G = nullptr;
-  float *Gh = nullptr, *X0 = nullptr, *dinv = nullptr;
-  const float *Xf = nullptr;
+  float *X0 = nullptr, *X1 = nullptr, *dinv = nullptr;
   int *flags = nullptr;
   __nv_bfloat16 *Ginv = nullptr;
   __nv_bfloat16 *T = nullptr;
@@ -236,7 +235,6 @@ dyra_status set_flat_rows(dyra::TcGemmParams &p, CUtensorMap &a0, CUtensorMap &o
 dyra::TcGemmParams base_params() {
   dyra::TcGemmParams p;
   std::memset(&p, 0, sizeof(p));
-  p.rb = 1 << 30;
   p.alpha = 1.f;
   p.cluster = 1;
   p.a_k1 = -1;
@@ -388,29 +386,29 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     const dyra_status fs = plan_monarch_front(L, X, batch, n, T, ldT, status, plan);
     if (fs != DYRA_OK) return fs;
   } else {
+    // X and T are dense [batch * n] row blocks: the static and L columns of every token are
+    // independent of its sample, so the GEMM tiles the flat rows (no per-sample tail tiles)
     CUtensorMap a, b, o;
     const int N = ldT;
-    const int nt = (int)cdiv(N, 256);
-    const int BN = roundup((int)cdiv(N, nt), 32);
-    DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
+    const long long rows = (long long)batch * n;
+    const int BN = pick_bn(rows, N, 32);
+    DY_MAP(make_map(&a, X, 2, d, rows, 1, d, 0, 128));
     DY_MAP(make_map(&b, L->w1, 2, d, N, 1, d, 0, BN / kBDiv));
-    DY_MAP(make_store_map(&o, T, N, n, batch, ldT, (long long)n * ldT));
+    DY_MAP(make_store_map(&o, T, N, rows, 1, ldT, 0));
     TcGemmParams p = base_params();
-    p.m_tiles = (int)cdiv(n, 128);
-    p.n_tiles = nt;
-    p.batch = batch;
+    p.m_tiles = (int)cdiv(rows, 128);
+    p.n_tiles = (int)cdiv(N, BN);
+    p.batch = 1;
     p.BN = BN;
     p.k_chunks = (int)cdiv(d, 64);
     p.elem_bytes = 2;
     p.a_split = p.m_tiles;
-    p.a_batched0 = 1;
     p.b_split = p.k_chunks;
     p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
     set_pair(p, 2, 0);
     p.epi = EPI_ROW_BF16;
     p.tma_store = 1;
-    p.out_batched = 1;
-    p.rows_valid = n;
+    p.rows_valid = (int)rows;
     p.cols_valid = N;
     p.timeouts = status + 1;
     Step st = gemm_step(p, a, a, b, b);
@@ -450,11 +448,13 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.timeouts = status + 1;
     plan.steps.push_back(gemm_step(p, ax, al, al, al));
   }
-  // 3. C~ = (G + lambda I)^-1 C: one kernel on the Cholesky branch; on the Newton-Schulz
-  //    branch a chain of small kernels and tf32 GEMMs forms G^-1, then a bf16 GEMM applies it.
+  // 3. C~ = (G + lambda I)^-1 C: on the Cholesky branch one CTA per sample inverts G, then
+  //    a wide kernel applies the inverse to C; on the Newton-Schulz branch a chain of small
+  //    kernels and tf32 GEMMs forms G^-1, then a tf32 GEMM applies it.
+  float *G32 = reinterpret_cast<float *>(ws + w.G32);
   if (L->solver == DYRA_SOLVE_CHOLESKY) {
     Step st;
-    st.kind = Step::SPD_SOLVE;
+    st.kind = Step::SPD_INVERT;
     st.G = G;
     st.batch = batch;
     st.r = r;
@@ -463,15 +463,19 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     st.Ct = Ct;
     st.Cs = Cs;
     st.Ginv = Ginv;
+    st.G32 = G32;
     st.status = status;
     plan.steps.push_back(st);
+    st.kind = Step::SPD_APPLY;
+    plan.steps.push_back(st);
   } else {
-    float *Gh = reinterpret_cast<float *>(ws + w.Gh);
-    float *Xa = reinterpret_cast<float *>(ws + w.X0);
-    float *Xb = reinterpret_cast<float *>(ws + w.X1);
-    float *Pt = reinterpret_cast<float *>(ws + w.Pt);
+    // Newton-Schulz in residual form: EX = [E ; X ; Y] per sample ([3r][r] fp32, Y = I + E,
+    // two buffers used in turn); each iteration forms X' = X Y, E' = E E and Y' = I + E'.
+    float *EXa = reinterpret_cast<float *>(ws + w.EX0);
+    float *EXb = reinterpret_cast<float *>(ws + w.EX1);
     float *dinv = reinterpret_cast<float *>(ws + w.dinv);
     int *flags = reinterpret_cast<int *>(ws + w.flags);
+    const long long ex_bs = 3LL * r * r;   // elements between samples of EX
     {
       Step st;
       st.kind = Step::NS_PREP;
@@ -479,74 +483,38 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
       st.batch = batch;
       st.r = r;
       st.ridge = (float)L->ridge;
-      st.Gh = Gh;
-      st.X0 = Xa;
+      st.X0 = EXa;
       st.dinv = dinv;
       st.flags = flags;
       plan.steps.push_back(st);
     }
-    // Both GEMMs of an iteration read K-major operands only. X_t stays symmetric (a
-    // polynomial in G_hat), so its rows serve as the columns of the B operand of
-    // P = G_hat X_t; P is stored transposed so X_{t+1} = 2 X_t - X_t P reads it K-major too.
-    const int BN = roundup(r, kPairMma ? 32 : 16);
-    for (int it = 0; it < L->ns_iters; ++it) {
-      CUtensorMap a, b;
-      DY_MAP(make_map(&a, Gh, 4, r, r, batch, r, (long long)r * r, 128));
-      DY_MAP(make_map(&b, Xa, 4, r, r, batch, r, (long long)r * r, BN / kBDiv));
-      TcGemmParams p = base_params();
-      p.m_tiles = (int)cdiv(r, 128);
-      p.n_tiles = 1;
-      p.batch = batch;
-      p.BN = BN;
-      p.k_chunks = (int)cdiv(r, 32);
-      p.elem_bytes = 4;
-      p.a_split = p.m_tiles;
-      p.a_batched0 = 1;
-      p.b_split = p.k_chunks;
-      p.b_batched0 = 1;
-      p.idesc = tc_idesc(4, 0, 0, BN);
-      set_pair(p, 4, 0);
-      p.epi = EPI_TRANS_F32;
-      p.out = Pt;
-      p.out_bstride = (long long)r * r;
-      p.rb = r;
-      p.out_gstride = 0;
-      p.out_ld = r;
-      p.rows_valid = r;
-      p.cols_valid = r;
-      p.timeouts = status + 1;
-      plan.steps.push_back(gemm_step(p, a, a, b, b));   // P^T = (G_hat X)^T
-      DY_MAP(make_map(&a, Xa, 4, r, r, batch, r, (long long)r * r, 128));
-      DY_MAP(make_map(&b, Pt, 4, r, r, batch, r, (long long)r * r, BN / kBDiv));
-      p.epi = EPI_ROW_F32;
-      p.out = Xb;
-      p.out_bstride = (long long)r * r;
-      p.out_ld = r;
-      p.aux = Xa;
-      p.aux_bstride = (long long)r * r;
-      p.aux_ld = r;
-      p.alpha = -1.f;
-      p.beta = 2.f;
-      plan.steps.push_back(gemm_step(p, a, a, b, b));   // X' = 2X - X P
-      std::swap(Xa, Xb);
+    {
+      // every iteration and the finish (G^-1 = D X D) in one kernel
+      Step st;
+      st.kind = Step::NS_FUSED;
+      float *bufs[2] = {EXa, EXb};
+      for (int bi = 0; bi < 2; ++bi)
+        for (int blk = 0; blk < 3; ++blk)
+          DY_MAP(make_map(&st.ns_maps[bi][blk], bufs[bi] + (size_t)blk * r * r, 4, r, r, batch, r,
+                          ex_bs, 128));
+      st.X0 = EXa;
+      st.X1 = EXb;
+      st.dinv = dinv;
+      st.batch = batch;
+      st.r = r;
+      st.nb = L->ns_iters;
+      st.flags = flags;
+      st.Ginv = Ginv;
+      st.G32 = G32;
+      st.status = status;
+      plan.steps.push_back(st);
     }
-    Step st;
-    st.kind = Step::NS_FINISH;
-    st.Xf = Xa;
-    st.dinv = dinv;
-    st.batch = batch;
-    st.r = r;
-    st.flags = flags;
-    st.Ginv = Ginv;
-    st.G32 = Pt;   // fp32 G^-1 for the apply GEMM (Pt is free after the iterations)
-    st.status = status;
-    plan.steps.push_back(st);
     // C~ = G^-1 C as a tf32 GEMM: M = r rows of G^-1 (fp32, K-major), N = d, K = r, with
     // B = C^T [d, r] (K-major); bf16 result [batch, r, d]
     {
       CUtensorMap a, b, o;
       const int BN = pick_bn((long long)batch * cdiv(r, 128) * 128, d, 32);
-      DY_MAP(make_map(&a, Pt, 4, r, r, batch, r, (long long)r * r, 128));
+      DY_MAP(make_map(&a, G32, 4, r, r, batch, r, (long long)r * r, 128));
       DY_MAP(make_map(&b, Ct, 4, r, d, batch, r, (long long)d * r, BN / kBDiv));
       DY_MAP(make_store_map(&o, Cs, d, r, batch, d, (long long)r * d));
       TcGemmParams p = base_params();
@@ -703,20 +671,22 @@ dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream
       case Step::GEMM:
         DY_TIMED(rec, ks, tc_gemm_launch(st.p, st.a0, st.a1, st.b0, st.b1, st.out, ks));
         break;
-      case Step::SPD_SOLVE:
-        DY_TIMED(rec, ks, launch_spd_solve(st.G, st.batch, st.r, st.ridge, st.Ct, st.d, st.Cs,
-                                            st.Ginv, st.status, ks));
+      case Step::SPD_INVERT:
+        DY_TIMED(rec, ks, launch_spd_invert(st.G, st.batch, st.r, st.ridge, st.G32, st.Ginv,
+                                             st.status, ks));
+        break;
+      case Step::SPD_APPLY:
+        DY_TIMED(rec, ks, launch_spd_apply(st.G32, st.batch, st.r, st.Ct, st.d, st.Cs, ks));
         break;
       case Step::NS_PREP:
-        DY_TIMED(rec, ks,
-                 launch_ns_prep(st.G, st.batch, st.r, st.ridge, st.Gh, st.X0, st.dinv, st.flags, ks));
+        DY_TIMED(rec, ks, launch_ns_prep(st.G, st.batch, st.r, st.ridge, st.X0, st.dinv, st.flags, ks));
         break;
       case Step::PERMUTE:
         DY_TIMED(rec, ks, launch_monarch_permute(st.T, st.rows, st.ldT, st.nb, ks));
         break;
-      case Step::NS_FINISH:
-        DY_TIMED(rec, ks, launch_ns_finish(st.Xf, st.dinv, st.batch, st.r, st.flags, st.Ginv,
-                                           st.G32, st.status, ks));
+      case Step::NS_FUSED:
+        DY_TIMED(rec, ks, launch_ns_fused(st.ns_maps, st.batch, st.r, st.nb, st.X0, st.X1,
+                                          st.dinv, st.flags, st.G32, st.Ginv, st.status, ks));
         break;
       default:
         break;
@@ -768,7 +738,7 @@ dyra_status forward_f32(const dyra_layer *L, const float *X, int batch, int n, f
   return DYRA_OK;
 }
 
-const char *const kNamesChol[] = {"xproj_static_L", "cg_c_gram", "spd_solve_c",
+const char *const kNamesChol[] = {"xproj_static_L", "cg_c_gram", "spd_invert", "spd_apply_c",
                                   "residual_product", "fused_output"};
 const char *const kNamesMonarchFront[] = {"monarch_bd1", "xproj_L", "monarch_permute"};
 const char *const kNamesF32[] = {"f32_xproj", "f32_gram_f64", "f32_c", "f32_b",
@@ -778,8 +748,8 @@ const char *const kNamesF32[] = {"f32_xproj", "f32_gram_f64", "f32_c", "f32_b",
 int kernels_per_forward(const dyra_layer *L) {
   if (L->dtype == DYRA_F32) return 8;
   const int front = L->kind == DYRA_STATIC_MONARCH ? 3 : 1;
-  if (L->solver == DYRA_SOLVE_CHOLESKY) return front + 4;
-  return front + 6 + 2 * L->ns_iters;
+  // Cholesky: invert, apply; Newton-Schulz: prep, fused iterations, apply GEMM
+  return front + (L->solver == DYRA_SOLVE_CHOLESKY ? 5 : 6);
 }
 
 const char *kernel_name(const dyra_layer *L, int i) {
@@ -789,13 +759,10 @@ const char *kernel_name(const dyra_layer *L, int i) {
   if (i < front) return L->kind == DYRA_STATIC_MONARCH ? kNamesMonarchFront[i] : kNamesChol[0];
   i -= front - 1;   // now indexes the low-rank list from "cg_c_gram" (= 1) on
   if (L->solver == DYRA_SOLVE_CHOLESKY) return kNamesChol[i];
-  const int it2 = 2 * L->ns_iters;
-  if (i < 2) return kNamesChol[i];
   if (i == 2) return "ns_prep";
-  if (i < 3 + it2) return ((i - 3) % 2 == 0) ? "ns_gemm_gx" : "ns_gemm_update";
-  if (i == 3 + it2) return "ns_finish";
-  if (i == 4 + it2) return "ginv_c";
-  return kNamesChol[i - it2 - 2];   // residual_product, fused_output
+  if (i == 3) return "ns_iterate";
+  if (i == 4) return "ginv_c";
+  return kNamesChol[i < 2 ? i : i - 1];   // cg_c_gram; residual_product, fused_output
 }
 
 dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, void *Y,
@@ -1020,7 +987,10 @@ dyra_layer *new_layer(const dyra_prepare_args *a, dyra_solver solver, int ns_ite
 dyra_status upload_layer(const dyra_prepare_args *a, dyra_layer *L) {
   const int d = L->d, m = L->m, k = L->k, r = L->r;
   dyra_status st = DYRA_OK;
+  // the bias in fp32, zero-padded by 256 columns: an output epilogue reads the bias of its
+  // whole last tile, which may reach past column m
   std::vector<float> bias32(L->bias.begin(), L->bias.end());
+  bias32.resize((size_t)m + 256, 0.f);
   if (a->dtype == DYRA_BF16 && L->kind == DYRA_STATIC_MONARCH) {
     const int nb = k, T0 = 256;
     std::vector<double> pt((size_t)r * d), b1((size_t)d * T0, 0.0), b2((size_t)m * T0, 0.0),

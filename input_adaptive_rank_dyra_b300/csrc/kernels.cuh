@@ -1,23 +1,34 @@
 // Launch helpers of the non-GEMM kernels of the DyRA forward.
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace dyra {
 
 // bf16 path, SPD solves (solve.cu)
-// C~ = (G + ridge I)^-1 C for r <= 64 (r % 4 == 0): G [batch][r][r] fp32, C given as
-// C^T [batch][d][r] fp32, C~ to Cs [batch][r][d] bf16; G^-1 also to Ginv [batch][r][r] bf16.
-cudaError_t launch_spd_solve(const float *G, int batch, int r, float ridge, const float *Ct,
-                             int d, __nv_bfloat16 *Cs, __nv_bfloat16 *Ginv, int *status,
-                             cudaStream_t s);
-// Newton-Schulz start: dinv = diag(G + ridge I)^-1/2, Gh = D (G + ridge I) D,
-// X0 = I / ||Gh||_inf; flags[b] marks a sample whose diagonal is not positive and finite.
-cudaError_t launch_ns_prep(const float *G, int batch, int r, float ridge, float *Gh, float *X0,
-                           float *dinv, int *flags, cudaStream_t s);
-// G^-1 from the Newton-Schulz iterate: to Ginv (bf16) and G32 (fp32), both [batch][r][r].
-cudaError_t launch_ns_finish(const float *X, const float *dinv, int batch, int r, const int *flags,
-                             __nv_bfloat16 *Ginv, float *G32, int *status, cudaStream_t s);
+// (G + ridge I)^-1 for r <= 64 (r % 4 == 0), one CTA per sample: G [batch][r][r] fp32 to
+// Ginv32 (fp32) and Ginv (bf16), both [batch][r][r]; a sample that is not positive definite
+// gets 0 and is counted in status[0].
+cudaError_t launch_spd_invert(const float *G, int batch, int r, float ridge, float *Ginv32,
+                              __nv_bfloat16 *Ginv, int *status, cudaStream_t s);
+// C~ = G^-1 C for r <= 64: G^-1 from Ginv32, C given as C^T [batch][d][r] fp32, C~ to
+// Cs [batch][r][d] bf16.
+cudaError_t launch_spd_apply(const float *Ginv32, int batch, int r, const float *Ct, int d,
+                             __nv_bfloat16 *Cs, cudaStream_t s);
+// Newton-Schulz start (r <= 256): dinv = diag(G + ridge I)^-1/2, Gh = D (G + ridge I) D,
+// alpha = 1 / ||Gh||_inf, EX[b] = [I - alpha Gh ; alpha I ; 2I - alpha Gh] ([batch][3r][r]
+// fp32); flags[b] marks a sample whose diagonal is not positive and finite (its alpha is 0).
+cudaError_t launch_ns_prep(const float *G, int batch, int r, float ridge, float *EX, float *dinv,
+                           int *flags, cudaStream_t s);
+// All Newton-Schulz iterations and the finish in one kernel (ns.cu): from the iterate
+// EX = [E0 ; X0 ; Y0] that ns_prep leaves in ex0 ([batch][3r][r] fp32; ex1 the second
+// buffer), iters steps of X' = X Y, E' = E E, Y' = I + E', then G^-1 = D X D to G32 (fp32)
+// and Ginv (bf16). maps[i][0..2]: fp32 tensor maps of the E, X and Y blocks of buffer i
+// ([batch][r][r], row stride r, batch stride 3 r r, box {32, 128}). r <= 256, r % 8 == 0.
+cudaError_t launch_ns_fused(const CUtensorMap (&maps)[2][3], int batch, int r, int iters,
+                            float *ex0, float *ex1, const float *dinv, const int *flags, float *G32,
+                            __nv_bfloat16 *Ginv, int *status, cudaStream_t s);
 
 // failure-path self-test (probe.cu): one CTA whose bounded mbarrier wait, limited to
 // limit_ns, runs out on a barrier nothing arrives on; counted in status[1]

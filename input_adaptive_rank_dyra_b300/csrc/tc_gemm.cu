@@ -12,8 +12,7 @@ namespace dyra {
 
 namespace {
 
-constexpr uint32_t kStagingBytesPerWarp = 4 * 2048;   // two pairs of 32 x 32 bf16 buffers
-constexpr uint32_t kBiasBytesPerWarp = 512;            // the bias of a warp's (<= 128) columns
+constexpr uint32_t kStagingPairBytes = 2 * 2048;   // one pair of 32 x 32 bf16 staging tiles
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -52,11 +51,36 @@ __device__ __forceinline__ int tile_chunks(const TcGemmParams &p, const TileCoor
   return p.b_split + (s_hi - s_lo + 1) * (p.k_chunks - p.b_split);
 }
 
+// dst[0..16) = alpha * f[0..16) + beta * ax[0..16) (ax may be null) for the first `valid`
+// columns; 16-byte vector accesses when every column is valid and the rows are aligned.
+__device__ __forceinline__ void store_row16_f32(float *dst, const float *ax, const float *f,
+                                                int valid, float alpha, float beta) {
+  if (valid >= 16 && ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(ax)) & 15) == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float4 o = make_float4(alpha * f[4 * q], alpha * f[4 * q + 1], alpha * f[4 * q + 2],
+                             alpha * f[4 * q + 3]);
+      if (ax) {
+        const float4 a = *reinterpret_cast<const float4 *>(ax + 4 * q);
+        o.x += beta * a.x;
+        o.y += beta * a.y;
+        o.z += beta * a.z;
+        o.w += beta * a.w;
+      }
+      *reinterpret_cast<float4 *>(dst + 4 * q) = o;
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (j < valid) dst[j] = alpha * f[j] + (ax ? beta * ax[j] : 0.f);
+}
+
 // Epilogue of 16 accumulator columns [col0, col0 + 16) of row g, direct global stores
 // (the modes without a TMA store: C / G of the Gram kernel, fp32 Newton-Schulz products).
 __device__ __forceinline__ void epilogue16(const TcGemmParams &p, const float *f, long long g,
                                            int col0, int bz, bool second) {
-  const int cols_lim = (p.epi == EPI_CG && second) ? p.cols2_valid : p.cols_valid;
+  const int cols_lim = second ? p.cols2_valid : p.cols_valid;
   const int valid = cols_lim - col0;
   if (valid <= 0) return;
   if (p.epi == EPI_ROW_BF16) {
@@ -67,36 +91,16 @@ __device__ __forceinline__ void epilogue16(const TcGemmParams &p, const float *f
       for (int j = 0; j < 16; ++j)
         if (j < valid) dst[j] = __float2bfloat16_rn(f[j] + (p.bias ? __ldg(p.bias + col0 + j) : 0.f));
     }
-  } else if (p.epi == EPI_CG) {
-    if (!second) {
-      if (g < p.rows_valid) {
-        float *dst = reinterpret_cast<float *>(p.out) + bz * p.out_bstride + g * p.out_ld + col0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (j < valid) dst[j] = f[j];
-      }
-    } else if (g < p.rows2_valid) {
-      float *dst = reinterpret_cast<float *>(p.out2) + bz * p.out2_bstride + g * p.out2_ld + col0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j < valid) dst[j] = f[j];
-    }
-  } else if (p.epi == EPI_TRANS_F32) {
-    if (g < p.rows_valid) {
-      float *dst = reinterpret_cast<float *>(p.out) + bz * p.out_bstride +
-                   (g / p.rb) * p.out_gstride + (g % p.rb);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j < valid) dst[(long long)(col0 + j) * p.out_ld] = p.alpha * f[j];
-    }
-  } else {   // EPI_ROW_F32
+  } else if (!second) {   // EPI_CG (C^T) and EPI_ROW_F32, first region
     if (g < p.rows_valid) {
       float *dst = reinterpret_cast<float *>(p.out) + bz * p.out_bstride + g * p.out_ld + col0;
       const float *ax = p.aux ? p.aux + bz * p.aux_bstride + g * p.aux_ld + col0 : nullptr;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j < valid) dst[j] = p.alpha * f[j] + (ax ? p.beta * ax[j] : 0.f);
+      store_row16_f32(dst, ax, f, valid, p.alpha, p.beta);
     }
+  } else if (g < p.rows2_valid) {   // second region (G of the Gram kernel, X of Newton-Schulz)
+    float *dst = reinterpret_cast<float *>(p.out2) + bz * p.out2_bstride + g * p.out2_ld + col0;
+    const float *ax = p.aux2 ? p.aux2 + bz * p.aux2_bstride + g * p.aux2_ld + col0 : nullptr;
+    store_row16_f32(dst, ax, f, valid, p.alpha, p.beta);
   }
 }
 
@@ -416,43 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int u_lo = (e < 4) ? 0 : (units + 1) / 2;
     const int u_hi = (e < 4) ? (units + 1) / 2 : units;
     const int c_lo = u_lo * 32, c_hi = u_hi * 32 < p.BN ? u_hi * 32 : p.BN;
-    const uint32_t stg = staging + (uint32_t)e * kStagingBytesPerWarp;
-    // this warp's slice of the bias, staged in shared memory once per tile
-    float *bias_s = reinterpret_cast<float *>(
-        smem + (staging - base) + (uint32_t)kEpiWarps * kStagingBytesPerWarp + (uint32_t)e * kBiasBytesPerWarp);
-    const bool stage_bias = p.tma_store && p.bias;
-    // bias[n_tile * BN + c_lo + 4 lane .. + 3] (zeros past the last column)
-    auto load_bias = [&](int n_tile) {
-      float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int c = n_tile * p.BN + c_lo + 4 * lane;
-      if (c_lo + 4 * lane < c_hi) {
-        if (c + 3 < p.cols_valid) {
-          bb = __ldg(reinterpret_cast<const float4 *>(p.bias + c));
-        } else {
-          if (c < p.cols_valid) bb.x = __ldg(p.bias + c);
-          if (c + 1 < p.cols_valid) bb.y = __ldg(p.bias + c + 1);
-          if (c + 2 < p.cols_valid) bb.z = __ldg(p.bias + c + 2);
-        }
-      }
-      return bb;
-    };
+    // this warp's staging tiles: epi_bufs pairs, used in turn
+    const uint32_t stg = staging + (uint32_t)e * (uint32_t)p.epi_bufs * kStagingPairBytes;
+    const bool add_bias = p.tma_store && p.bias;
     uint32_t buf_i = 0, i = 0;
-    // the next tile's coordinates and bias are fetched one tile ahead
     TileCoord tcn = decode_tile(cid < total ? cid : 0, p, mp_tiles, crank);
-    float4 bnext = (stage_bias && cid < total) ? load_bias(tcn.n_tile) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int t = cid; t < total; t += ncl, ++i) {
       const uint32_t acc = i & 1u;
       const TileCoord tc = tcn;
-      const float4 bcur = bnext;
-      if (t + ncl < total) {
-        tcn = decode_tile(t + ncl, p, mp_tiles, crank);
-        if (stage_bias) bnext = load_bias(tcn.n_tile);
-      }
-      if (stage_bias) {
-        __syncwarp();   // the previous tile's reads of bias_s are done
-        reinterpret_cast<float4 *>(bias_s)[lane] = bcur;
-        __syncwarp();
-      }
+      if (t + ncl < total) tcn = decode_tile(t + ncl, p, mp_tiles, crank);
       int got = 0;
       if (lane == 0) got = ptx::mbar_wait(tfull_bar + 8u * acc, (i >> 1) & 1u, p.timeouts) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -473,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = (second ? tc.m_tile - p.a_split : tc.m_tile) * 128;
       const int n0 = tc.n_tile * p.BN;
       const uint32_t taddr = tmem_base + acc * p.acc_cols + ((uint32_t)(q * 32) << 16);
-      const int cols_lim = (p.epi == EPI_CG && second) ? p.cols2_valid : p.cols_valid;
+      const int cols_lim = second ? p.cols2_valid : p.cols_valid;
       if (p.tma_store) {
         // bf16 rows. A warp has at most 128 columns of a tile: up to four 32-column pieces,
         // handled in pairs. Both TMEM loads of a pair complete (tcgen05.wait::ld) before any
@@ -498,13 +474,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tmem_ld32(taddr + (uint32_t)(c_lo + 32 * s0), v[0]);
               if (two) ptx::tmem_ld32(taddr + (uint32_t)(c_lo + 32 * s0 + 32), v[1]);
               ptx::tmem_ld_wait();
-              if (stage_bias) {   // every lane reads the same bytes: a shared-memory broadcast
+              if (add_bias) {   // every lane reads the same bytes: one broadcast line per load
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                  const float4 *b4 = reinterpret_cast<const float4 *>(bias_s + 32 * (s0 + h));
+                  // the bias array is padded to a multiple of 256 columns (no bound check)
+                  const float4 *b4 =
+                      reinterpret_cast<const float4 *>(p.bias + n0 + c_lo + 32 * (s0 + h));
 #pragma unroll
                   for (int j = 0; j < 8; ++j) {
-                    const float4 bb = b4[j];
+                    const float4 bb = __ldg(b4 + j);
                     v[h][4 * j + 0] = __float_as_uint(__uint_as_float(v[h][4 * j + 0]) + bb.x);
                     v[h][4 * j + 1] = __float_as_uint(__uint_as_float(v[h][4 * j + 1]) + bb.y);
                     v[h][4 * j + 2] = __float_as_uint(__uint_as_float(v[h][4 * j + 2]) + bb.z);
@@ -512,9 +490,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                   }
                 }
               }
-              if (lane == 0) ptx::bulk_wait_read<1>();   // this pair was read by its last group
+              // the pair about to be overwritten has been read by the group that stored it
+              if (lane == 0) {
+                if (p.epi_bufs > 1)
+                  ptx::bulk_wait_read<1>();
+                else
+                  ptx::bulk_wait_read<0>();
+              }
               __syncwarp();
-              const uint32_t buf = stg + buf_i * 4096u;
+              const uint32_t buf = stg + buf_i * kStagingPairBytes;
               stage_bits32(buf, lane, v[0]);
               if (two) stage_bits32(buf + 2048u, lane, v[1]);
               ptx::fence_proxy_async_smem();
@@ -524,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (two) ptx::tma_store_3d(&tmOut, buf + 2048u, n0 + c_lo + 32 * s0 + 32, row0, zb);
                 ptx::bulk_commit();
               }
-              buf_i ^= 1u;
+              if (++buf_i == (uint32_t)p.epi_bufs) buf_i = 0;
             }
           }
         }
@@ -716,7 +700,11 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
     if (p.a_major) return cudaErrorNotSupported;
   }
   const uint32_t stage = 16384u + (uint32_t)p.BN * 128u / (p.pair_mma ? 2u : 1u);
-  const uint32_t staging = p.tma_store ? (uint32_t)kEpiWarps * (kStagingBytesPerWarp + kBiasBytesPerWarp) : 0u;
+  // Epilogue staging: two pairs of tiles per warp when a tile's main loop is short (the
+  // epilogue then sets the pace and alternates pairs without waiting), one pair otherwise,
+  // which leaves room for more pipeline stages to hide the operand loads' latency.
+  if (p.epi_bufs != 1 && p.epi_bufs != 2) p.epi_bufs = p.k_chunks <= 6 ? 2 : 1;
+  const uint32_t staging = p.tma_store ? (uint32_t)kEpiWarps * (uint32_t)p.epi_bufs * kStagingPairBytes : 0u;
   const uint32_t fixed = 1024u + staging + 256u;   // alignment slack, staging, barriers
   int S = (int)((232448u - fixed) / stage);
   if (S > 8) S = 8;

@@ -38,8 +38,9 @@ enum TcEpi : int {
   EPI_ROW_BF16 = 0,    // out[b][g][c] = bf16(acc + bias[c]); TMA store when tma_store is set
   EPI_CG = 2,          // m tiles < a_split: out[b*bs + g*ld + c] = acc     (C^T, fp32)
                        // m tiles >= a_split: out2[b*bs2 + g*ld2 + c] = acc  (G, fp32)
-  EPI_ROW_F32 = 3,     // out[b][g][c] = alpha*acc + beta*aux[b][g][c]   (fp32)
-  EPI_TRANS_F32 = 4    // out[b*bs + (g/rb)*gs + g%rb + c*ld] = alpha*acc (fp32)
+  EPI_ROW_F32 = 3      // m tiles < a_split: out[b][g][c] = alpha*acc + beta*aux[b][g][c]
+                       // m tiles >= a_split: out2[b][g][c] = alpha*acc + beta*aux2[b][g][c]
+                       // (fp32; aux / aux2 may be null; 16-byte vector accesses)
 };
 
 struct TcGemmParams {
@@ -81,17 +82,17 @@ struct TcGemmParams {
   // epilogue
   int epi;
   int tma_store;     // EPI_ROW_BF16 through the output tensor map (needs BN % 32 == 0)
+  int epi_bufs;      // staging-tile pairs per epilogue warp (1 or 2; 0: chosen at launch)
   int out_batched;   // output map carries the batch coordinate
   void *out;
-  long long out_bstride, out_ld, out_gstride;
-  int rb;
+  long long out_bstride, out_ld;
   int rows_valid, cols_valid;     // region of tiles < a_split
   void *out2;
   long long out2_bstride, out2_ld;
-  int rows2_valid, cols2_valid;   // region of tiles >= a_split (EPI_CG)
+  int rows2_valid, cols2_valid;   // region of tiles >= a_split (EPI_CG, EPI_ROW_F32)
   const float *bias;
-  const float *aux;
-  long long aux_bstride, aux_ld;
+  const float *aux, *aux2;        // addends of EPI_ROW_F32's two regions (or null)
+  long long aux_bstride, aux_ld, aux2_bstride, aux2_ld;
   float alpha, beta;
   int *timeouts;                  // device counter of bounded waits that gave up
 };

@@ -625,6 +625,88 @@ def measure_config(cfg, args, dev, world, pk, with_e2e: bool, clocks=None):
     return out
 
 
+def measure_mlp(cfg1, cfg2, args, dev, world):
+    """The DINOv3 MLP block, fc1 -> GELU -> fc2, with both layers replaced (one
+    dyra_mlp_forward call, CUDA-graph replays, L2 flushed before each step), next to the dense
+    block addmm -> gelu -> addmm (cuBLAS) on the same input."""
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    W1, b1 = WL.make_weights(cfg1)
+    W2, b2 = WL.make_weights(cfg2)
+    fc1 = dy.prepare(W1, b1, kind=cfg1.kind, k=cfg1.k, r=cfg1.r, dtype="bf16", device=dev.index,
+                     activation="gelu")
+    fc2 = dy.prepare(W2, b2, kind=cfg2.kind, k=cfg2.k, r=cfg2.r, dtype="bf16", device=dev.index)
+    X = WL.make_inputs(cfg1)
+    Xd = _torch_input(cfg1, X).to(dev)
+    B, n = cfg1.batch, cfg1.n
+    H = torch.empty((B, n, cfg1.m), dtype=torch.bfloat16, device=dev)
+    Y = torch.empty((B, n, cfg2.m), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(fc1.workspace_size(B, n), fc2.workspace_size(B, n)), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    K, Wm = args.steps, args.warmup
+    for _ in range(3):
+        dy.mlp_forward(fc1, fc2, Xd, H, Y, ws)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        dy.mlp_forward(fc1, fc2, Xd, H, Y, ws, stream=cap)
+    for _ in range(Wm):
+        flush.fill_(1.0)
+        g.replay()
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    torch.cuda.synchronize()
+    barrier(world)
+    for i in range(K):
+        flush.fill_(float(i))
+        st[i].record(stream)
+        g.replay()
+        en[i].record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(float(np.mean([st[i].elapsed_time(en[i]) for i in range(K)])), world)
+    nsp, tmo = dy.workspace_status(fc2, ws)
+    if tmo:
+        raise RuntimeError(f"MLP block: {tmo} bounded waits timed out")
+    W1d = torch.from_numpy(WL.bf16_bits(W1).view(np.int16)).view(torch.bfloat16).to(dev)
+    W2d = torch.from_numpy(WL.bf16_bits(W2).view(np.int16)).view(torch.bfloat16).to(dev)
+    b1d = torch.from_numpy(b1.astype(np.float32)).to(dev).to(torch.bfloat16)
+    b2d = torch.from_numpy(b2.astype(np.float32)).to(dev).to(torch.bfloat16)
+    X2 = Xd.view(-1, cfg1.d)
+    Hd = torch.empty((B * n, cfg1.m), dtype=torch.bfloat16, device=dev)
+    Yd = torch.empty((B * n, cfg2.m), dtype=torch.bfloat16, device=dev)
+
+    def dense():
+        torch.addmm(b1d, X2, W1d, out=Hd)
+        Hg = torch.nn.functional.gelu(Hd)
+        torch.addmm(b2d, Hg, W2d, out=Yd)
+
+    for _ in range(Wm):
+        flush.fill_(1.0)
+        dense()
+    for i in range(K):
+        flush.fill_(float(i))
+        st[i].record(stream)
+        dense()
+        en[i].record(stream)
+    torch.cuda.synchronize()
+    dense_ms = float(np.mean([st[i].elapsed_time(en[i]) for i in range(K)]))
+    fl = layer_flops(cfg1) + layer_flops(cfg2)
+    out = {"workload": "c3_dinov3_vitl16_mlp_block", "latency_us": ms * 1e3,
+           "tokens_per_s": world * B * n / (ms * 1e-3),
+           "tc_frac_of_peak": fl / (ms * 1e-3) / (peaks()[0]["bf16_tflops"] * 1e12),
+           "dense_cublas": {"us": dense_ms * 1e3, "tokens_per_s": B * n / (dense_ms * 1e-3),
+                            "speedup_of_dyra": dense_ms / ms,
+                            "what": "addmm -> gelu -> addmm (bf16)"},
+           "layers": [cfg1.name + " (GELU in its output epilogue)", cfg2.name],
+           "not_spd_samples": nsp}
+    fc1.close()
+    fc2.close()
+    return out
+
+
 def summarize(res, pk, pk_kind):
     """The per-configuration numbers: latency, dense reference, TC and roofline fractions,
     per-kernel times (keyed by launch index) and the roofline of the dominant kernel."""
@@ -695,6 +777,8 @@ def run_dyra(args, cfg):
                 continue
             others.append(summarize(measure_config(c, args, dev, world, pk, with_e2e=False),
                                     pk, pk_kind))
+        others.append(measure_mlp(WL.get_config("c3_fc1"), WL.get_config("c3_fc2"), args, dev,
+                                  world))
     tokens = head["tokens"]
     ebytes = 2 if cfg.dtype == "bf16" else 4
     line = {

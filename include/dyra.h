@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define DYRA_ABI_VERSION 2
+#define DYRA_ABI_VERSION 3
 
 typedef enum dyra_status {
   DYRA_OK = 0,
@@ -69,6 +69,25 @@ typedef enum dyra_solver {
   DYRA_SOLVE_NEWTON_SCHULZ = 2 /* ns_iters steps of X <- X (2I - G X) after Jacobi scaling */
 } dyra_solver;
 
+/* Input-aware static decomposition (summary page Appendix B; blog section
+ * "已有结构化矩阵方法分工有何不同": calibration activations define an input-side transform S, the
+ * weight is written W = (W S) S^-1 and W S is truncated by its SVD). In this library's
+ * row-vector convention y = x W that is W_hat = S^-T TSVD_k(S^T W). Low-rank layers only. */
+typedef enum dyra_input_aware {
+  DYRA_INPUT_AWARE_NONE = 0,      /* plain truncated SVD of W                                */
+  DYRA_INPUT_AWARE_DIAG = 1,      /* S = diag(rms of each input channel over calib rows)     */
+  DYRA_INPUT_AWARE_CHOLESKY = 2   /* S = lower Cholesky factor of calib^T calib / n_calib
+                                     (needs n_calib >= d and a full-rank calibration set)    */
+} dyra_input_aware;
+
+/* Activation applied to the layer's output, Y = act(X W_hat + b + L R), in the output
+ * kernel's epilogue (bf16 layers only). GELU is the erf form x Phi(x) of the ViT / DINOv3 MLP
+ * blocks (summary page Appendix D: every linear layer of those models is replaced). */
+typedef enum dyra_activation {
+  DYRA_ACT_NONE = 0,
+  DYRA_ACT_GELU = 1
+} dyra_activation;
+
 /* Arguments of dyra_prepare / dyra_fit. All pointers are HOST pointers to float64, read
  * only during the call. Zero-initialise the struct and set what you need. */
 typedef struct dyra_prepare_args {
@@ -92,6 +111,10 @@ typedef struct dyra_prepare_args {
   dyra_dtype dtype;
   int device;           /* CUDA device ordinal the layer lives on                        */
   int fit_threads;      /* host threads for the fit, 0 => hardware concurrency           */
+  const double *calib;  /* [n_calib, d] calibration activations (input_aware != NONE)     */
+  int n_calib;
+  dyra_input_aware input_aware; /* ignored when F1/F2 are given                           */
+  dyra_activation activation;   /* applied to Y (bf16 layers); NONE for a plain linear    */
 } dyra_prepare_args;
 
 /* Read-only description of a prepared layer (the shapes and options of dyra_prepare). */
@@ -104,6 +127,7 @@ typedef struct dyra_layer_desc {
   double ridge;
   int device;
   int kernels_per_forward; /* kernel launches one dyra_linear_forward enqueues           */
+  dyra_activation activation;
 } dyra_layer_desc;
 
 typedef struct dyra_layer dyra_layer;   /* opaque; owns its device copies of the factors */
@@ -172,6 +196,20 @@ dyra_status dyra_workspace_size(const dyra_layer *layer, int batch, int n, size_
 dyra_status dyra_linear_forward(const dyra_layer *layer, const void *X, int batch, int n,
                                 void *Y, void *workspace, size_t workspace_bytes,
                                 cudaStream_t stream);
+
+/* A transformer MLP block with both linear layers replaced (summary page Appendix D: the
+ * evaluated ViT / DINOv3 models replace every linear layer; summary page 3.2: end-to-end
+ * latency): H = fc1(X), with fc1's own activation (GELU for an MLP block), then Y = fc2(H),
+ * each layer's correction computed from its own input, both enqueued on `stream`.
+ * X: device [batch, n, fc1.d]; H: device [batch, n, fc1.m], caller-owned, overwritten; Y:
+ * device [batch, n, fc2.m]; all in the layers' dtype (bf16), 16-byte aligned. workspace:
+ * >= max(dyra_workspace_size(fc1), dyra_workspace_size(fc2)) bytes, used by one layer after
+ * the other; its status words (dyra_workspace_status) count both layers. Errors (nothing
+ * launched): INVALID_ARG (fc1.m != fc2.d, different dtype or device, null pointers),
+ * WORKSPACE, CUDA. */
+dyra_status dyra_mlp_forward(const dyra_layer *fc1, const dyra_layer *fc2, const void *X,
+                             int batch, int n, void *H, void *Y, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
 
 /* Same step (same passages as dyra_linear_forward) from HOST buffers: copies X_host -> X_dev, runs the forward, copies Y_dev ->
  * Y_host, all enqueued on `stream` (use page-locked host memory for asynchronous copies;

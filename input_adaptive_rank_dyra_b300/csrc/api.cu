@@ -34,6 +34,7 @@ struct dyra_layer {
   dyra_static_kind kind = DYRA_STATIC_LOWRANK;
   dyra_dtype dtype = DYRA_BF16;
   dyra_solver solver = DYRA_SOLVE_CHOLESKY;
+  dyra_activation activation = DYRA_ACT_NONE;
   int ns_iters = 8;
   double ridge = 0.0;
   int device = 0;
@@ -603,6 +604,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.rows_valid = n;
     p.cols_valid = m;
     p.bias = L->bias_d;
+    p.act = L->activation == DYRA_ACT_GELU ? 1 : 0;
     p.timeouts = status + 1;
     CUtensorMap a0 = a;
     if (use_flat_rows(batch, n)) {
@@ -648,6 +650,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.rows_valid = n;
     p.cols_valid = m;
     p.bias = L->bias_d;
+    p.act = L->activation == DYRA_ACT_GELU ? 1 : 0;
     p.timeouts = status + 1;
     CUtensorMap a0 = a;
     if (flat) {
@@ -662,9 +665,9 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
 }
 
 dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream_t s,
-                     Recorder &rec) {
+                     Recorder &rec, bool clear_status) {
   using namespace dyra;
-  DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
+  if (clear_status) DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
   for (const Step &st : plan.steps) {
     const cudaStream_t ks = s;
     switch (st.kind) {
@@ -698,7 +701,8 @@ dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream
 // ------------------------------------------------------------------------ fp32 path
 
 dyra_status forward_f32(const dyra_layer *L, const float *X, int batch, int n, float *Y,
-                        uint8_t *ws, const WsLayout &w, cudaStream_t s, Recorder &rec) {
+                        uint8_t *ws, const WsLayout &w, cudaStream_t s, Recorder &rec,
+                        bool clear_status) {
   using namespace dyra;
   const int d = L->d, m = L->m, k = L->k, r = L->r, ldT = w.ldT;
   int *status = reinterpret_cast<int *>(ws);
@@ -712,7 +716,7 @@ dyra_status forward_f32(const dyra_layer *L, const float *X, int batch, int n, f
   const float *V = static_cast<const float *>(L->v);
   const float *Wr = static_cast<const float *>(L->wres);
   const long long nT = (long long)n * ldT;
-  DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
+  if (clear_status) DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
   // T = X [U | P]
   DY_TIMED(rec, s, launch_sgemm(batch, n, ldT, d, X, (long long)n * d, d, 1, Wcat, 0, ldT, 1, T,
                                 nT, ldT, 1, false, nullptr, s));
@@ -766,7 +770,8 @@ const char *kernel_name(const dyra_layer *L, int i) {
 }
 
 dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, void *Y,
-                         void *workspace, size_t ws_bytes, cudaStream_t s, Recorder &rec) {
+                         void *workspace, size_t ws_bytes, cudaStream_t s, Recorder &rec,
+                         bool clear_status = true) {
   if (!L) return DYRA_ERR_INVALID_ARG;
   if (batch < 0 || n < 0) return DYRA_ERR_INVALID_ARG;
   if (batch == 0 || n == 0) return DYRA_OK;
@@ -780,7 +785,7 @@ dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, v
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   if (L->dtype == DYRA_F32)
     return forward_f32(L, static_cast<const float *>(X), batch, n, static_cast<float *>(Y), ws, w,
-                       s, rec);
+                       s, rec, clear_status);
   const std::array<uintptr_t, 5> key = {reinterpret_cast<uintptr_t>(X),
                                          reinterpret_cast<uintptr_t>(Y),
                                          reinterpret_cast<uintptr_t>(workspace), (uintptr_t)batch,
@@ -796,7 +801,7 @@ dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, v
     if (L->plans.size() >= 64) L->plans.erase(L->plans.begin());
     L->plans.emplace_back(key, plan);
   }
-  return run_plan(L, *plan, ws, s, rec);
+  return run_plan(L, *plan, ws, s, rec, clear_status);
 }
 
 // ------------------------------------------------------------------------ preparation
@@ -878,7 +883,14 @@ dyra_status validate(const dyra_prepare_args *a, dyra_solver *solver_out, int *n
   if (d <= 0 || m <= 0 || r <= 0 || k < 0) return DYRA_ERR_INVALID_ARG;
   if ((a->F1 == nullptr) != (a->F2 == nullptr)) return DYRA_ERR_INVALID_ARG;
   if (!(a->ridge >= 0.0) || !std::isfinite(a->ridge)) return DYRA_ERR_INVALID_ARG;
+  if (a->input_aware != DYRA_INPUT_AWARE_NONE) {
+    if (a->input_aware != DYRA_INPUT_AWARE_DIAG && a->input_aware != DYRA_INPUT_AWARE_CHOLESKY)
+      return DYRA_ERR_INVALID_ARG;
+    if (a->kind != DYRA_STATIC_LOWRANK || (!a->F1 && (!a->calib || a->n_calib <= 0)))
+      return DYRA_ERR_INVALID_ARG;
+  }
   if (a->dtype != DYRA_F32 && a->dtype != DYRA_BF16) return DYRA_ERR_INVALID_ARG;
+  if (a->activation != DYRA_ACT_NONE && a->activation != DYRA_ACT_GELU) return DYRA_ERR_INVALID_ARG;
   if (a->kind == DYRA_STATIC_LOWRANK) {
     if (k >= std::min(d, m) || r > std::min(d, m)) return DYRA_ERR_INVALID_ARG;
     if (!a->R0 && k + r > std::min(d, m)) return DYRA_ERR_INVALID_ARG;
@@ -896,12 +908,67 @@ dyra_status validate(const dyra_prepare_args *a, dyra_solver *solver_out, int *n
   if (!device_checks) return DYRA_OK;
   if (a->dtype == DYRA_F32) {
     if (r > 64) return DYRA_ERR_UNSUPPORTED;
+    if (a->activation != DYRA_ACT_NONE) return DYRA_ERR_UNSUPPORTED;
     if (a->kind != DYRA_STATIC_LOWRANK) return DYRA_ERR_UNSUPPORTED;
   } else {
     if (r > 256 || r % 8 || d % 8 || m % 8) return DYRA_ERR_UNSUPPORTED;
     if (solver == DYRA_SOLVE_CHOLESKY && r > 64) return DYRA_ERR_UNSUPPORTED;
     if (a->kind == DYRA_STATIC_MONARCH && !dyra::monarch_supported(d, m, k, r))
       return DYRA_ERR_UNSUPPORTED;
+  }
+  return DYRA_OK;
+}
+
+// Input-aware truncated SVD: W_hat = S^-T TSVD_k(S^T W) with S from the calibration rows
+// (diag: channel rms; cholesky: lower Cholesky factor of calib^T calib / n_calib). Stores the
+// factors F1 = S^-T U_k sqrt(S_k), F2 = sqrt(S_k) V_k^T.
+dyra_status fit_input_aware(const dyra_prepare_args *a, const std::vector<double> &W,
+                            dyra_layer *L) {
+  const int d = a->d, m = a->m, k = a->k, N = a->n_calib, th = a->fit_threads;
+  std::vector<double> A(W);   // S^T W
+  std::vector<double> Lc;     // Cholesky factor (cholesky mode)
+  std::vector<double> s;      // channel rms (diag mode)
+  if (a->input_aware == DYRA_INPUT_AWARE_DIAG) {
+    s.assign(d, 0.0);
+    for (int n = 0; n < N; ++n)
+      for (int i = 0; i < d; ++i) s[i] += a->calib[(size_t)n * d + i] * a->calib[(size_t)n * d + i];
+    for (int i = 0; i < d; ++i) {
+      s[i] = std::sqrt(s[i] / N);
+      if (!(s[i] > 0.0)) {
+        g_last_error = "input-aware fit: an input channel is zero on every calibration row";
+        return DYRA_ERR_INVALID_ARG;
+      }
+      for (int j = 0; j < m; ++j) A[(size_t)i * m + j] *= s[i];
+    }
+  } else {
+    Lc.assign((size_t)d * d, 0.0);
+    dyra::fit::gemm(d, d, N, a->calib, true, a->calib, false, Lc.data(), th);   // calib^T calib
+    for (double &x : Lc) x /= N;
+    if (!dyra::fit::cholesky(d, Lc.data())) {
+      g_last_error = "input-aware fit: the calibration covariance is not positive definite";
+      return DYRA_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < d; ++i)   // keep the lower triangle only
+      for (int j = i + 1; j < d; ++j) Lc[(size_t)i * d + j] = 0.0;
+    dyra::fit::gemm(d, m, d, Lc.data(), true, W.data(), false, A.data(), th);   // L^T W
+  }
+  std::vector<double> U((size_t)d * k), S(k), Vt((size_t)k * m);
+  if (k > 0 && !dyra::fit::top_svd(d, m, A.data(), k, U.data(), S.data(), Vt.data(), th)) {
+    g_last_error = "eigen-decomposition did not converge";
+    return DYRA_ERR_INVALID_ARG;
+  }
+  L->F1.assign((size_t)d * k, 0.0);
+  L->F2.assign((size_t)k * m, 0.0);
+  for (int j = 0; j < k; ++j) {
+    const double root = std::sqrt(S[j]);
+    for (int i = 0; i < d; ++i) L->F1[(size_t)i * k + j] = U[(size_t)i * k + j] * root;
+    for (int i = 0; i < m; ++i) L->F2[(size_t)j * m + i] = Vt[(size_t)j * m + i] * root;
+  }
+  if (a->input_aware == DYRA_INPUT_AWARE_DIAG) {
+    for (int i = 0; i < d; ++i)
+      for (int j = 0; j < k; ++j) L->F1[(size_t)i * k + j] /= s[i];
+  } else if (k > 0) {
+    dyra::fit::lower_transpose_solve(d, Lc.data(), L->F1.data(), k);   // S^-T (U_k sqrt(S_k))
   }
   return DYRA_OK;
 }
@@ -917,6 +984,9 @@ dyra_status fit_host(const dyra_prepare_args *a, dyra_layer *L) {
     if (a->F1) {
       L->F1.assign(a->F1, a->F1 + (size_t)d * k);
       L->F2.assign(a->F2, a->F2 + (size_t)k * m);
+    } else if (a->input_aware != DYRA_INPUT_AWARE_NONE) {
+      const dyra_status st = fit_input_aware(a, W, L);
+      if (st != DYRA_OK) return st;
     } else {
       const int cnt = k + (a->R0 ? 0 : r);
       std::vector<double> U((size_t)d * cnt), S(cnt), Vt((size_t)cnt * m);
@@ -980,7 +1050,7 @@ dyra_layer *new_layer(const dyra_prepare_args *a, dyra_solver solver, int ns_ite
   L->d = a->d; L->m = a->m; L->k = a->k; L->r = a->r;
   L->kp = (a->kind == DYRA_STATIC_LOWRANK) ? roundup(a->k, 64) : a->d;
   L->kind = a->kind; L->dtype = a->dtype; L->solver = solver; L->ns_iters = ns_iters;
-  L->ridge = a->ridge; L->device = a->device;
+  L->ridge = a->ridge; L->device = a->device; L->activation = a->activation;
   return L;
 }
 
@@ -1209,6 +1279,7 @@ dyra_status dyra_layer_info(const dyra_layer *L, dyra_layer_desc *out) {
   out->kind = L->kind; out->dtype = L->dtype; out->solver = L->solver;
   out->ns_iters = L->ns_iters; out->ridge = L->ridge; out->device = L->device;
   out->kernels_per_forward = kernels_per_forward(L);
+  out->activation = L->activation;
   return DYRA_OK;
 }
 
@@ -1251,6 +1322,23 @@ dyra_status dyra_linear_forward_profiled(const dyra_layer *L, const void *X, int
   dyra_status st = forward_impl(L, X, batch, n, Y, workspace, workspace_bytes, stream, rec);
   if (recorded) *recorded = rec.count;
   return st;
+}
+
+dyra_status dyra_mlp_forward(const dyra_layer *fc1, const dyra_layer *fc2, const void *X,
+                             int batch, int n, void *H, void *Y, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  if (!fc1 || !fc2 || batch < 0 || n < 0) return DYRA_ERR_INVALID_ARG;
+  if (fc1->m != fc2->d || fc1->dtype != fc2->dtype || fc1->device != fc2->device)
+    return DYRA_ERR_INVALID_ARG;
+  if (batch == 0 || n == 0) return DYRA_OK;
+  if (!X || !H || !Y || !workspace) return DYRA_ERR_INVALID_ARG;
+  const size_t need = std::max(layout_of(fc1, batch, n).total, layout_of(fc2, batch, n).total);
+  if (workspace_bytes < need) return DYRA_ERR_WORKSPACE;
+  Recorder rec;
+  dyra_status st = forward_impl(fc1, X, batch, n, H, workspace, workspace_bytes, stream, rec);
+  if (st != DYRA_OK) return st;
+  // the second layer keeps the status words the first one counted into
+  return forward_impl(fc2, H, batch, n, Y, workspace, workspace_bytes, stream, rec, false);
 }
 
 dyra_status dyra_linear_forward_host(const dyra_layer *L, const void *X_host, int batch, int n,

@@ -273,7 +273,15 @@ bool sym_eig(int n, const double *Ain, double *evals, double *evecs, int threads
   Q.clear();
   Q.shrink_to_fit();
 
-  // Implicit QL with Wilkinson shift on (diag, off).
+  // Implicit QL with Wilkinson shift on (diag, off). An off-diagonal entry is negligible when
+  // it is small against its two diagonal neighbours (relative accuracy for well-separated
+  // eigenvalues) or against the whole tridiagonal matrix (a cluster of eigenvalues near zero,
+  // e.g. the Gram matrix of a rank-deficient residual, has off-diagonal rounding noise of the
+  // size eps * ||T|| that no relative test ever deflates).
+  double tnorm = 0.0;
+  for (int i = 0; i < n; ++i)
+    tnorm = std::max(tnorm, std::fabs(diag[i]) + std::fabs(off[i]) + (i ? std::fabs(off[i - 1]) : 0.0));
+  const double abs_tol = 4e-16 * tnorm;
   const int kQueue = 1 << 16;
   std::vector<int> ridx;
   std::vector<double> rc_, rs_;
@@ -294,7 +302,7 @@ bool sym_eig(int n, const double *Ain, double *evals, double *evecs, int threads
       int mm = l;
       for (; mm < n - 1; ++mm) {
         const double dd = std::fabs(diag[mm]) + std::fabs(diag[mm + 1]);
-        if (std::fabs(off[mm]) <= 1e-16 * dd) break;
+        if (std::fabs(off[mm]) <= 1e-16 * dd || std::fabs(off[mm]) <= abs_tol) break;
       }
       if (mm == l) break;
       if (++iter > 60) {
@@ -412,6 +420,15 @@ void cholesky_solve(int r, const double *L, double *B, int ncols) {
       B[(size_t)i * ncols + col] = t / L[(size_t)i * r + i];
     }
   }
+}
+
+void lower_transpose_solve(int r, const double *L, double *B, int ncols) {
+  for (int col = 0; col < ncols; ++col)
+    for (int i = r - 1; i >= 0; --i) {
+      double t = B[(size_t)i * ncols + col];
+      for (int k = i + 1; k < r; ++k) t -= L[(size_t)k * r + i] * B[(size_t)k * ncols + col];
+      B[(size_t)i * ncols + col] = t / L[(size_t)i * r + i];
+    }
 }
 
 }  // namespace fit

@@ -31,6 +31,8 @@ bool top_svd(int d, int m, const double *W, int count, double *U, double *S, dou
 bool cholesky(int r, double *A);
 // Solve (L L^T) X = B for X, B [r x ncols] row-major, in place.
 void cholesky_solve(int r, const double *L, double *B, int ncols);
+// Solve L^T X = B for X (L lower triangular from cholesky), B [r x ncols] row-major, in place.
+void lower_transpose_solve(int r, const double *L, double *B, int ncols);
 
 }  // namespace fit
 }  // namespace dyra

@@ -8,8 +8,8 @@
 //   * r <= 64 (the Cholesky branch): spd_invert, one CTA per sample, inverts G + lambda I
 //     (padded to R x R, R = 32 or 64, by the identity) in place by symmetric Gauss-Jordan
 //     sweeps without pivoting, whose pivots on an SPD matrix are the squared diagonal of the
-//     Cholesky factor, with the matrix spread over the CTA's registers, and stores G^-1
-//     (fp32 and bf16). spd_apply then forms C~ = G^-1 C in fp32 FMA, one CTA per sample and
+//     Cholesky factor, with the matrix spread over the registers of 1024 threads, and stores
+//     G^-1 (fp32 and bf16). spd_apply then forms C~ = G^-1 C in fp32 FMA, one CTA per sample and
 //     128 columns of C, each thread a 4 x 8 block of the result.
 //   * larger r: Newton-Schulz. ns_prep scales G symmetrically to unit diagonal and starts
 //     from X0 = I / ||G_hat||_inf. The iteration X <- X (2I - G_hat X) runs in residual
@@ -39,86 +39,82 @@ constexpr int kSolveCols = 128;   // columns of C per spd_apply CTA
 // p = a_kk and t_j = a_kj / p,
 //   a_ij -= a_ik t_j  (i, j != k),   a_kj = a_jk = t_j,   a_kk = -1 / p,
 // which keeps the matrix symmetric; after all r pivots it holds -(G + ridge I)^-1. The matrix
-// (padded to R x R by the identity, never swept) is spread over the CTA's registers as 4 x 4
-// blocks, one per thread. Each step reads the pivot row (= column) from shared memory; the
-// owners of the next row publish it after their update, into the other half of a double
-// buffer: one barrier per pivot, r steps. The inverse goes to Ginv32 (fp32, read by
-// spd_apply) and Ginv (bf16).
+// (padded to R x R by the identity, never swept) is spread over 1024 threads, an E x E block
+// each (E = R / 32): a pivot step is a handful of independent instructions per thread, so its
+// latency is a shared-memory load, a reciprocal, two FMAs, a store and the barrier. Each step
+// reads the pivot row (= column) from shared memory; the owners of the next row publish it
+// after their update into the other half of a double buffer: one barrier per pivot. The
+// reciprocal of the pivot is the approximate one (within 2 ulp), far below the rounding of
+// the bf16 result. The inverse goes to Ginv32 (fp32, read by spd_apply) and Ginv (bf16).
+constexpr int kInvThreads = 1024;
+
 template <int R>
-__global__ void __launch_bounds__((R / 4) * (R / 4))
+__global__ void __launch_bounds__(kInvThreads)
     spd_invert_kernel(const float *__restrict__ G, int r, float ridge,
                       float *__restrict__ Ginv32, __nv_bfloat16 *__restrict__ Ginv, int *status) {
-  constexpr int Q = R / 4;   // 4 x 4 blocks per side; one thread per block
+  constexpr int E = R / 32;   // elements per thread per side
   __shared__ __align__(16) float piv[2][R];   // the current pivot row, double-buffered
   const int tid = threadIdx.x, b = blockIdx.x;
-  const int i0 = (tid / Q) * 4, j0 = (tid % Q) * 4;
+  const int i0 = (tid >> 5) * E, j0 = (tid & 31) * E;
   // G comes from the previous kernel of the stream: nothing is read before this wait
   ptx::pdl_wait();
-  float a[4][4];
+  float a[E][E];
   {
     const float *g = G + (size_t)b * r * r;
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < E; ++u)
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
+      for (int v = 0; v < E; ++v) {
         const int i = i0 + u, j = j0 + v;
         a[u][v] = (i < r && j < r) ? g[i * r + j] + (i == j ? ridge : 0.f) : (i == j ? 1.f : 0.f);
       }
   }
-  if (i0 == 0) *reinterpret_cast<float4 *>(&piv[0][j0]) = make_float4(a[0][0], a[0][1], a[0][2], a[0][3]);
+  if (i0 == 0) {
+#pragma unroll
+    for (int v = 0; v < E; ++v) piv[0][j0 + v] = a[0][v];
+  }
   __syncthreads();
   bool bad = false;   // every thread takes the same decision from the same pivots
   for (int k = 0; k < r; ++k) {
     const int cur = k & 1;
     const float pk = piv[cur][k];
     bad = bad || !(pk > 0.f && pk < INFINITY);
-    const float pinv = 1.f / pk;
-    const float4 ri4 = *reinterpret_cast<const float4 *>(&piv[cur][i0]);
-    const float4 rj4 = *reinterpret_cast<const float4 *>(&piv[cur][j0]);
-    const float ri[4] = {ri4.x, ri4.y, ri4.z, ri4.w};
-    const float tj[4] = {rj4.x * pinv, rj4.y * pinv, rj4.z * pinv, rj4.w * pinv};
+    const float pinv = __fdividef(1.f, pk);
+    float ri[E], tj[E];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < E; ++u) ri[u] = piv[cur][i0 + u];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) a[u][v] = fmaf(-ri[u], tj[v], a[u][v]);
-    if (i0 == (k & ~3)) {   // this block row holds pivot row k: a_kj = t_j
+    for (int v = 0; v < E; ++v) tj[v] = piv[cur][j0 + v] * pinv;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (i0 + u == k) {
+    for (int u = 0; u < E; ++u)
 #pragma unroll
-          for (int v = 0; v < 4; ++v) a[u][v] = tj[v];
-        }
-    }
-    if (j0 == (k & ~3)) {   // pivot column k: a_ik = a_ki / p; the pivot itself -1 / p
-#pragma unroll
-      for (int v = 0; v < 4; ++v)
-        if (j0 + v == k) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) a[u][v] = (i0 + u == k) ? -pinv : ri[u] * pinv;
-        }
-    }
+      for (int v = 0; v < E; ++v) {
+        const int i = i0 + u, j = j0 + v;
+        float nv = fmaf(-ri[u], tj[v], a[u][v]);
+        nv = (j == k) ? ri[u] * pinv : nv;
+        nv = (i == k) ? ((j == k) ? -pinv : tj[v]) : nv;
+        a[u][v] = nv;
+      }
     const int kn = k + 1;   // the next pivot row, published after this step's update
-    if (kn < r && i0 == (kn & ~3)) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (i0 + u == kn)
-          *reinterpret_cast<float4 *>(&piv[cur ^ 1][j0]) = make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
-    }
+    for (int u = 0; u < E; ++u)
+      if (i0 + u == kn && kn < r) {
+#pragma unroll
+        for (int v = 0; v < E; ++v) piv[cur ^ 1][j0 + v] = a[u][v];
+      }
     __syncthreads();
   }
-  if (i0 < r && j0 < r) {   // r % 4 == 0: a block is inside r x r or outside it
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const size_t row = (size_t)b * r * r + (size_t)(i0 + u) * r + j0;
-      const float4 o = bad ? make_float4(0.f, 0.f, 0.f, 0.f)
-                           : make_float4(-a[u][0], -a[u][1], -a[u][2], -a[u][3]);
-      *reinterpret_cast<float4 *>(Ginv32 + row) = o;
-      Ginv[row] = __float2bfloat16_rn(o.x);
-      Ginv[row + 1] = __float2bfloat16_rn(o.y);
-      Ginv[row + 2] = __float2bfloat16_rn(o.z);
-      Ginv[row + 3] = __float2bfloat16_rn(o.w);
+  for (int u = 0; u < E; ++u)
+#pragma unroll
+    for (int v = 0; v < E; ++v) {
+      const int i = i0 + u, j = j0 + v;
+      if (i < r && j < r) {
+        const float o = bad ? 0.f : -a[u][v];
+        Ginv32[(size_t)b * r * r + (size_t)i * r + j] = o;
+        Ginv[(size_t)b * r * r + (size_t)i * r + j] = __float2bfloat16_rn(o);
+      }
     }
-  }
   if (tid == 0 && bad) atomicAdd(status, 1);
   // the apply kernel may launch now (it waits for this grid to complete before reading)
   ptx::pdl_launch_dependents();
@@ -349,10 +345,10 @@ cudaError_t launch_spd_invert(const float *G, int batch, int r, float ridge, flo
   if (r <= 0 || r > 64 || r % 4) return cudaErrorInvalidValue;
   if (batch <= 0) return cudaSuccess;
   if (r <= 32)
-    return launch_pdl(spd_invert_kernel<32>, dim3(batch), dim3(64), 0u, s, G, r, ridge, Ginv32,
-                      Ginv, status);
-  return launch_pdl(spd_invert_kernel<64>, dim3(batch), dim3(256), 0u, s, G, r, ridge, Ginv32,
-                    Ginv, status);
+    return launch_pdl(spd_invert_kernel<32>, dim3(batch), dim3(kInvThreads), 0u, s, G, r, ridge,
+                      Ginv32, Ginv, status);
+  return launch_pdl(spd_invert_kernel<64>, dim3(batch), dim3(kInvThreads), 0u, s, G, r, ridge,
+                    Ginv32, Ginv, status);
 }
 
 cudaError_t launch_spd_apply(const float *Ginv32, int batch, int r, const float *Ct, int d,

@@ -14,6 +14,11 @@ namespace {
 
 constexpr uint32_t kStagingPairBytes = 2 * 2048;   // one pair of 32 x 32 bf16 staging tiles
 
+// GELU(x) = x Phi(x) = x (1 + erf(x / sqrt 2)) / 2 (the erf form of the ViT MLP blocks).
+__device__ __forceinline__ float gelu_erf(float x) {
+  return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -489,6 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v[h][4 * j + 3] = __float_as_uint(__uint_as_float(v[h][4 * j + 3]) + bb.w);
                   }
                 }
+              }
+              if (p.act == 1) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    v[h][j] = __float_as_uint(gelu_erf(__uint_as_float(v[h][j])));
               }
               // the pair about to be overwritten has been read by the group that stored it
               if (lane == 0) {

@@ -83,6 +83,7 @@ struct TcGemmParams {
   int epi;
   int tma_store;     // EPI_ROW_BF16 through the output tensor map (needs BN % 32 == 0)
   int epi_bufs;      // staging-tile pairs per epilogue warp (1 or 2; 0: chosen at launch)
+  int act;           // TMA-store epilogue: 0 none, 1 GELU (erf form) after the bias
   int out_batched;   // output map carries the batch coordinate
   void *out;
   long long out_bstride, out_ld;

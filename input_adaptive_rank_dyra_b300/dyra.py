@@ -21,6 +21,8 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "OOM"
 KINDS = {"lowrank": 0, "monarch": 1}
 DTYPES = {"f32": 0, "bf16": 1}
 SOLVERS = {"auto": 0, "cholesky": 1, "newton_schulz": 2}
+INPUT_AWARE = {None: 0, "none": 0, "diag": 1, "cholesky": 2}
+ACTIVATIONS = {None: 0, "none": 0, "gelu": 1}
 BUFFERS = {"T": 0, "C": 1, "G": 2, "GINV": 3, "B": 4, "R": 5, "CS": 6}
 
 _c_double_p = ctypes.POINTER(ctypes.c_double)
@@ -32,7 +34,8 @@ class PrepareArgs(ctypes.Structure):
         ("kind", ctypes.c_int), ("k", ctypes.c_int), ("r", ctypes.c_int), ("R0", _c_double_p),
         ("F1", _c_double_p), ("F2", _c_double_p), ("ridge", ctypes.c_double),
         ("solver", ctypes.c_int), ("ns_iters", ctypes.c_int), ("dtype", ctypes.c_int),
-        ("device", ctypes.c_int), ("fit_threads", ctypes.c_int),
+        ("device", ctypes.c_int), ("fit_threads", ctypes.c_int), ("calib", _c_double_p),
+        ("n_calib", ctypes.c_int), ("input_aware", ctypes.c_int), ("activation", ctypes.c_int),
     ]
 
 
@@ -41,7 +44,7 @@ class LayerDesc(ctypes.Structure):
         ("d", ctypes.c_int), ("m", ctypes.c_int), ("k", ctypes.c_int), ("r", ctypes.c_int),
         ("kind", ctypes.c_int), ("dtype", ctypes.c_int), ("solver", ctypes.c_int),
         ("ns_iters", ctypes.c_int), ("ridge", ctypes.c_double), ("device", ctypes.c_int),
-        ("kernels_per_forward", ctypes.c_int),
+        ("kernels_per_forward", ctypes.c_int), ("activation", ctypes.c_int),
     ]
 
 
@@ -51,6 +54,7 @@ EXPORTED = [
     "dyra_linear_forward_host", "dyra_linear_forward_profiled", "dyra_kernel_name",
     "dyra_workspace_status", "dyra_workspace_tensor", "dyra_status_string", "dyra_last_error",
     "dyra_abi_version", "dyra_linear_forward_static", "dyra_selftest_bounded_wait",
+    "dyra_mlp_forward",
 ]
 
 _lib = None
@@ -101,6 +105,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.dyra_abi_version.argtypes = []
     lib.dyra_linear_forward_static.argtypes = [vp, vp, i, i, vp, vp]
     lib.dyra_selftest_bounded_wait.argtypes = [i, vp, vp]
+    lib.dyra_mlp_forward.argtypes = [vp, vp, vp, i, i, vp, vp, vp, sz, vp]
     for name in EXPORTED:   # raises AttributeError if the library lacks an entry point
         getattr(lib, name)
     if path is None:
@@ -148,6 +153,7 @@ class Layer:
         self.ns_iters = d.ns_iters
         self.device = d.device
         self.kernels_per_forward = d.kernels_per_forward
+        self.activation = {v: k for k, v in ACTIVATIONS.items() if k}[d.activation]
 
     @property
     def handle(self):
@@ -199,24 +205,34 @@ def _factor_arrays(kind, d, m, k):
     return np.zeros((k, d // k, k)), np.zeros((k, k, m // k))
 
 
-def _args(W, b, kind, k, r, R0, F1, F2, ridge, solver, ns_iters, dtype, device, fit_threads):
+def _args(W, b, kind, k, r, R0, F1, F2, ridge, solver, ns_iters, dtype, device, fit_threads,
+          calib=None, input_aware=None, activation=None):
     W = _f64(W)
     d, m = W.shape
     keep = dict(W=W, b=_f64(b, (m,)) if b is not None else None,
-                R0=_f64(R0, (r, m)) if R0 is not None else None, F1=_f64(F1), F2=_f64(F2))
+                R0=_f64(R0, (r, m)) if R0 is not None else None, F1=_f64(F1), F2=_f64(F2),
+                calib=_f64(calib) if calib is not None else None)
+    if keep["calib"] is not None and (keep["calib"].ndim != 2 or keep["calib"].shape[1] != d):
+        raise ValueError(f"calib must be [n_calib, {d}]")
     args = PrepareArgs(W=_ptr(keep["W"]), b=_ptr(keep["b"]), d=d, m=m, kind=KINDS[kind], k=k, r=r,
                        R0=_ptr(keep["R0"]), F1=_ptr(keep["F1"]), F2=_ptr(keep["F2"]),
                        ridge=float(ridge), solver=SOLVERS[solver], ns_iters=ns_iters,
-                       dtype=DTYPES[dtype], device=device, fit_threads=fit_threads)
+                       dtype=DTYPES[dtype], device=device, fit_threads=fit_threads,
+                       calib=_ptr(keep["calib"]),
+                       n_calib=0 if keep["calib"] is None else keep["calib"].shape[0],
+                       input_aware=INPUT_AWARE[input_aware], activation=ACTIVATIONS[activation])
     return args, keep
 
 
 def prepare(W, b=None, kind: str = "lowrank", k: int = 0, r: int = 8, R0=None, F1=None, F2=None,
             ridge: float = 0.0, solver: str = "auto", ns_iters: int = 0, dtype: str = "bf16",
-            device: int = 0, fit_threads: int = 0) -> Layer:
-    """dyra_prepare: offline fit, residual, R0, P and upload (synchronous)."""
+            device: int = 0, fit_threads: int = 0, calib=None, input_aware=None,
+            activation=None) -> Layer:
+    """dyra_prepare: offline fit, residual, R0, P and upload (synchronous). input_aware
+    ("diag" or "cholesky") fits the static branch on the calibration rows `calib` [N, d];
+    activation="gelu" applies GELU to the layer's output."""
     args, keep = _args(W, b, kind, k, r, R0, F1, F2, ridge, solver, ns_iters, dtype, device,
-                       fit_threads)
+                       fit_threads, calib, input_aware, activation)
     h = ctypes.c_void_p()
     _check(load().dyra_prepare(ctypes.byref(args), ctypes.byref(h)), "dyra_prepare")
     del keep
@@ -224,9 +240,10 @@ def prepare(W, b=None, kind: str = "lowrank", k: int = 0, r: int = 8, R0=None, F
 
 
 def fit(W, b=None, kind: str = "lowrank", k: int = 0, r: int = 8, R0=None, F1=None, F2=None,
-        fit_threads: int = 0) -> dict:
+        fit_threads: int = 0, calib=None, input_aware=None) -> dict:
     """dyra_fit: the offline step on the host only; returns float64 arrays."""
-    args, keep = _args(W, b, kind, k, r, R0, F1, F2, 0.0, "auto", 0, "bf16", 0, fit_threads)
+    args, keep = _args(W, b, kind, k, r, R0, F1, F2, 0.0, "auto", 0, "bf16", 0, fit_threads,
+                       calib, input_aware)
     d, m = keep["W"].shape
     out = dict(W_hat=np.zeros((d, m)), W_res=np.zeros((d, m)), P=np.zeros((d, r)),
                R0=np.zeros((r, m)))
@@ -273,6 +290,23 @@ def linear_forward(layer: Layer, X, Y=None, workspace=None, stream=None):
                                     ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                                     _stream_handle(stream))
     _check(st, "dyra_linear_forward")
+    return Y
+
+
+def mlp_forward(fc1: Layer, fc2: Layer, X, H=None, Y=None, workspace=None, stream=None):
+    """dyra_mlp_forward: H = fc1(X) (with fc1's activation), Y = fc2(H)."""
+    import torch
+    H = _check_io(fc1, X, H)
+    Y = _check_io(fc2, H, Y)
+    batch, n = X.shape[0], X.shape[1]
+    if workspace is None:
+        nbytes = max(fc1.workspace_size(batch, n), fc2.workspace_size(batch, n), 256)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=f"cuda:{fc1.device}")
+    st = load().dyra_mlp_forward(fc1.handle, fc2.handle, ctypes.c_void_p(X.data_ptr()), batch, n,
+                                 ctypes.c_void_p(H.data_ptr()), ctypes.c_void_p(Y.data_ptr()),
+                                 ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                 _stream_handle(stream))
+    _check(st, "dyra_mlp_forward")
     return Y
 
 

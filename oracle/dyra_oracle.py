@@ -36,6 +36,9 @@ Readings taken where the pages are silent (the same list is kept with the design
     (a,c) block of W gets its best rank-1 approximation;
   * Newton-Schulz: Jacobi scaling G_hat = D G D with D = diag(G)^-1/2, X0 = I/||G_hat||_inf,
     X_{t+1} = X_t (2I - G_hat X_t), G^-1 ~ D X_T D;
+  * input-aware decomposition, written for this build's row-vector convention y = x W:
+    W_hat = S^-T TSVD_k(S^T W), with S = diag(channel rms) or the lower Cholesky factor of the
+    calibration covariance; R0 and P are then formed from W_res as for the plain fit;
   * one least-squares system per sample over all of its n tokens;
   * a sample whose G is not positive definite (e.g. an all-zero sample with lambda = 0)
     gets R = 0, i.e. its output is the static branch plus the bias.
@@ -46,9 +49,10 @@ import numpy as np
 import scipy.linalg as sla
 
 __all__ = [
-    "tsvd_factors", "lowrank_dense", "monarch_factors", "monarch_dense", "residual",
+    "tsvd_factors", "lowrank_dense", "monarch_factors", "monarch_dense", "input_aware_scaling",
+    "input_aware_factors", "residual",
     "top_right_singular", "projection", "prepare", "newton_schulz_inverse",
-    "solve_right_factor", "forward", "als_factors", "approximation_error",
+    "solve_right_factor", "forward", "als_factors", "gelu", "mlp_forward", "approximation_error",
     "relative_frobenius",
 ]
 
@@ -107,6 +111,36 @@ def monarch_dense(B1: np.ndarray, B2: np.ndarray) -> np.ndarray:
         for c in range(nb):
             pi[a * nb + c, c * nb + a] = 1.0
     return bd1 @ pi @ bd2
+
+
+def input_aware_scaling(X_cal: np.ndarray, mode: str) -> np.ndarray:
+    """The input-side transform S of an input-aware decomposition, from calibration
+    activations X_cal [N, d] ([S] Appendix B: input-aware methods use an activation-based
+    diagonal scaling or a Cholesky factor of the input covariance; [B] structured-methods
+    section: S built from calibration activations).
+      "diag":     S = diag(rms of each input channel over the calibration rows);
+      "cholesky": S = the lower Cholesky factor of the covariance X_cal^T X_cal / N.
+    In the row-vector convention y = x W of this build the output error over the calibration
+    rows is ||X_cal (W - W_hat)||_F, which equals ||S^T (W - W_hat)||_F for the Cholesky
+    factor (X_cal^T X_cal / N = S S^T), up to the factor sqrt(N)."""
+    N = X_cal.shape[0]
+    if mode == "diag":
+        return np.diag(np.sqrt(np.mean(X_cal * X_cal, axis=0)))
+    if mode == "cholesky":
+        return np.linalg.cholesky(X_cal.T @ X_cal / N)
+    raise ValueError(mode)
+
+
+def input_aware_factors(W: np.ndarray, k: int, X_cal: np.ndarray, mode: str):
+    """Input-aware truncated SVD ([S] Appendix B; [B] structured-methods section): write
+    W = S^-T (S^T W), truncate S^T W to rank k by its SVD, and map back, so
+    W_hat = S^-T TSVD_k(S^T W) (the pages' W = (W S) S^-1 with W acting on column vectors).
+    Returned as U = S^-T U_k sqrt(S_k) [d x k] and V = sqrt(S_k) V_k^T [k x m]."""
+    S = input_aware_scaling(X_cal, mode)
+    u, sv, vt = np.linalg.svd(S.T @ W, full_matrices=False)
+    root = np.sqrt(sv[:k])
+    U = np.linalg.solve(S.T, u[:, :k] * root[None, :])
+    return U, root[:, None] * vt[:k]
 
 
 def residual(W: np.ndarray, W_hat: np.ndarray) -> np.ndarray:
@@ -241,6 +275,22 @@ def als_factors(Xs: np.ndarray, W_res: np.ndarray, R0: np.ndarray, t: float,
             G = L.T @ L + ridge * np.eye(r)
             R = np.linalg.solve(G, (L.T @ Xs) @ W_res)
     return L, R
+
+
+def gelu(x: np.ndarray) -> np.ndarray:
+    """GELU(x) = x Phi(x) = x (1 + erf(x / sqrt 2)) / 2, the erf form used by the ViT and DINOv3
+    MLP blocks the pages evaluate ([S] Appendix D, their MLP layers)."""
+    from scipy.special import erf
+    return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+
+
+def mlp_forward(X: np.ndarray, prep1: dict, prep2: dict, ridge: float = 0.0,
+                solver: str = "cholesky", ns_iters: int = 8):
+    """A transformer MLP block with both linear layers replaced by DyRA ([S] Appendix D: every
+    linear layer of the evaluated models is replaced): H = GELU(DyRA_fc1(X)), then
+    Y = DyRA_fc2(H), each layer's correction computed from its own input."""
+    H = gelu(forward(X, prep1, ridge=ridge, solver=solver, ns_iters=ns_iters))
+    return forward(H, prep2, ridge=ridge, solver=solver, ns_iters=ns_iters)
 
 
 # ------------------------------------------------------------------------------------

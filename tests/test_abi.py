@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for name in declared:
         assert hasattr(lib, name), name
     assert set(declared) <= set(D.EXPORTED)
-    assert lib.dyra_abi_version() == 2
+    assert lib.dyra_abi_version() == 3
 
 
 def test_status_strings():
@@ -117,6 +117,45 @@ def test_fit_monarch_matches_oracle():
     scale = np.abs(W).max()
     assert np.abs(f["W_hat"] - p["W_hat"]).max() < 1e-9 * scale
     assert np.abs(f["P"] @ f["R0"] - p["P"] @ p["R0"]).max() < 1e-8 * scale
+
+
+@pytest.mark.parametrize("mode", ["diag", "cholesky"])
+def test_fit_input_aware_matches_oracle(mode):
+    """The library's input-aware static fit (host fp64, its own eigensolver and Cholesky)
+    against the oracle's, on the DINOv3 fc1 weights with calibration rows of the same
+    per-sample-covariance recipe: W_hat, W_res and the projector P R0 agree."""
+    cfg = WL.reduced(WL.get_config("c3_fc1"))
+    W, b = WL.make_weights(cfg)
+    Xc = WL.make_calibration(cfg, 3000)
+    f = D.fit(W, kind="lowrank", k=cfg.k, r=cfg.r, calib=Xc, input_aware=mode)
+    U, V = O.input_aware_factors(W, cfg.k, Xc, mode)
+    p = O.prepare(W, b, "lowrank", cfg.k, cfg.r, factors=(U, V))
+    scale = np.abs(W).max()
+    assert np.abs(f["W_hat"] - p["W_hat"]).max() < 1e-8 * scale
+    assert np.abs(f["P"] @ f["R0"] - p["P"] @ p["R0"]).max() < 1e-7 * scale
+    plain = O.prepare(W, b, "lowrank", cfg.k, cfg.r)
+    # the fit is input-aware: a smaller output error on the calibration rows than plain TSVD
+    assert (np.linalg.norm(Xc @ p["W_res"]) < np.linalg.norm(Xc @ plain["W_res"]))
+
+
+def test_fit_r0_from_rank_deficient_residual():
+    """Static factors given, R0 not: R0 comes from the SVD of W_res, which for a truncated-SVD
+    W_hat has d - k exactly-zero singular values (a cluster of zero eigenvalues in the Gram
+    matrix that the eigensolver must still deflate)."""
+    cfg = WL.get_config("c2")
+    W, b = WL.make_weights(cfg)
+    p = O.prepare(W, b, "lowrank", cfg.k, cfg.r)
+    f = D.fit(W, kind="lowrank", k=cfg.k, r=cfg.r, F1=p["F1"], F2=p["F2"])
+    scale = np.abs(W).max()
+    assert np.abs(f["P"] @ f["R0"] - p["P"] @ p["R0"]).max() < 1e-8 * scale
+
+
+def test_fit_input_aware_rejects_bad_calibration():
+    W = np.random.default_rng(5).standard_normal((16, 24))
+    with pytest.raises(D.DyraError):      # fewer rows than features: covariance singular
+        D.fit(W, kind="lowrank", k=3, r=2, calib=np.ones((4, 16)), input_aware="cholesky")
+    with pytest.raises(D.DyraError):      # no calibration rows
+        D.fit(W, kind="lowrank", k=3, r=2, input_aware="diag")
 
 
 def test_fit_rejects_rank_deficient_r0():

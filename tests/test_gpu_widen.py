@@ -1,0 +1,102 @@
+"""GPU parity of the layer variants beyond the one-step low-rank / Monarch forward, against
+the fp64 oracle through the C ABI (bf16: relative Frobenius error <= 2e-2 and the
+approximation error E within 2% of the oracle's):
+
+* input-aware static decomposition (summary page Appendix B; blog structured-methods
+  section): the static branch is fitted on calibration activations, the online path is the
+  low-rank one;
+* a transformer MLP block (fc1 -> GELU -> fc2) with both linear layers replaced (summary page
+  Appendix D), on the DINOv3 ViT-L/16 shapes.
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as WL
+from gpu_util import BF16_TOL, e_close, rel, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import input_adaptive_rank_dyra_b300 as dy
+    dy.load()
+    yield
+
+
+@functools.lru_cache(maxsize=None)
+def _input_aware_case(mode):
+    cfg = WL.reduced(WL.get_config("c3_fc1"), batch=2)
+    W, b = WL.make_weights(cfg)
+    Xc = WL.make_calibration(cfg, 4000)
+    U, V = O.input_aware_factors(W, cfg.k, Xc, mode)
+    prep = O.prepare(W, b, "lowrank", cfg.k, cfg.r, factors=(U, V))
+    return cfg, W, b, Xc, prep
+
+
+@pytest.mark.parametrize("mode", ["diag", "cholesky"])
+def test_input_aware_layer_matches_oracle(mode):
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    cfg, W, b, Xc, prep = _input_aware_case(mode)
+    X = WL.make_inputs(cfg)
+    # the library's own input-aware fit, from the same calibration rows
+    layer = dy.prepare(W, b, kind="lowrank", k=cfg.k, r=cfg.r, dtype="bf16", device=0,
+                       calib=Xc, input_aware=mode)
+    Y = dy.linear_forward(layer, to_device(X, "bf16"))
+    torch.cuda.synchronize()
+    Yg = to_host(Y)
+    Yo = O.forward(X, prep)
+    assert rel(Yg, Yo) <= BF16_TOL
+    e_gpu = O.approximation_error(Yg, X, W, b)
+    e_or = O.approximation_error(Yo, X, W, b)
+    assert e_close(e_gpu, e_or), f"E gpu {e_gpu:.5f} vs oracle {e_or:.5f}"
+    layer.close()
+
+
+@functools.lru_cache(maxsize=None)
+def _mlp_case():
+    c1, c2 = WL.get_config("c3_fc1"), WL.get_config("c3_fc2")
+    W1, b1 = WL.make_weights(c1)
+    W2, b2 = WL.make_weights(c2)
+    p1 = O.prepare(W1, b1, "lowrank", c1.k, c1.r)
+    p2 = O.prepare(W2, b2, "lowrank", c2.k, c2.r)
+    return c1, c2, W1, b1, W2, b2, p1, p2
+
+
+@pytest.mark.parametrize("batch,n", [(2, 1029), (3, 200)])
+def test_mlp_block_matches_oracle(batch, n):
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    c1, c2, W1, b1, W2, b2, p1, p2 = _mlp_case()
+    cfg = WL.reduced(c1, batch=batch, n=n)
+    X = WL.make_inputs(cfg)
+    fc1 = dy.prepare(W1, b1, kind="lowrank", k=c1.k, r=c1.r, F1=p1["F1"], F2=p1["F2"],
+                     R0=p1["R0"], dtype="bf16", device=0, activation="gelu")
+    fc2 = dy.prepare(W2, b2, kind="lowrank", k=c2.k, r=c2.r, F1=p2["F1"], F2=p2["F2"],
+                     R0=p2["R0"], dtype="bf16", device=0)
+    assert fc1.activation == "gelu" and fc2.activation == "none"
+    Xd = to_device(X, "bf16")
+    ws = torch.empty(max(fc1.workspace_size(batch, n), fc2.workspace_size(batch, n)),
+                     dtype=torch.uint8, device="cuda")
+    Y = dy.mlp_forward(fc1, fc2, Xd, workspace=ws)
+    torch.cuda.synchronize()
+    assert dy.workspace_status(fc2, ws) == (0, 0)
+    Yg = to_host(Y)
+    Yo = O.mlp_forward(X, p1, p2)
+    assert rel(Yg, Yo) <= BF16_TOL
+    # the block's error against the dense block, E = ||Y - Y_dense|| / ||Y_dense - b2||
+    dense = O.gelu(X @ W1 + b1) @ W2 + b2
+    e_gpu = np.linalg.norm(Yg - dense) / np.linalg.norm(dense - b2)
+    e_or = np.linalg.norm(Yo - dense) / np.linalg.norm(dense - b2)
+    assert e_close(e_gpu, e_or), f"E gpu {e_gpu:.5f} vs oracle {e_or:.5f}"
+    # the hidden activation alone: GELU applied in fc1's output epilogue
+    H = dy.linear_forward(fc1, Xd)
+    torch.cuda.synchronize()
+    assert rel(to_host(H), O.gelu(O.forward(X, p1))) <= BF16_TOL

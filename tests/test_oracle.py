@@ -99,6 +99,77 @@ def test_monarch_fit_is_blockwise_optimal():
     assert np.isclose(err, tail, rtol=1e-10)
 
 
+# -------------------------------------------------------------------- input-aware fit
+
+def _correlated_calibration(rng, N, d):
+    """Rows with a strongly anisotropic, correlated covariance."""
+    Q = _orth(rng, d, d)
+    return (rng.standard_normal((N, d)) * np.geomspace(5.0, 0.05, d)[None, :]) @ Q.T
+
+
+def test_input_aware_cholesky_is_optimal_on_calibration_rows():
+    """Appendix B input-aware decomposition with S the Cholesky factor of the calibration
+    covariance: the output error on the calibration rows equals the smallest any rank-k W_hat
+    can reach, the sum of the trailing eigenvalues of W^T X^T X W (Eckart-Young on S^T W),
+    here computed by eigh of that matrix directly; the plain truncated SVD does worse."""
+    rng = _rng(20)
+    d, m, k, N = 16, 24, 5, 200
+    W = rng.standard_normal((d, m))
+    Xc = _correlated_calibration(rng, N, d)
+    U, V = O.input_aware_factors(W, k, Xc, "cholesky")
+    What = U @ V
+    assert np.linalg.matrix_rank(What) == k
+    err = np.linalg.norm(Xc @ (W - What)) ** 2
+    lam = np.sort(np.linalg.eigvalsh(W.T @ (Xc.T @ Xc) @ W))[::-1]
+    assert np.isclose(err, lam[k:].sum(), rtol=1e-9)
+    Up, Vp = O.tsvd_factors(W, k)
+    assert err < np.linalg.norm(Xc @ (W - Up @ Vp)) ** 2
+
+
+def test_input_aware_reduces_to_tsvd_for_isotropic_calibration():
+    """With X^T X = c I (isotropic calibration) both scalings are multiples of the identity,
+    and the input-aware W_hat is the plain truncated SVD."""
+    rng = _rng(21)
+    d, m, k = 12, 20, 4
+    W = rng.standard_normal((d, m))
+    Xc = 3.0 * _orth(rng, 60, d)
+    Up, Vp = O.tsvd_factors(W, k)
+    for mode in ("cholesky", "diag"):
+        U, V = O.input_aware_factors(W, k, Xc, mode)
+        assert np.allclose(U @ V, Up @ Vp, atol=1e-10)
+
+
+def test_input_aware_diag_scaling_weights_channels():
+    """Diagonal mode: S = diag(channel rms). For calibration rows with independent channels
+    of known scales, W_hat is the best rank-k fit of W in the norm weighted by those scales:
+    it equals diag(1/s) TSVD_k(diag(s) W), checked against the weighted problem solved by
+    eigh, and its calibration error is below the plain truncated SVD's."""
+    rng = _rng(22)
+    d, m, k, N = 10, 14, 3, 4000
+    scales = np.geomspace(4.0, 0.1, d)
+    Xc = rng.standard_normal((N, d)) * scales[None, :]
+    W = rng.standard_normal((d, m))
+    U, V = O.input_aware_factors(W, k, Xc, "diag")
+    s = np.sqrt(np.mean(Xc * Xc, axis=0))
+    Ws = s[:, None] * W
+    w, vecs = np.linalg.eigh(Ws @ Ws.T)
+    top = vecs[:, np.argsort(w)[::-1][:k]]
+    assert np.allclose(U @ V, (top @ top.T @ Ws) / s[:, None], atol=1e-10)
+    Up, Vp = O.tsvd_factors(W, k)
+    assert np.linalg.norm(Xc @ (W - U @ V)) < np.linalg.norm(Xc @ (W - Up @ Vp))
+
+
+def test_input_aware_fit_ignores_calibration_scale():
+    """Scaling every calibration row by the same factor leaves W_hat unchanged."""
+    rng = _rng(23)
+    W = rng.standard_normal((12, 16))
+    Xc = _correlated_calibration(rng, 100, 12)
+    for mode in ("cholesky", "diag"):
+        U1, V1 = O.input_aware_factors(W, 4, Xc, mode)
+        U2, V2 = O.input_aware_factors(W, 4, 7.0 * Xc, mode)
+        assert np.allclose(U1 @ V1, U2 @ V2, atol=1e-10)
+
+
 # -------------------------------------------------------------------- residual / R0 / P
 
 def test_residual_split_is_exact():
@@ -284,6 +355,36 @@ def test_newton_schulz_converges_to_inverse():
     B = rng.standard_normal((32, 7))
     R, ok = O.solve_right_factor(G, B, "newton_schulz", 30)
     assert ok and np.allclose(R, np.linalg.solve(G, B), rtol=1e-10, atol=1e-12)
+
+
+# -------------------------------------------------------------------- MLP block
+
+def test_gelu_table_values():
+    """GELU(x) = x Phi(x) at points where the standard normal CDF is tabulated:
+    Phi(1) = 0.8413447460685429, Phi(2) = 0.9772498680518208, Phi(0) = 1/2; and
+    GELU(x) - GELU(-x) = x (Phi(x) + Phi(-x) = 1)."""
+    assert O.gelu(np.array([1.0]))[0] == pytest.approx(0.8413447460685429, rel=1e-14)
+    assert O.gelu(np.array([-1.0]))[0] == pytest.approx(-(1 - 0.8413447460685429), rel=1e-13)
+    assert O.gelu(np.array([2.0]))[0] == pytest.approx(2 * 0.9772498680518208, rel=1e-14)
+    assert O.gelu(np.array([0.0]))[0] == 0.0
+    x = np.linspace(-6, 6, 97)
+    assert np.allclose(O.gelu(x) - O.gelu(-x), x, atol=1e-14)
+    assert np.allclose(O.gelu(np.array([40.0, -40.0])), [40.0, 0.0], atol=1e-12)
+
+
+def test_mlp_block_exact_when_both_residuals_have_rank_at_most_r():
+    """Both layers exact (rank(W_res) <= r, R0 spanning it): the DyRA MLP block equals the
+    dense GELU(X W1 + b1) W2 + b2."""
+    rng = _rng(24)
+    d, hdim, m, k, r = 12, 20, 10, 3, 2
+    W1 = _orth(rng, d, k + r) @ np.diag(np.linspace(4, 1, k + r)) @ _orth(rng, hdim, k + r).T
+    W2 = _orth(rng, hdim, k + r) @ np.diag(np.linspace(3, 1, k + r)) @ _orth(rng, m, k + r).T
+    b1, b2 = rng.standard_normal(hdim), rng.standard_normal(m)
+    X = rng.standard_normal((2, 30, d))
+    p1 = O.prepare(W1, b1, "lowrank", k, r)
+    p2 = O.prepare(W2, b2, "lowrank", k, r)
+    ref = O.gelu(X @ W1 + b1) @ W2 + b2
+    assert np.allclose(O.mlp_forward(X, p1, p2), ref, atol=1e-9)
 
 
 # -------------------------------------------------------------------- metric and workloads

@@ -26,7 +26,7 @@ import numpy as np
 from scipy.linalg import solve_triangular
 
 __all__ = ["LayerConfig", "CONFIGS", "get_config", "make_weights", "make_inputs",
-           "round_to_bf16", "bf16_bits", "reduced"]
+           "make_calibration", "round_to_bf16", "bf16_bits", "reduced"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -201,6 +201,21 @@ def _sample(cfg: LayerConfig, s: int) -> np.ndarray:
     if cfg.x_recipe == "student_t":
         return rng.standard_t(4.0, size=(n, d)) * _channel_scales(cfg)[None, :]
     raise ValueError(cfg.x_recipe)
+
+
+_CALIB_BASE = 1_000_000   # sample indices of calibration draws (disjoint from the workload's)
+
+
+def make_calibration(cfg: LayerConfig, rows: int) -> np.ndarray:
+    """Calibration activations [rows, d] for an input-aware fit: the rows of fresh samples of
+    the same recipe, drawn from streams no workload sample uses (float64; bf16-representable
+    for bf16 layers, like the inputs)."""
+    out, s = [], 0
+    while sum(x.shape[0] for x in out) < rows:
+        out.append(_sample(cfg, _CALIB_BASE + s))
+        s += 1
+    x = np.concatenate(out)[:rows]
+    return round_to_bf16(x) if cfg.dtype == "bf16" else x.astype(np.float32).astype(np.float64)
 
 
 def make_inputs(cfg: LayerConfig, samples: Optional[range] = None) -> np.ndarray:

@@ -39,8 +39,16 @@ import workloads as WL  # noqa: E402
 METRIC = "DyRA layer tokens/s and latency vs dense cuBLAS XW; % bf16 TC peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 L2_BYTES = 126 * 1024 * 1024
-# the workloads timed beside the headline one (each as its own entry of "per_config")
-PER_CONFIG = ["c2", "c3_fc1", "c3_fc2", "c4"]
+# the workloads timed beside the headline one (each as its own entry of "per_config"); "c2_t2"
+# is the ViT-B fc1 layer with two ALS iterations (summary page 3.3 / Figure 9)
+PER_CONFIG = ["c2", "c3_fc1", "c3_fc2", "c4", "c2_t2"]
+
+
+def bench_config(name):
+    import dataclasses
+    if name == "c2_t2":
+        return dataclasses.replace(WL.get_config("c2"), name="c2_vitb16_fc1_als_t2", als_t=2.0)
+    return WL.get_config(name)
 _CSRC = "input_adaptive_rank_dyra_b300/csrc/"
 # the source files that define each kernel of the forward (a recorded DRAM-traffic figure is
 # used only while their hash matches the one recorded with it)
@@ -118,6 +126,12 @@ def kernel_work(cfg, name: str):
         return B * 2.0 * r * r * d, 4 * (B * r * r + B * r * d) + e * B * r * d
     if name == "ginv_c":
         return 2.0 * B * r * r * d, 4 * (B * r * r + B * r * d) + e * B * r * d
+    if name == "als_gram_r":    # H = R R^T
+        return 2.0 * B * r * r * m, e * B * r * m + 4 * B * r * r
+    if name == "als_q":         # Q = W_res R^T, fp32 out
+        return 2.0 * B * d * m * r, e * (d * m + B * r * m) + 4 * B * d * r
+    if name == "als_l_update":  # L = X P_s into T
+        return 2.0 * B * n * d * r, e * (B * n * d + B * r * d + B * n * r)
     if name == "residual_product":
         return 2.0 * B * r * d * m, e * (B * r * d + d * m + B * r * m)
     if name == "fused_output":
@@ -138,7 +152,12 @@ def layer_flops(cfg):
     block-diagonal factors of nb blocks (2 n d nb + 2 n m nb)."""
     B, n, d, m, k, r = cfg.batch, cfg.n, cfg.d, cfg.m, cfg.k, cfg.r
     static = 2.0 * n * (d * k + k * m)
-    dyn = 2.0 * n * d * r + 2.0 * n * r * r + 2.0 * n * r * d + 2.0 * r * d * m + 2.0 * n * r * m
+    r_update = 2.0 * n * r * r + 2.0 * n * r * d + 2.0 * r * d * m
+    dyn = 2.0 * n * d * r + r_update + 2.0 * n * r * m
+    for hs in range(2, int(round(2 * getattr(cfg, "als_t", 1.0)))):
+        # L-update: R R^T, W_res R^T, apply of (R R^T)^-1, X P; R-update as above
+        dyn += (2.0 * r * r * m + 2.0 * d * m * r + 2.0 * r * r * d + 2.0 * n * d * r
+                if hs % 2 == 0 else r_update)
     return B * (static + dyn)
 
 
@@ -305,7 +324,7 @@ def workload_config(cfg):
     return {"workload": cfg.name, "batch": cfg.batch, "n_tokens": cfg.n, "d": cfg.d, "m": cfg.m,
             "static": cfg.kind, "k": cfg.k, "r": cfg.r,
             "solver": cfg.solver if cfg.solver != "auto" else
-            ("cholesky" if cfg.r <= 64 else "newton_schulz"),
+            ("cholesky" if cfg.r <= 64 else "newton_schulz"), "als_t": cfg.als_t,
             "l2": "flushed before every timed step (write of 2x L2)"}
 
 
@@ -493,7 +512,8 @@ def measure_config(cfg, args, dev, world, pk, with_e2e: bool, clocks=None):
     W, b = WL.make_weights(cfg)
     t0 = time.perf_counter()
     layer = dy.prepare(W, b, kind=cfg.kind, k=cfg.k, r=cfg.r, dtype=cfg.dtype,
-                       device=dev.index, solver=cfg.solver, ns_iters=cfg.ns_iters)
+                       device=dev.index, solver=cfg.solver, ns_iters=cfg.ns_iters,
+                       als_t=cfg.als_t)
     prep_s = time.perf_counter() - t0
     X = WL.make_inputs(cfg)
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
@@ -772,7 +792,7 @@ def run_dyra(args, cfg):
     others = []
     if not args.no_per_config:
         for name in PER_CONFIG:
-            c = WL.get_config(name)
+            c = bench_config(name)
             if c.name == cfg.name:
                 continue
             others.append(summarize(measure_config(c, args, dev, world, pk, with_e2e=False),

@@ -115,6 +115,11 @@ typedef struct dyra_prepare_args {
   int n_calib;
   dyra_input_aware input_aware; /* ignored when F1/F2 are given                           */
   dyra_activation activation;   /* applied to Y (bf16 layers); NONE for a plain linear    */
+  double als_t;         /* ALS iterations t of the correction (summary page 3.3 / Figure 9;
+                           blog ablation: t = 1.5 updates L, R, L): 1, 1.5, 2, ... 8 (bf16
+                           layers); 0 => 1, the pages' default one-step form. A further
+                           L-update from R solves P = W_res R^T (R R^T)^-1, L = X P; a further
+                           R-update repeats the one-step R-update from the new L.          */
 } dyra_prepare_args;
 
 /* Read-only description of a prepared layer (the shapes and options of dyra_prepare). */
@@ -128,6 +133,7 @@ typedef struct dyra_layer_desc {
   int device;
   int kernels_per_forward; /* kernel launches one dyra_linear_forward enqueues           */
   dyra_activation activation;
+  double als_t;
 } dyra_layer_desc;
 
 typedef struct dyra_layer dyra_layer;   /* opaque; owns its device copies of the factors */

@@ -36,6 +36,7 @@ struct dyra_layer {
   dyra_solver solver = DYRA_SOLVE_CHOLESKY;
   dyra_activation activation = DYRA_ACT_NONE;
   int ns_iters = 8;
+  int als_half = 2;        // ALS half-steps: 2 t (t = 1: one L-update, one R-update)
   double ridge = 0.0;
   int device = 0;
   std::vector<double> W_hat, W_res, P, R0, F1, F2, bias;
@@ -133,6 +134,7 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
 
 struct Step {
   enum Kind { GEMM, SPD_INVERT, SPD_APPLY, NS_PREP, NS_FUSED, PERMUTE } kind = GEMM;
+  const char *name = nullptr;   // the kernel's name in dyra_kernel_name
   dyra::TcGemmParams p;
   CUtensorMap a0, a1, b0, b1, out;
   CUtensorMap ns_maps[2][3];
@@ -319,6 +321,7 @@ dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, in
     p.timeouts = status + 1;
     Step st = gemm_step(p, a, a, b, b);
     st.out = o;
+    st.name = "monarch_bd1";
     plan.steps.push_back(st);
   }
   // L = X P into T[:, d:d+r]
@@ -355,6 +358,7 @@ dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, in
     }
     Step st = gemm_step(p, a, a, b, b);
     st.out = o;
+    st.name = "xproj_L";
     plan.steps.push_back(st);
   }
   // the stride permutation between the two factors, in place
@@ -365,7 +369,297 @@ dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, in
     st.rows = (long long)batch * n;
     st.ldT = ldT;
     st.nb = nb;
+    st.name = "monarch_permute";
     plan.steps.push_back(st);
+  }
+  return DYRA_OK;
+}
+
+// [C^T ; G] = [X | L]^T L per sample, from the L columns of T (both operands MN-major: the
+// reduction runs over tokens). C^T [batch, d, r] and G [batch, r, r], fp32.
+dyra_status plan_gram_c(const dyra_layer *L, const void *X, int batch, int n,
+                        const __nv_bfloat16 *T, int ldT, float *Ct, float *G, int *status,
+                        Plan &plan) {
+  using namespace dyra;
+  const int d = L->d, r = L->r, kp = L->kp;
+  {
+    CUtensorMap ax, al;
+    DY_MAP(make_map(&ax, X, 2, d, n, batch, d, (long long)n * d, 64));
+    DY_MAP(make_map(&al, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 64));
+    TcGemmParams p = base_params();
+    p.a_split = (int)cdiv(d, 128);
+    p.m_tiles = p.a_split + (int)cdiv(r, 128);
+    p.n_tiles = 1;
+    p.batch = batch;
+    p.BN = roundup(r, 64);
+    p.k_chunks = (int)cdiv(n, 64);
+    p.elem_bytes = 2;
+    p.a_major = 1;
+    p.b_major = 1;
+    p.a_batched0 = p.a_batched1 = 1;
+    p.b_split = p.k_chunks;
+    p.b_batched0 = 1;
+    p.idesc = tc_idesc(2, 1, 1, p.BN);
+    p.epi = EPI_CG;
+    p.out = Ct;                      // C^T [batch, d, r], fp32
+    p.out_bstride = (long long)d * r;
+    p.out_ld = r;
+    p.rows_valid = d;
+    p.cols_valid = r;
+    p.out2 = G;
+    p.out2_bstride = (long long)r * r;
+    p.out2_ld = r;
+    p.rows2_valid = r;
+    p.cols2_valid = r;
+    p.timeouts = status + 1;
+    plan.steps.push_back(gemm_step(p, ax, al, al, al));
+    plan.steps.back().name = "cg_c_gram";
+  }
+  return DYRA_OK;
+}
+
+// Cs = (Gs + lambda I)^-1 Cs_src^T per sample: Gs [batch, r, r] fp32 (consumed), the operand
+// given as its transpose Ct [batch, d, r] fp32, the result bf16 [batch, r, d]; G^-1 also to
+// Ginv (bf16) and G32 (fp32). r <= 64 (Cholesky branch): one CTA per sample inverts G, then
+// a wide kernel applies the inverse; larger r: Newton-Schulz (ns_prep, ns_iterate), then a
+// tf32 GEMM applies the inverse.
+dyra_status plan_solve(const dyra_layer *L, int batch, float *G, float ridge, const float *Ct,
+                       __nv_bfloat16 *Cs, uint8_t *ws, const WsLayout &w, int *status,
+                       Plan &plan) {
+  using namespace dyra;
+  const int d = L->d, r = L->r;
+  __nv_bfloat16 *Ginv = reinterpret_cast<__nv_bfloat16 *>(ws + w.Ginv);
+  float *G32 = reinterpret_cast<float *>(ws + w.G32);
+  if (L->solver == DYRA_SOLVE_CHOLESKY) {
+    Step st;
+    st.kind = Step::SPD_INVERT;
+    st.G = G;
+    st.batch = batch;
+    st.r = r;
+    st.d = d;
+    st.ridge = ridge;
+    st.Ct = Ct;
+    st.Cs = Cs;
+    st.Ginv = Ginv;
+    st.G32 = G32;
+    st.status = status;
+    st.name = "spd_invert";
+    plan.steps.push_back(st);
+    st.kind = Step::SPD_APPLY;
+    st.name = "spd_apply_c";
+    plan.steps.push_back(st);
+  } else {
+    // Newton-Schulz in residual form: EX = [E ; X ; Y] per sample ([3r][r] fp32, Y = I + E,
+    // two buffers used in turn); each iteration forms X' = X Y, E' = E E and Y' = I + E'.
+    float *EXa = reinterpret_cast<float *>(ws + w.EX0);
+    float *EXb = reinterpret_cast<float *>(ws + w.EX1);
+    float *dinv = reinterpret_cast<float *>(ws + w.dinv);
+    int *flags = reinterpret_cast<int *>(ws + w.flags);
+    const long long ex_bs = 3LL * r * r;   // elements between samples of EX
+    {
+      Step st;
+      st.kind = Step::NS_PREP;
+      st.G = G;
+      st.batch = batch;
+      st.r = r;
+      st.ridge = ridge;
+      st.X0 = EXa;
+      st.dinv = dinv;
+      st.flags = flags;
+      st.name = "ns_prep";
+      plan.steps.push_back(st);
+    }
+    {
+      // every iteration and the finish (G^-1 = D X D) in one kernel
+      Step st;
+      st.kind = Step::NS_FUSED;
+      float *bufs[2] = {EXa, EXb};
+      for (int bi = 0; bi < 2; ++bi)
+        for (int blk = 0; blk < 3; ++blk)
+          DY_MAP(make_map(&st.ns_maps[bi][blk], bufs[bi] + (size_t)blk * r * r, 4, r, r, batch, r,
+                          ex_bs, 128));
+      st.X0 = EXa;
+      st.X1 = EXb;
+      st.dinv = dinv;
+      st.batch = batch;
+      st.r = r;
+      st.nb = L->ns_iters;
+      st.flags = flags;
+      st.Ginv = Ginv;
+      st.G32 = G32;
+      st.status = status;
+      st.name = "ns_iterate";
+      plan.steps.push_back(st);
+    }
+    // C~ = G^-1 C as a tf32 GEMM: M = r rows of G^-1 (fp32, K-major), N = d, K = r, with
+    // B = C^T [d, r] (K-major); bf16 result [batch, r, d]
+    {
+      CUtensorMap a, b, o;
+      const int BN = pick_bn((long long)batch * cdiv(r, 128) * 128, d, 32);
+      DY_MAP(make_map(&a, G32, 4, r, r, batch, r, (long long)r * r, 128));
+      DY_MAP(make_map(&b, Ct, 4, r, d, batch, r, (long long)d * r, BN / kBDiv));
+      DY_MAP(make_store_map(&o, Cs, d, r, batch, d, (long long)r * d));
+      TcGemmParams p = base_params();
+      p.m_tiles = (int)cdiv(r, 128);
+      p.n_tiles = (int)cdiv(d, BN);
+      p.batch = batch;
+      p.BN = BN;
+      p.k_chunks = (int)cdiv(r, 32);
+      p.elem_bytes = 4;
+      p.a_split = p.m_tiles;
+      p.a_batched0 = 1;
+      p.b_split = p.k_chunks;
+      p.b_batched0 = 1;
+      p.idesc = p.idesc1 = tc_idesc(4, 0, 0, BN);
+      set_pair(p, 4, 0);
+      p.epi = EPI_ROW_BF16;
+      p.tma_store = 1;
+      p.out_batched = 1;
+      p.rows_valid = r;
+      p.cols_valid = d;
+      p.timeouts = status + 1;
+      Step st = gemm_step(p, a, a, b, b);
+      st.out = o;
+      st.name = "ginv_c";
+      plan.steps.push_back(st);
+    }
+  }
+  return DYRA_OK;
+}
+
+// R = C~ W_res, one [batch * r, d] x [d, m] GEMM, row-major [batch * r, m].
+dyra_status plan_residual(const dyra_layer *L, int batch, const __nv_bfloat16 *Cs,
+                          __nv_bfloat16 *Rm, int *status, Plan &plan) {
+  using namespace dyra;
+  const int d = L->d, m = L->m, r = L->r;
+  {
+    CUtensorMap a, b, o;
+    const long long rows = (long long)batch * r;
+    const int BN = pick_bn(rows, m, 32);
+    DY_MAP(make_map(&a, Cs, 2, d, rows, 1, d, 0, 128));
+    DY_MAP(make_map(&b, L->wres, 2, d, m, 1, d, 0, BN / kBDiv));
+    DY_MAP(make_store_map(&o, Rm, m, rows, 1, m, 0));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(rows, 128);
+    p.n_tiles = (int)cdiv(m, BN);
+    p.batch = 1;
+    p.BN = BN;
+    p.k_chunks = (int)cdiv(d, 64);
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.b_split = p.k_chunks;
+    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    set_pair(p, 2, 0);
+    p.epi = EPI_ROW_BF16;
+    p.tma_store = 1;
+    p.rows_valid = (int)rows;
+    p.cols_valid = m;
+    p.timeouts = status + 1;
+    Step st = gemm_step(p, a, a, b, b);
+    st.out = o;
+    st.name = "residual_product";
+    plan.steps.push_back(st);
+  }
+  return DYRA_OK;
+}
+
+// L-update of ALS with R held fixed (t > 1; blog section "残差乘积的低秩优化目标是什么": with R
+// fixed, L is the least-squares solution, computed by reducing the output dimension to r
+// first): from R [batch, r, m] (bf16),
+//   H = R R^T,   Q = W_res R^T,   P_s^T = H^-1 Q^T,   L = X P_s,
+// the new L written into the L columns of T. H, Q and P_s^T reuse the G, C^T and C~ buffers.
+dyra_status plan_l_update(const dyra_layer *L, const void *X, int batch, int n,
+                          __nv_bfloat16 *T, int ldT, const __nv_bfloat16 *Rm, float *H, float *Q,
+                          __nv_bfloat16 *PsT, uint8_t *ws, const WsLayout &w, int *status,
+                          Plan &plan) {
+  using namespace dyra;
+  const int d = L->d, m = L->m, r = L->r, kp = L->kp;
+  {   // H = R R^T: K = m, both operands rows of R (K-major)
+    CUtensorMap a, b;
+    const int BN = roundup(r, 16);
+    DY_MAP(make_map(&a, Rm, 2, m, r, batch, m, (long long)r * m, 128));
+    DY_MAP(make_map(&b, Rm, 2, m, r, batch, m, (long long)r * m, BN));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(r, 128);
+    p.n_tiles = 1;
+    p.batch = batch;
+    p.BN = BN;
+    p.k_chunks = (int)cdiv(m, 64);
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.a_batched0 = 1;
+    p.b_split = p.k_chunks;
+    p.b_batched0 = 1;
+    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    p.epi = EPI_ROW_F32;
+    p.out = H;
+    p.out_bstride = (long long)r * r;
+    p.out_ld = r;
+    p.rows_valid = r;
+    p.cols_valid = r;
+    p.timeouts = status + 1;
+    plan.steps.push_back(gemm_step(p, a, a, b, b));
+    plan.steps.back().name = "als_gram_r";
+  }
+  {   // Q = W_res R^T [batch, d, r]: A = W_res read MN-major from W_res^T [m, d]
+    CUtensorMap a, b;
+    const int BN = roundup(r, 16);
+    DY_MAP(make_map(&a, L->wres, 2, d, m, 1, d, 0, 64));
+    DY_MAP(make_map(&b, Rm, 2, m, r, batch, m, (long long)r * m, BN));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(d, 128);
+    p.n_tiles = 1;
+    p.batch = batch;
+    p.BN = BN;
+    p.k_chunks = (int)cdiv(m, 64);
+    p.elem_bytes = 2;
+    p.a_major = 1;
+    p.a_split = p.m_tiles;
+    p.b_split = p.k_chunks;
+    p.b_batched0 = 1;
+    p.idesc = p.idesc1 = tc_idesc(2, 1, 0, BN);
+    p.epi = EPI_ROW_F32;
+    p.out = Q;
+    p.out_bstride = (long long)d * r;
+    p.out_ld = r;
+    p.rows_valid = d;
+    p.cols_valid = r;
+    p.timeouts = status + 1;
+    plan.steps.push_back(gemm_step(p, a, a, b, b));
+    plan.steps.back().name = "als_q";
+  }
+  // P_s^T = H^-1 Q^T (no ridge: the L-update is the plain least-squares step)
+  dyra_status st = plan_solve(L, batch, H, 0.f, Q, PsT, ws, w, status, plan);
+  if (st != DYRA_OK) return st;
+  {   // L = X P_s per sample, into T's L columns
+    CUtensorMap a, b, o;
+    const int BN = roundup(r, kPairMma ? 32 : 16);
+    DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
+    DY_MAP(make_map(&b, PsT, 2, d, r, batch, d, (long long)r * d, BN / kBDiv));
+    DY_MAP(make_store_map(&o, T + kp, r, n, batch, ldT, (long long)n * ldT));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(n, 128);
+    p.n_tiles = 1;
+    p.batch = batch;
+    p.BN = BN;
+    p.k_chunks = (int)cdiv(d, 64);
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.a_batched0 = 1;
+    p.b_split = p.k_chunks;
+    p.b_batched0 = 1;
+    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    set_pair(p, 2, 0);
+    p.epi = EPI_ROW_BF16;
+    p.tma_store = 1;
+    p.out_batched = 1;
+    p.rows_valid = n;
+    p.cols_valid = r;
+    p.timeouts = status + 1;
+    Step stp = gemm_step(p, a, a, b, b);
+    stp.out = o;
+    stp.name = "als_l_update";
+    plan.steps.push_back(stp);
   }
   return DYRA_OK;
 }
@@ -378,7 +672,6 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
   __nv_bfloat16 *T = reinterpret_cast<__nv_bfloat16 *>(ws + w.T);
   float *Ct = reinterpret_cast<float *>(ws + w.C);   // C^T [batch, d, r]
   float *G = reinterpret_cast<float *>(ws + w.G);
-  __nv_bfloat16 *Ginv = reinterpret_cast<__nv_bfloat16 *>(ws + w.Ginv);
   __nv_bfloat16 *Cs = reinterpret_cast<__nv_bfloat16 *>(ws + w.Cs);
   __nv_bfloat16 *Rm = reinterpret_cast<__nv_bfloat16 *>(ws + w.R);
 
@@ -414,161 +707,25 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.timeouts = status + 1;
     Step st = gemm_step(p, a, a, b, b);
     st.out = o;
+    st.name = "xproj_static_L";
     plan.steps.push_back(st);
   }
-  // 2. [C^T ; G] = [X | L]^T L   (both operands MN-major: the reduction runs over tokens)
-  {
-    CUtensorMap ax, al;
-    DY_MAP(make_map(&ax, X, 2, d, n, batch, d, (long long)n * d, 64));
-    DY_MAP(make_map(&al, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 64));
-    TcGemmParams p = base_params();
-    p.a_split = (int)cdiv(d, 128);
-    p.m_tiles = p.a_split + (int)cdiv(r, 128);
-    p.n_tiles = 1;
-    p.batch = batch;
-    p.BN = roundup(r, 64);
-    p.k_chunks = (int)cdiv(n, 64);
-    p.elem_bytes = 2;
-    p.a_major = 1;
-    p.b_major = 1;
-    p.a_batched0 = p.a_batched1 = 1;
-    p.b_split = p.k_chunks;
-    p.b_batched0 = 1;
-    p.idesc = tc_idesc(2, 1, 1, p.BN);
-    p.epi = EPI_CG;
-    p.out = Ct;                      // C^T [batch, d, r], fp32
-    p.out_bstride = (long long)d * r;
-    p.out_ld = r;
-    p.rows_valid = d;
-    p.cols_valid = r;
-    p.out2 = G;
-    p.out2_bstride = (long long)r * r;
-    p.out2_ld = r;
-    p.rows2_valid = r;
-    p.cols2_valid = r;
-    p.timeouts = status + 1;
-    plan.steps.push_back(gemm_step(p, ax, al, al, al));
-  }
-  // 3. C~ = (G + lambda I)^-1 C: on the Cholesky branch one CTA per sample inverts G, then
-  //    a wide kernel applies the inverse to C; on the Newton-Schulz branch a chain of small
-  //    kernels and tf32 GEMMs forms G^-1, then a tf32 GEMM applies it.
-  float *G32 = reinterpret_cast<float *>(ws + w.G32);
-  if (L->solver == DYRA_SOLVE_CHOLESKY) {
-    Step st;
-    st.kind = Step::SPD_INVERT;
-    st.G = G;
-    st.batch = batch;
-    st.r = r;
-    st.d = d;
-    st.ridge = (float)L->ridge;
-    st.Ct = Ct;
-    st.Cs = Cs;
-    st.Ginv = Ginv;
-    st.G32 = G32;
-    st.status = status;
-    plan.steps.push_back(st);
-    st.kind = Step::SPD_APPLY;
-    plan.steps.push_back(st);
-  } else {
-    // Newton-Schulz in residual form: EX = [E ; X ; Y] per sample ([3r][r] fp32, Y = I + E,
-    // two buffers used in turn); each iteration forms X' = X Y, E' = E E and Y' = I + E'.
-    float *EXa = reinterpret_cast<float *>(ws + w.EX0);
-    float *EXb = reinterpret_cast<float *>(ws + w.EX1);
-    float *dinv = reinterpret_cast<float *>(ws + w.dinv);
-    int *flags = reinterpret_cast<int *>(ws + w.flags);
-    const long long ex_bs = 3LL * r * r;   // elements between samples of EX
-    {
-      Step st;
-      st.kind = Step::NS_PREP;
-      st.G = G;
-      st.batch = batch;
-      st.r = r;
-      st.ridge = (float)L->ridge;
-      st.X0 = EXa;
-      st.dinv = dinv;
-      st.flags = flags;
-      plan.steps.push_back(st);
+  // 2-4. the R-update: [C^T ; G] = [X | L]^T L, C~ = (G + lambda I)^-1 C, R = C~ W_res
+  dyra_status st2 = plan_gram_c(L, X, batch, n, T, ldT, Ct, G, status, plan);
+  if (st2 == DYRA_OK) st2 = plan_solve(L, batch, G, (float)L->ridge, Ct, Cs, ws, w, status, plan);
+  if (st2 == DYRA_OK) st2 = plan_residual(L, batch, Cs, Rm, status, plan);
+  if (st2 != DYRA_OK) return st2;
+  // further ALS half-steps (t > 1): an L-update from the current R, then (t >= 2) another
+  // R-update from the new L, and so on; the workspace buffers are reused
+  for (int hs = 2; hs < L->als_half; ++hs) {
+    if (hs % 2 == 0)
+      st2 = plan_l_update(L, X, batch, n, T, ldT, Rm, G, Ct, Cs, ws, w, status, plan);
+    else {
+      st2 = plan_gram_c(L, X, batch, n, T, ldT, Ct, G, status, plan);
+      if (st2 == DYRA_OK) st2 = plan_solve(L, batch, G, (float)L->ridge, Ct, Cs, ws, w, status, plan);
+      if (st2 == DYRA_OK) st2 = plan_residual(L, batch, Cs, Rm, status, plan);
     }
-    {
-      // every iteration and the finish (G^-1 = D X D) in one kernel
-      Step st;
-      st.kind = Step::NS_FUSED;
-      float *bufs[2] = {EXa, EXb};
-      for (int bi = 0; bi < 2; ++bi)
-        for (int blk = 0; blk < 3; ++blk)
-          DY_MAP(make_map(&st.ns_maps[bi][blk], bufs[bi] + (size_t)blk * r * r, 4, r, r, batch, r,
-                          ex_bs, 128));
-      st.X0 = EXa;
-      st.X1 = EXb;
-      st.dinv = dinv;
-      st.batch = batch;
-      st.r = r;
-      st.nb = L->ns_iters;
-      st.flags = flags;
-      st.Ginv = Ginv;
-      st.G32 = G32;
-      st.status = status;
-      plan.steps.push_back(st);
-    }
-    // C~ = G^-1 C as a tf32 GEMM: M = r rows of G^-1 (fp32, K-major), N = d, K = r, with
-    // B = C^T [d, r] (K-major); bf16 result [batch, r, d]
-    {
-      CUtensorMap a, b, o;
-      const int BN = pick_bn((long long)batch * cdiv(r, 128) * 128, d, 32);
-      DY_MAP(make_map(&a, G32, 4, r, r, batch, r, (long long)r * r, 128));
-      DY_MAP(make_map(&b, Ct, 4, r, d, batch, r, (long long)d * r, BN / kBDiv));
-      DY_MAP(make_store_map(&o, Cs, d, r, batch, d, (long long)r * d));
-      TcGemmParams p = base_params();
-      p.m_tiles = (int)cdiv(r, 128);
-      p.n_tiles = (int)cdiv(d, BN);
-      p.batch = batch;
-      p.BN = BN;
-      p.k_chunks = (int)cdiv(r, 32);
-      p.elem_bytes = 4;
-      p.a_split = p.m_tiles;
-      p.a_batched0 = 1;
-      p.b_split = p.k_chunks;
-      p.b_batched0 = 1;
-      p.idesc = p.idesc1 = tc_idesc(4, 0, 0, BN);
-      set_pair(p, 4, 0);
-      p.epi = EPI_ROW_BF16;
-      p.tma_store = 1;
-      p.out_batched = 1;
-      p.rows_valid = r;
-      p.cols_valid = d;
-      p.timeouts = status + 1;
-      Step st = gemm_step(p, a, a, b, b);
-      st.out = o;
-      plan.steps.push_back(st);
-    }
-  }
-  // 4. R = C~ W_res, row-major [batch * r, m]
-  {
-    CUtensorMap a, b, o;
-    const long long rows = (long long)batch * r;
-    const int BN = pick_bn(rows, m, 32);
-    DY_MAP(make_map(&a, Cs, 2, d, rows, 1, d, 0, 128));
-    DY_MAP(make_map(&b, L->wres, 2, d, m, 1, d, 0, BN / kBDiv));
-    DY_MAP(make_store_map(&o, Rm, m, rows, 1, m, 0));
-    TcGemmParams p = base_params();
-    p.m_tiles = (int)cdiv(rows, 128);
-    p.n_tiles = (int)cdiv(m, BN);
-    p.batch = 1;
-    p.BN = BN;
-    p.k_chunks = (int)cdiv(d, 64);
-    p.elem_bytes = 2;
-    p.a_split = p.m_tiles;
-    p.b_split = p.k_chunks;
-    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
-    set_pair(p, 2, 0);
-    p.epi = EPI_ROW_BF16;
-    p.tma_store = 1;
-    p.rows_valid = (int)rows;
-    p.cols_valid = m;
-    p.timeouts = status + 1;
-    Step st = gemm_step(p, a, a, b, b);
-    st.out = o;
-    plan.steps.push_back(st);
+    if (st2 != DYRA_OK) return st2;
   }
   // 5. Y = [X U | L] [V ; R] + b: K chunks of V^T (K-major, shared by all samples), then
   //    the sample's R (MN-major, [r, m] with m contiguous). Monarch: the first chunks are
@@ -613,6 +770,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     }
     Step st = gemm_step(p, a0, a, b0, b1);
     st.out = o;
+    st.name = "fused_output";
     plan.steps.push_back(st);
     return DYRA_OK;
   }
@@ -659,6 +817,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     }
     Step st = gemm_step(p, a0, a, b0, b1);
     st.out = o;
+    st.name = "fused_output";
     plan.steps.push_back(st);
   }
   return DYRA_OK;
@@ -742,31 +901,52 @@ dyra_status forward_f32(const dyra_layer *L, const float *X, int batch, int n, f
   return DYRA_OK;
 }
 
-const char *const kNamesChol[] = {"xproj_static_L", "cg_c_gram", "spd_invert", "spd_apply_c",
-                                  "residual_product", "fused_output"};
-const char *const kNamesMonarchFront[] = {"monarch_bd1", "xproj_L", "monarch_permute"};
 const char *const kNamesF32[] = {"f32_xproj", "f32_gram_f64", "f32_c", "f32_b",
                                  "f32_inverse_f64", "f32_apply_inverse", "f32_static_out",
                                  "f32_correction_out"};
 
-int kernels_per_forward(const dyra_layer *L) {
-  if (L->dtype == DYRA_F32) return 8;
-  const int front = L->kind == DYRA_STATIC_MONARCH ? 3 : 1;
-  // Cholesky: invert, apply; Newton-Schulz: prep, fused iterations, apply GEMM
-  return front + (L->solver == DYRA_SOLVE_CHOLESKY ? 5 : 6);
+// The kernels one forward launches, in order (the plan builders push them in this order).
+std::vector<const char *> forward_kernel_names(const dyra_layer *L) {
+  std::vector<const char *> v;
+  if (L->dtype == DYRA_F32) {
+    v.assign(std::begin(kNamesF32), std::end(kNamesF32));
+    return v;
+  }
+  if (L->kind == DYRA_STATIC_MONARCH)
+    v.insert(v.end(), {"monarch_bd1", "xproj_L", "monarch_permute"});
+  else
+    v.push_back("xproj_static_L");
+  auto solve = [&]() {
+    if (L->solver == DYRA_SOLVE_CHOLESKY)
+      v.insert(v.end(), {"spd_invert", "spd_apply_c"});
+    else
+      v.insert(v.end(), {"ns_prep", "ns_iterate", "ginv_c"});
+  };
+  auto r_update = [&]() {
+    v.push_back("cg_c_gram");
+    solve();
+    v.push_back("residual_product");
+  };
+  r_update();
+  for (int hs = 2; hs < L->als_half; ++hs) {
+    if (hs % 2 == 0) {
+      v.insert(v.end(), {"als_gram_r", "als_q"});
+      solve();
+      v.push_back("als_l_update");
+    } else {
+      r_update();
+    }
+  }
+  v.push_back("fused_output");
+  return v;
 }
 
+int kernels_per_forward(const dyra_layer *L) { return (int)forward_kernel_names(L).size(); }
+
 const char *kernel_name(const dyra_layer *L, int i) {
-  if (i < 0 || i >= kernels_per_forward(L)) return nullptr;
-  if (L->dtype == DYRA_F32) return kNamesF32[i];
-  const int front = L->kind == DYRA_STATIC_MONARCH ? 3 : 1;
-  if (i < front) return L->kind == DYRA_STATIC_MONARCH ? kNamesMonarchFront[i] : kNamesChol[0];
-  i -= front - 1;   // now indexes the low-rank list from "cg_c_gram" (= 1) on
-  if (L->solver == DYRA_SOLVE_CHOLESKY) return kNamesChol[i];
-  if (i == 2) return "ns_prep";
-  if (i == 3) return "ns_iterate";
-  if (i == 4) return "ginv_c";
-  return kNamesChol[i < 2 ? i : i - 1];   // cg_c_gram; residual_product, fused_output
+  const std::vector<const char *> v = forward_kernel_names(L);
+  if (i < 0 || i >= (int)v.size()) return nullptr;
+  return v[i];
 }
 
 dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, void *Y,
@@ -798,6 +978,10 @@ dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, v
     plan = std::make_shared<Plan>();
     dyra_status ps = plan_bf16(L, X, batch, n, Y, ws, w, *plan);
     if (ps != DYRA_OK) return ps;
+    if (plan->steps.size() != (size_t)kernels_per_forward(L)) {
+      g_last_error = "internal: the launch plan does not match the kernel list";
+      return DYRA_ERR_INVALID_ARG;
+    }
     if (L->plans.size() >= 64) L->plans.erase(L->plans.begin());
     L->plans.emplace_back(key, plan);
   }
@@ -891,6 +1075,10 @@ dyra_status validate(const dyra_prepare_args *a, dyra_solver *solver_out, int *n
   }
   if (a->dtype != DYRA_F32 && a->dtype != DYRA_BF16) return DYRA_ERR_INVALID_ARG;
   if (a->activation != DYRA_ACT_NONE && a->activation != DYRA_ACT_GELU) return DYRA_ERR_INVALID_ARG;
+  if (a->als_t != 0.0) {   // t in {1, 1.5, 2, ..., 8}
+    const double h = 2.0 * a->als_t;
+    if (!(a->als_t >= 1.0 && a->als_t <= 8.0) || h != std::floor(h)) return DYRA_ERR_INVALID_ARG;
+  }
   if (a->kind == DYRA_STATIC_LOWRANK) {
     if (k >= std::min(d, m) || r > std::min(d, m)) return DYRA_ERR_INVALID_ARG;
     if (!a->R0 && k + r > std::min(d, m)) return DYRA_ERR_INVALID_ARG;
@@ -909,6 +1097,7 @@ dyra_status validate(const dyra_prepare_args *a, dyra_solver *solver_out, int *n
   if (a->dtype == DYRA_F32) {
     if (r > 64) return DYRA_ERR_UNSUPPORTED;
     if (a->activation != DYRA_ACT_NONE) return DYRA_ERR_UNSUPPORTED;
+    if (a->als_t != 0.0 && a->als_t != 1.0) return DYRA_ERR_UNSUPPORTED;
     if (a->kind != DYRA_STATIC_LOWRANK) return DYRA_ERR_UNSUPPORTED;
   } else {
     if (r > 256 || r % 8 || d % 8 || m % 8) return DYRA_ERR_UNSUPPORTED;
@@ -1051,6 +1240,7 @@ dyra_layer *new_layer(const dyra_prepare_args *a, dyra_solver solver, int ns_ite
   L->kp = (a->kind == DYRA_STATIC_LOWRANK) ? roundup(a->k, 64) : a->d;
   L->kind = a->kind; L->dtype = a->dtype; L->solver = solver; L->ns_iters = ns_iters;
   L->ridge = a->ridge; L->device = a->device; L->activation = a->activation;
+  L->als_half = a->als_t > 0.0 ? (int)std::lround(2.0 * a->als_t) : 2;
   return L;
 }
 
@@ -1280,6 +1470,7 @@ dyra_status dyra_layer_info(const dyra_layer *L, dyra_layer_desc *out) {
   out->ns_iters = L->ns_iters; out->ridge = L->ridge; out->device = L->device;
   out->kernels_per_forward = kernels_per_forward(L);
   out->activation = L->activation;
+  out->als_t = 0.5 * L->als_half;
   return DYRA_OK;
 }
 

@@ -6,10 +6,10 @@
 // R = C~ W_res directly and the output GEMM multiplies L itself. The solve then touches r x d values per sample whatever the token
 // count.
 //   * r <= 64 (the Cholesky branch): spd_invert, one CTA per sample, inverts G + lambda I
-//     (padded to R x R, R = 32 or 64, by the identity) in place by symmetric Gauss-Jordan
-//     sweeps without pivoting, whose pivots on an SPD matrix are the squared diagonal of the
-//     Cholesky factor, with the matrix spread over the registers of 1024 threads, and stores
-//     G^-1 (fp32 and bf16). spd_apply then forms C~ = G^-1 C in fp32 FMA, one CTA per sample and
+//     (padded to R x R, R = 32 or 64, by the identity) in place by block sweeps on 4 x 4
+//     pivot blocks -- Gauss-Jordan without pivoting, whose scalar pivots on an SPD matrix are
+//     the squared diagonal of the Cholesky factor -- with the matrix spread over the CTA's
+//     registers, and stores G^-1 (fp32 and bf16). spd_apply then forms C~ = G^-1 C in fp32 FMA, one CTA per sample and
 //     128 columns of C, each thread a 4 x 8 block of the result.
 //   * larger r: Newton-Schulz. ns_prep scales G symmetrically to unit diagonal and starts
 //     from X0 = I / ||G_hat||_inf. The iteration X <- X (2I - G_hat X) runs in residual
@@ -32,89 +32,177 @@ namespace {
 
 constexpr int kSolveCols = 128;   // columns of C per spd_apply CTA
 
-// (G + ridge I)^-1 for one sample by symmetric Gauss-Jordan sweeps without pivoting, one CTA
-// per sample. On an SPD matrix every pivot is a Schur complement's leading entry (the squared
-// diagonal of the Cholesky factor), so no pivoting is needed and a pivot that is not positive
-// and finite marks a matrix that is not positive definite. Sweeping pivot k maps, with
-// p = a_kk and t_j = a_kj / p,
-//   a_ij -= a_ik t_j  (i, j != k),   a_kj = a_jk = t_j,   a_kk = -1 / p,
-// which keeps the matrix symmetric; after all r pivots it holds -(G + ridge I)^-1. The matrix
-// (padded to R x R by the identity, never swept) is spread over 1024 threads, an E x E block
-// each (E = R / 32): a pivot step is a handful of independent instructions per thread, so its
-// latency is a shared-memory load, a reciprocal, two FMAs, a store and the barrier. Each step
-// reads the pivot row (= column) from shared memory; the owners of the next row publish it
-// after their update into the other half of a double buffer: one barrier per pivot. The
-// reciprocal of the pivot is the approximate one (within 2 ulp), far below the rounding of
-// the bf16 result. The inverse goes to Ginv32 (fp32, read by spd_apply) and Ginv (bf16).
-constexpr int kInvThreads = 1024;
+// p = -(m^-1) of an SPD 4 x 4 block by four scalar sweeps; false if a pivot is not positive
+// and finite.
+__device__ __forceinline__ bool sweep4(const float (&m)[4][4], float (&p)[4][4]) {
+  float w[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[i][j] = m[i][j];
+  bool ok = true;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float dk = w[k][k];
+    ok = ok && dk > 0.f && dk < INFINITY;
+    const float di = 1.f / dk;
+    float c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = w[i][k];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[i][j] = fmaf(-c[i] * di, c[j], w[i][j]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[k][i] = c[i] * di;
+      w[i][k] = c[i] * di;
+    }
+    w[k][k] = -di;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) p[i][j] = w[i][j];
+  return ok;
+}
 
+// (G + ridge I)^-1 for one sample by in-place block sweeps on 4 x 4 pivot blocks (block
+// Gauss-Jordan without pivoting; on an SPD matrix the pivot blocks are SPD Schur complements,
+// whose scalar pivots are the squared diagonal of the Cholesky factor), one CTA per sample.
+// With K the pivot block, P = A_KK^-1 and S_i = A_iK P, one block sweep is
+//   A_ij -= S_i A_Kj  (i, j outside K),  A_iK = S_i,  A_Kj = P A_Kj,  A_KK = -P,
+// and after the sweeps over all blocks the matrix holds -(G + ridge I)^-1 (the identity
+// padding up to R x R is never swept). Each of (R/4)^2 threads keeps one 4 x 4 block in
+// registers. The pivot columns of the next step (rows of 4, = its pivot rows by symmetry) and
+// the inverse of its pivot block, which the owner of that block forms after its update, go
+// through double-buffered shared memory: one barrier per step, r / 4 steps. The inverse goes
+// to Ginv32 (fp32, read by spd_apply) and Ginv (bf16).
 template <int R>
-__global__ void __launch_bounds__(kInvThreads)
+__global__ void __launch_bounds__((R / 4) * (R / 4))
     spd_invert_kernel(const float *__restrict__ G, int r, float ridge,
                       float *__restrict__ Ginv32, __nv_bfloat16 *__restrict__ Ginv, int *status) {
-  constexpr int E = R / 32;   // elements per thread per side
-  __shared__ __align__(16) float piv[2][R];   // the current pivot row, double-buffered
+  constexpr int Q = R / 4;   // 4 x 4 blocks per side; one thread per block
+  __shared__ __align__(16) float colbuf[2][R][4];   // the step's pivot columns A_iK
+  __shared__ __align__(16) float pinv[2][4][4];     // P of the step
+  __shared__ int bad_s;
   const int tid = threadIdx.x, b = blockIdx.x;
-  const int i0 = (tid >> 5) * E, j0 = (tid & 31) * E;
+  const int i0 = (tid / Q) * 4, j0 = (tid % Q) * 4;
   // G comes from the previous kernel of the stream: nothing is read before this wait
   ptx::pdl_wait();
-  float a[E][E];
+  float a[4][4];
   {
     const float *g = G + (size_t)b * r * r;
 #pragma unroll
-    for (int u = 0; u < E; ++u)
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
-      for (int v = 0; v < E; ++v) {
+      for (int v = 0; v < 4; ++v) {
         const int i = i0 + u, j = j0 + v;
         a[u][v] = (i < r && j < r) ? g[i * r + j] + (i == j ? ridge : 0.f) : (i == j ? 1.f : 0.f);
       }
   }
-  if (i0 == 0) {
+  if (tid == 0) bad_s = 0;
+  __syncthreads();
+  if (j0 == 0) {
 #pragma unroll
-    for (int v = 0; v < E; ++v) piv[0][j0 + v] = a[0][v];
+    for (int u = 0; u < 4; ++u)
+      *reinterpret_cast<float4 *>(colbuf[0][i0 + u]) = make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
+  }
+  if (tid == 0) {   // owner of the first pivot block
+    float p[4][4];
+    if (!sweep4(a, p)) bad_s = 1;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) pinv[0][u][v] = -p[u][v];
   }
   __syncthreads();
-  bool bad = false;   // every thread takes the same decision from the same pivots
-  for (int k = 0; k < r; ++k) {
-    const int cur = k & 1;
-    const float pk = piv[cur][k];
-    bad = bad || !(pk > 0.f && pk < INFINITY);
-    const float pinv = __fdividef(1.f, pk);
-    float ri[E], tj[E];
+  const int steps = r / 4;
+  for (int kb = 0; kb < steps; ++kb) {
+    const int k0 = kb * 4, cur = kb & 1;
+    {
+      float P[4][4], crow[4][4], ccol[4][4];
 #pragma unroll
-    for (int u = 0; u < E; ++u) ri[u] = piv[cur][i0 + u];
-#pragma unroll
-    for (int v = 0; v < E; ++v) tj[v] = piv[cur][j0 + v] * pinv;
-#pragma unroll
-    for (int u = 0; u < E; ++u)
-#pragma unroll
-      for (int v = 0; v < E; ++v) {
-        const int i = i0 + u, j = j0 + v;
-        float nv = fmaf(-ri[u], tj[v], a[u][v]);
-        nv = (j == k) ? ri[u] * pinv : nv;
-        nv = (i == k) ? ((j == k) ? -pinv : tj[v]) : nv;
-        a[u][v] = nv;
+      for (int u = 0; u < 4; ++u) {
+        const float4 pp = *reinterpret_cast<const float4 *>(pinv[cur][u]);
+        const float4 cr = *reinterpret_cast<const float4 *>(colbuf[cur][i0 + u]);
+        const float4 cc = *reinterpret_cast<const float4 *>(colbuf[cur][j0 + u]);
+        P[u][0] = pp.x; P[u][1] = pp.y; P[u][2] = pp.z; P[u][3] = pp.w;
+        crow[u][0] = cr.x; crow[u][1] = cr.y; crow[u][2] = cr.z; crow[u][3] = cr.w;
+        ccol[u][0] = cc.x; ccol[u][1] = cc.y; ccol[u][2] = cc.z; ccol[u][3] = cc.w;
       }
-    const int kn = k + 1;   // the next pivot row, published after this step's update
+      const bool rowsK = i0 == k0, colsK = j0 == k0;
+      if (rowsK && colsK) {
 #pragma unroll
-    for (int u = 0; u < E; ++u)
-      if (i0 + u == kn && kn < r) {
+        for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int v = 0; v < E; ++v) piv[cur ^ 1][j0 + v] = a[u][v];
+          for (int v = 0; v < 4; ++v) a[u][v] = -P[u][v];
+      } else if (rowsK) {   // A_Kj = P A_Kj = (A_jK P)^T
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float t = 0.f;
+#pragma unroll
+            for (int l = 0; l < 4; ++l) t = fmaf(ccol[v][l], P[l][u], t);
+            a[u][v] = t;
+          }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float S[4];   // S_i = A_iK P
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            float t = 0.f;
+#pragma unroll
+            for (int l = 0; l < 4; ++l) t = fmaf(crow[u][l], P[l][m], t);
+            S[m] = t;
+          }
+          if (colsK) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) a[u][v] = S[v];
+          } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+#pragma unroll
+              for (int m = 0; m < 4; ++m) a[u][v] = fmaf(-S[m], ccol[v][m], a[u][v]);
+          }
+        }
       }
-    __syncthreads();
-  }
+      const int kn = k0 + 4;   // the next pivot block, after this step
+      if (kn < r) {
+        if (j0 == kn) {
 #pragma unroll
-  for (int u = 0; u < E; ++u)
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<float4 *>(colbuf[cur ^ 1][i0 + u]) =
+                make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
+        }
+        if (i0 == kn && j0 == kn) {
+          float p[4][4];
+          if (!sweep4(a, p)) bad_s = 1;
 #pragma unroll
-    for (int v = 0; v < E; ++v) {
-      const int i = i0 + u, j = j0 + v;
-      if (i < r && j < r) {
-        const float o = bad ? 0.f : -a[u][v];
-        Ginv32[(size_t)b * r * r + (size_t)i * r + j] = o;
-        Ginv[(size_t)b * r * r + (size_t)i * r + j] = __float2bfloat16_rn(o);
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) pinv[cur ^ 1][u][v] = -p[u][v];
+        }
       }
     }
+    __syncthreads();
+  }
+  const bool bad = bad_s != 0;
+  if (i0 < r && j0 < r) {   // r % 4 == 0: a block is inside r x r or outside it
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const size_t row = (size_t)b * r * r + (size_t)(i0 + u) * r + j0;
+      const float4 o = bad ? make_float4(0.f, 0.f, 0.f, 0.f)
+                           : make_float4(-a[u][0], -a[u][1], -a[u][2], -a[u][3]);
+      *reinterpret_cast<float4 *>(Ginv32 + row) = o;
+      Ginv[row] = __float2bfloat16_rn(o.x);
+      Ginv[row + 1] = __float2bfloat16_rn(o.y);
+      Ginv[row + 2] = __float2bfloat16_rn(o.z);
+      Ginv[row + 3] = __float2bfloat16_rn(o.w);
+    }
+  }
   if (tid == 0 && bad) atomicAdd(status, 1);
   // the apply kernel may launch now (it waits for this grid to complete before reading)
   ptx::pdl_launch_dependents();
@@ -345,10 +433,10 @@ cudaError_t launch_spd_invert(const float *G, int batch, int r, float ridge, flo
   if (r <= 0 || r > 64 || r % 4) return cudaErrorInvalidValue;
   if (batch <= 0) return cudaSuccess;
   if (r <= 32)
-    return launch_pdl(spd_invert_kernel<32>, dim3(batch), dim3(kInvThreads), 0u, s, G, r, ridge,
-                      Ginv32, Ginv, status);
-  return launch_pdl(spd_invert_kernel<64>, dim3(batch), dim3(kInvThreads), 0u, s, G, r, ridge,
-                    Ginv32, Ginv, status);
+    return launch_pdl(spd_invert_kernel<32>, dim3(batch), dim3(64), 0u, s, G, r, ridge, Ginv32,
+                      Ginv, status);
+  return launch_pdl(spd_invert_kernel<64>, dim3(batch), dim3(256), 0u, s, G, r, ridge, Ginv32,
+                    Ginv, status);
 }
 
 cudaError_t launch_spd_apply(const float *Ginv32, int batch, int r, const float *Ct, int d,

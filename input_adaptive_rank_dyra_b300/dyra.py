@@ -36,6 +36,7 @@ class PrepareArgs(ctypes.Structure):
         ("solver", ctypes.c_int), ("ns_iters", ctypes.c_int), ("dtype", ctypes.c_int),
         ("device", ctypes.c_int), ("fit_threads", ctypes.c_int), ("calib", _c_double_p),
         ("n_calib", ctypes.c_int), ("input_aware", ctypes.c_int), ("activation", ctypes.c_int),
+        ("als_t", ctypes.c_double),
     ]
 
 
@@ -45,6 +46,7 @@ class LayerDesc(ctypes.Structure):
         ("kind", ctypes.c_int), ("dtype", ctypes.c_int), ("solver", ctypes.c_int),
         ("ns_iters", ctypes.c_int), ("ridge", ctypes.c_double), ("device", ctypes.c_int),
         ("kernels_per_forward", ctypes.c_int), ("activation", ctypes.c_int),
+        ("als_t", ctypes.c_double),
     ]
 
 
@@ -154,6 +156,7 @@ class Layer:
         self.device = d.device
         self.kernels_per_forward = d.kernels_per_forward
         self.activation = {v: k for k, v in ACTIVATIONS.items() if k}[d.activation]
+        self.als_t = d.als_t
 
     @property
     def handle(self):
@@ -206,7 +209,7 @@ def _factor_arrays(kind, d, m, k):
 
 
 def _args(W, b, kind, k, r, R0, F1, F2, ridge, solver, ns_iters, dtype, device, fit_threads,
-          calib=None, input_aware=None, activation=None):
+          calib=None, input_aware=None, activation=None, als_t=0.0):
     W = _f64(W)
     d, m = W.shape
     keep = dict(W=W, b=_f64(b, (m,)) if b is not None else None,
@@ -220,19 +223,21 @@ def _args(W, b, kind, k, r, R0, F1, F2, ridge, solver, ns_iters, dtype, device, 
                        dtype=DTYPES[dtype], device=device, fit_threads=fit_threads,
                        calib=_ptr(keep["calib"]),
                        n_calib=0 if keep["calib"] is None else keep["calib"].shape[0],
-                       input_aware=INPUT_AWARE[input_aware], activation=ACTIVATIONS[activation])
+                       input_aware=INPUT_AWARE[input_aware], activation=ACTIVATIONS[activation],
+                       als_t=float(als_t))
     return args, keep
 
 
 def prepare(W, b=None, kind: str = "lowrank", k: int = 0, r: int = 8, R0=None, F1=None, F2=None,
             ridge: float = 0.0, solver: str = "auto", ns_iters: int = 0, dtype: str = "bf16",
             device: int = 0, fit_threads: int = 0, calib=None, input_aware=None,
-            activation=None) -> Layer:
+            activation=None, als_t: float = 0.0) -> Layer:
     """dyra_prepare: offline fit, residual, R0, P and upload (synchronous). input_aware
     ("diag" or "cholesky") fits the static branch on the calibration rows `calib` [N, d];
-    activation="gelu" applies GELU to the layer's output."""
+    activation="gelu" applies GELU to the layer's output; als_t (1, 1.5, 2, ...) sets the
+    number of ALS iterations of the correction."""
     args, keep = _args(W, b, kind, k, r, R0, F1, F2, ridge, solver, ns_iters, dtype, device,
-                       fit_threads, calib, input_aware, activation)
+                       fit_threads, calib, input_aware, activation, als_t)
     h = ctypes.c_void_p()
     _check(load().dyra_prepare(ctypes.byref(args), ctypes.byref(h)), "dyra_prepare")
     del keep

@@ -52,7 +52,8 @@ __all__ = [
     "tsvd_factors", "lowrank_dense", "monarch_factors", "monarch_dense", "input_aware_scaling",
     "input_aware_factors", "residual",
     "top_right_singular", "projection", "prepare", "newton_schulz_inverse",
-    "solve_right_factor", "forward", "als_factors", "gelu", "mlp_forward", "approximation_error",
+    "solve_right_factor", "forward", "als_factors", "forward_als", "gelu", "mlp_forward",
+    "approximation_error",
     "relative_frobenius",
 ]
 
@@ -275,6 +276,35 @@ def als_factors(Xs: np.ndarray, W_res: np.ndarray, R0: np.ndarray, t: float,
             G = L.T @ L + ridge * np.eye(r)
             R = np.linalg.solve(G, (L.T @ Xs) @ W_res)
     return L, R
+
+
+def forward_als(X: np.ndarray, prep: dict, t: float, ridge: float = 0.0,
+                solver: str = "cholesky", ns_iters: int = 8):
+    """DyRA output with t ALS iterations ([S] 3.3 / Figure 9; [B] ablation paragraph: t = 1,
+    1.5, 2, where 1.5 updates L, R, L), per sample, in the rank-r objective's order of
+    operations ([B] rank-r objective section):
+        L-update (R fixed): P = W_res R^T (R R^T)^-1, L = X P   (the first one from R0 is
+                            the offline P)
+        R-update (L fixed): R = (L^T L + ridge I)^-1 (L^T X) W_res
+    alternating for round(2 t) half-steps from R0, then Y_s = X_s W_hat + b + L R. Both
+    solves use `solver` (Cholesky, or the Newton-Schulz mirror). t = 1 is forward()."""
+    W_hat, W_res, b, R0, P0 = prep["W_hat"], prep["W_res"], prep["b"], prep["R0"], prep["P"]
+    r = R0.shape[0]
+    outs = []
+    for s in range(X.shape[0]):
+        Xs = X[s]
+        R, L = R0, None
+        for step in range(int(round(2 * t))):
+            if step == 0:
+                L = Xs @ P0
+            elif step % 2 == 0:
+                Pt, _ = solve_right_factor(R @ R.T, R @ W_res.T, solver, ns_iters)   # P^T
+                L = Xs @ Pt.T
+            else:
+                G = L.T @ L + ridge * np.eye(r)
+                R, _ = solve_right_factor(G, (L.T @ Xs) @ W_res, solver, ns_iters)
+        outs.append(Xs @ W_hat + b[None, :] + L @ R)
+    return np.stack(outs)
 
 
 def gelu(x: np.ndarray) -> np.ndarray:

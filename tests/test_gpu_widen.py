@@ -6,7 +6,9 @@ approximation error E within 2% of the oracle's):
   section): the static branch is fitted on calibration activations, the online path is the
   low-rank one;
 * a transformer MLP block (fc1 -> GELU -> fc2) with both linear layers replaced (summary page
-  Appendix D), on the DINOv3 ViT-L/16 shapes.
+  Appendix D), on the DINOv3 ViT-L/16 shapes;
+* more ALS iterations, t = 1.5 (L, R, L) and t = 2 (summary page 3.3 / Figure 9), on the
+  Cholesky, Newton-Schulz and Monarch paths.
 """
 import functools
 
@@ -100,3 +102,33 @@ def test_mlp_block_matches_oracle(batch, n):
     H = dy.linear_forward(fc1, Xd)
     torch.cuda.synchronize()
     assert rel(to_host(H), O.gelu(O.forward(X, p1))) <= BF16_TOL
+
+
+ALS_CASES = [("c2", 2, None, 1.5), ("c2", 3, 150, 2.0), ("c3_fc1", 2, 300, 2.0),
+             ("c4", 2, 300, 1.5), ("c5", 1, 700, 1.5), ("c2", 2, None, 3.0)]
+
+
+@pytest.mark.parametrize("name,batch,n,t", ALS_CASES)
+def test_als_iterations_match_oracle(name, batch, n, t):
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    from gpu_util import make_layer, weights_and_prep
+    cfg = WL.reduced(WL.get_config(name), batch=batch, n=n)
+    W, b, prep = weights_and_prep(name)
+    X = WL.make_inputs(cfg)
+    layer = make_layer(cfg, prep, W, b, als_t=t)
+    assert layer.als_t == t
+    ws = dy.new_workspace(layer, cfg.batch, cfg.n)
+    Y = dy.linear_forward(layer, to_device(X, "bf16"), workspace=ws)
+    torch.cuda.synchronize()
+    assert dy.workspace_status(layer, ws) == (0, 0)
+    Yg = to_host(Y)
+    solver = "cholesky" if layer.solver == "cholesky" else "newton_schulz"
+    Yo = O.forward_als(X, prep, t, solver=solver, ns_iters=layer.ns_iters)
+    assert rel(Yg, Yo) <= BF16_TOL
+    e_gpu = O.approximation_error(Yg, X, W, b)
+    e_or = O.approximation_error(Yo, X, W, b)
+    assert e_close(e_gpu, e_or), f"E gpu {e_gpu:.5f} vs oracle {e_or:.5f}"
+    # more iterations do not raise the error (ALS is monotone on ||X W_res - L R||)
+    e1 = O.approximation_error(O.forward(X, prep), X, W, b)
+    assert e_gpu <= e1 * 1.002

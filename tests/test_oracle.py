@@ -296,6 +296,31 @@ def test_lr_error_above_eckart_young_bound_and_als_monotone():
     assert errs[-1] <= bound * (1 + 1e-3)
 
 
+def test_als_half_steps_satisfy_their_normal_equations():
+    """E.3 / Figure 9 ALS variants: after t = 1.5 (L, R, L) the last L-update is the
+    least-squares L for the R it used, (X W_res - L R) R^T = 0; after t = 2 the last R-update
+    satisfies L^T (X W_res - L R) = 0; t = 1 reproduces forward()."""
+    W, b, X, k, r = _small_case(seed=25, n=50)
+    prep = O.prepare(W, b, "lowrank", k, r)
+    Xs = X[0]
+    target = Xs @ prep["W_res"]
+    L1, R1 = O.als_factors(Xs, prep["W_res"], prep["R0"], 1)
+    L15, R15 = O.als_factors(Xs, prep["W_res"], prep["R0"], 1.5)
+    assert np.allclose(R15, R1, atol=1e-12)     # t = 1.5 keeps the t = 1 right factor
+    scale = np.linalg.norm(target) * np.linalg.norm(R15)
+    assert np.abs((target - L15 @ R15) @ R15.T).max() < 1e-10 * scale
+    L2, R2 = O.als_factors(Xs, prep["W_res"], prep["R0"], 2)
+    assert np.abs(L2.T @ (target - L2 @ R2)).max() < 1e-10 * np.linalg.norm(L2) * np.linalg.norm(target)
+    assert np.allclose(O.forward_als(X, prep, 1), O.forward(X, prep), atol=1e-10)
+    # forward_als and als_factors are written separately; they agree for every t
+    for t, (Lt, Rt) in ((1.5, (L15, R15)), (2, (L2, R2))):
+        Yt = O.forward_als(X[:1], prep, t)
+        assert np.allclose(Yt[0], Xs @ prep["W_hat"] + b + Lt @ Rt, atol=1e-9)
+    # with the Newton-Schulz solver run to convergence the same result comes out
+    Yns = O.forward_als(X[:1], prep, 2, solver="newton_schulz", ns_iters=40)
+    assert np.allclose(Yns[0], Xs @ prep["W_hat"] + b + L2 @ R2, atol=1e-8)
+
+
 def test_gauge_invariance_of_r0():
     """Rotating or sign-flipping R0's rows leaves L R (hence Y) unchanged."""
     rng = _rng(10)

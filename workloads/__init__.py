@@ -46,6 +46,7 @@ class LayerConfig:
     x_recipe: str       # "geometric" | "outliers" | "covariance" | "student_t"
     solver: str = "auto"
     ns_iters: int = 8
+    als_t: float = 1.0  # ALS iterations of the correction (1: the one-step form)
     stream: int = 0     # distinguishes two layers that share a seed (fc1 / fc2)
 
     @property

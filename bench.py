@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 L2_BYTES = 126 * 1024 * 1024
 # the workloads timed beside the headline one (each as its own entry of "per_config"); "c2_t2"
 # is the ViT-B fc1 layer with two ALS iterations (summary page 3.3 / Figure 9)
-PER_CONFIG = ["c2", "c3_fc1", "c3_fc2", "c4", "c2_t2"]
+PER_CONFIG = ["c2", "c3_fc1", "c3_fc2", "c4", "c6", "c2_t2"]
 
 
 def bench_config(name):
@@ -106,6 +106,15 @@ def kernel_work(cfg, name: str):
     (bf16 = 2 B; G fp32)."""
     B, n, d, m, k, r = cfg.batch, cfg.n, cfg.d, cfg.m, cfg.k, cfg.r
     e = 2
+    if cfg.kind == "blast":     # k = blocks per side, t = middle rank: stage 1 X blockdiag(U)
+        t = cfg.blast_t
+        if name == "blast_stage1":
+            return 2.0 * B * n * d * t, e * (B * n * d + d * t + B * n * k * t)
+        if name == "xproj_L":
+            return 2.0 * B * n * d * r, e * (B * n * d + d * r + B * n * r)
+        if name == "fused_output":
+            return (2.0 * B * n * (k * t + r) * m,
+                    e * (B * n * (k * t + r) + k * t * m + B * r * m + B * n * m) + 4 * m)
     if cfg.kind == "monarch":   # k = number of blocks; Z = X BD1 has nb * nb = d columns
         if name == "monarch_bd1":
             return 2.0 * B * n * d * k, e * (2 * B * n * d + d * k)
@@ -152,6 +161,8 @@ def layer_flops(cfg):
     block-diagonal factors of nb blocks (2 n d nb + 2 n m nb)."""
     B, n, d, m, k, r = cfg.batch, cfg.n, cfg.d, cfg.m, cfg.k, cfg.r
     static = 2.0 * n * (d * k + k * m)
+    if cfg.kind == "blast":   # stage 1 block-diagonal; stages 2-3 as the coupled factor
+        static = 2.0 * n * (d * cfg.blast_t + k * cfg.blast_t * m)
     r_update = 2.0 * n * r * r + 2.0 * n * r * d + 2.0 * r * d * m
     dyn = 2.0 * n * d * r + r_update + 2.0 * n * r * m
     for hs in range(2, int(round(2 * getattr(cfg, "als_t", 1.0)))):
@@ -168,6 +179,8 @@ def layer_bytes(cfg):
         acts = 2 * (B * n * d + B * n * m)
         inter = 2 * (3 * B * n * (d + r) + 2 * B * r * d + 2 * B * r * m) + 4 * B * r * r
         return weights + acts + inter
+    if cfg.kind == "blast":
+        k = k * cfg.blast_t
     weights = 2 * (d * (k + r) + k * m + d * m) + 4 * m
     acts = 2 * (B * n * d + B * n * m)
     inter = 2 * (2 * B * n * (k + r) + 2 * B * r * d + 2 * B * r * m) + 4 * B * r * r
@@ -513,7 +526,7 @@ def measure_config(cfg, args, dev, world, pk, with_e2e: bool, clocks=None):
     t0 = time.perf_counter()
     layer = dy.prepare(W, b, kind=cfg.kind, k=cfg.k, r=cfg.r, dtype=cfg.dtype,
                        device=dev.index, solver=cfg.solver, ns_iters=cfg.ns_iters,
-                       als_t=cfg.als_t)
+                       als_t=cfg.als_t, blast_t=cfg.blast_t)
     prep_s = time.perf_counter() - t0
     X = WL.make_inputs(cfg)
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32

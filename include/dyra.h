@@ -54,7 +54,13 @@ typedef enum dyra_status {
 
 typedef enum dyra_static_kind {
   DYRA_STATIC_LOWRANK = 0,    /* W_hat = U V, U: d x k, V: k x m (truncated SVD)        */
-  DYRA_STATIC_MONARCH = 1     /* W_hat = blockdiag(B1) . stride permutation . blockdiag(B2) */
+  DYRA_STATIC_MONARCH = 1,    /* W_hat = blockdiag(B1) . stride permutation . blockdiag(B2) */
+  DYRA_STATIC_BLAST = 2       /* nb x nb blocks, block (i,j) = U_i S_ij V_j^T: row bases U_i
+                                 [d/nb x t] shared along block row i, column bases V_j
+                                 [m/nb x t] shared along block column j, a t x t middle matrix
+                                 per block (summary page Appendix B; blog structured-methods
+                                 section), fitted by alternating exact minimisations of
+                                 ||W - W_hat||_F from truncated SVDs, 10 sweeps             */
 } dyra_static_kind;
 
 typedef enum dyra_dtype {
@@ -97,14 +103,17 @@ typedef struct dyra_prepare_args {
   dyra_static_kind kind;
   int k;                /* LOWRANK: static rank, 0 <= k < min(d, m).
                            MONARCH: block count nb, d % nb == 0 and m % nb == 0
-                           (W_hat[(a,i),(c,j)] = B1[a][i,c] B2[c][a,j])                  */
+                           (W_hat[(a,i),(c,j)] = B1[a][i,c] B2[c][a,j]).
+                           BLAST: blocks per side nb, d % nb == 0 and m % nb == 0        */
   int r;                /* residual rank, 1 <= r <= 256 (bf16) / 1 <= r <= 64 (f32)      */
   const double *R0;     /* [r, m] fixed initial right factor, full row rank, or NULL for
                            the top-r right singular vectors of W_res                     */
   const double *F1;     /* optional static factors (both or neither):                     */
   const double *F2;     /*   LOWRANK: F1 = U [d, k], F2 = V [k, m]
                              MONARCH: F1 = B1 [nb, d/nb, nb], F2 = B2 [nb, nb, m/nb]
-                           NULL: fitted here (truncated SVD / blockwise rank-1 SVD)       */
+                           BLAST: F1 = U [nb, d/nb, t], F2 = V [nb, m/nb, t] (and F3)
+                           NULL: fitted here (truncated SVD / blockwise rank-1 SVD /
+                           BLAST alternating fit)                                         */
   double ridge;         /* lambda >= 0 added to the diagonal of L^T L (absolute)          */
   dyra_solver solver;
   int ns_iters;         /* Newton-Schulz iterations (0 => 8)                             */
@@ -120,6 +129,9 @@ typedef struct dyra_prepare_args {
                            layers); 0 => 1, the pages' default one-step form. A further
                            L-update from R solves P = W_res R^T (R R^T)^-1, L = X P; a further
                            R-update repeats the one-step R-update from the new L.          */
+  int blast_t;          /* BLAST: rank t of every block's middle matrix, 1 <= t <= min(d,
+                           m) / nb (bf16 kernels: d / nb % 64 == 0, t % 32 == 0, t <= 256) */
+  const double *F3;     /* BLAST with F1/F2 given: middle matrices S [nb, nb, t, t]       */
 } dyra_prepare_args;
 
 /* Read-only description of a prepared layer (the shapes and options of dyra_prepare). */

@@ -39,7 +39,8 @@ struct dyra_layer {
   int als_half = 2;        // ALS half-steps: 2 t (t = 1: one L-update, one R-update)
   double ridge = 0.0;
   int device = 0;
-  std::vector<double> W_hat, W_res, P, R0, F1, F2, bias;
+  std::vector<double> W_hat, W_res, P, R0, F1, F2, F3, bias;
+  int blast_t = 0;
   // device copies. kp = the static columns of T: roundup(k, 64) (low rank) or d (Monarch).
   // bf16 low rank: w1 = [U^T (padded to kp rows); P^T] [kp + r, d], v = V^T [m, kp];
   // bf16 Monarch: w1 = P^T [r, d], bd1 / bd2 = the block-diagonal factors as K-major tiles
@@ -288,11 +289,86 @@ int pick_bn(long long M, int N, int q) {
   return best;
 }
 
+// L = X P (P^T [r, d] is the layer's w1) into T[:, col : col + r], over the flat batch * n
+// rows (X and T are dense row blocks).
+dyra_status plan_l_projection(const dyra_layer *L, const void *X, int batch, int n,
+                              __nv_bfloat16 *T, int ldT, int col, int *status, Plan &plan) {
+  using namespace dyra;
+  const int d = L->d, r = L->r;
+  const long long rows = (long long)batch * n;
+  CUtensorMap a, b, o;
+  const int BN = roundup(r, kPairMma ? 32 : 16);
+  DY_MAP(make_map(&a, X, 2, d, rows, 1, d, 0, 128));
+  DY_MAP(make_map(&b, L->w1, 2, d, r, 1, d, 0, BN / kBDiv));
+  DY_MAP(make_store_map(&o, T + col, r, rows, 1, ldT, 0));
+  TcGemmParams p = base_params();
+  p.m_tiles = (int)cdiv(rows, 128);
+  p.n_tiles = 1;
+  p.batch = 1;
+  p.BN = BN;
+  p.k_chunks = (int)cdiv(d, 64);
+  p.elem_bytes = 2;
+  p.a_split = p.m_tiles;
+  p.b_split = p.k_chunks;
+  p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+  set_pair(p, 2, 0);
+  p.epi = EPI_ROW_BF16;
+  p.tma_store = 1;
+  p.rows_valid = (int)rows;
+  p.cols_valid = r;
+  p.timeouts = status + 1;
+  Step st = gemm_step(p, a, a, b, b);
+  st.out = o;
+  st.name = "xproj_L";
+  plan.steps.push_back(st);
+  return DYRA_OK;
+}
+
+// BLAST static branch, front half ([S] Appendix B; blog structured-methods section): stage 1,
+// Z[:, i t : (i + 1) t] = X[:, i p : (i + 1) p] U_i for every block row i, as one GEMM whose
+// N tile i contracts only with input block i; then L = X P into T[:, kp : kp + r]. The
+// middle matrices and the column bases are folded into the output GEMM's static factor.
+dyra_status plan_blast_front(const dyra_layer *L, const void *X, int batch, int n,
+                             __nv_bfloat16 *T, int ldT, int *status, Plan &plan) {
+  using namespace dyra;
+  const int d = L->d, nb = L->k, t = L->blast_t, pb = d / nb;
+  const long long rows = (long long)batch * n;
+  {
+    CUtensorMap a, b, o;
+    const int BN = t;
+    DY_MAP(make_map(&a, X, 2, d, rows, 1, d, 0, 128));
+    DY_MAP(make_map(&b, L->bd1, 2, pb, (long long)nb * t, 1, pb, 0, BN / kBDiv));
+    DY_MAP(make_store_map(&o, T, (long long)nb * t, rows, 1, ldT, 0));
+    TcGemmParams p = base_params();
+    p.m_tiles = (int)cdiv(rows, 128);
+    p.n_tiles = nb;
+    p.batch = 1;
+    p.BN = BN;
+    p.k_chunks = pb / 64;
+    p.elem_bytes = 2;
+    p.a_split = p.m_tiles;
+    p.a_kdiag = pb;
+    p.b_split = p.k_chunks;
+    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
+    set_pair(p, 2, 0);
+    p.epi = EPI_ROW_BF16;
+    p.tma_store = 1;
+    p.rows_valid = (int)rows;
+    p.cols_valid = nb * t;
+    p.timeouts = status + 1;
+    Step st = gemm_step(p, a, a, b, b);
+    st.out = o;
+    st.name = "blast_stage1";
+    plan.steps.push_back(st);
+  }
+  return plan_l_projection(L, X, batch, n, T, ldT, L->kp, status, plan);
+}
+
 // Monarch static branch, front half: T[:, 0:d] = the permuted X BD1, T[:, d:d+r] = L = X P.
 dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, int n,
                                __nv_bfloat16 *T, int ldT, int *status, Plan &plan) {
   using namespace dyra;
-  const int d = L->d, r = L->r, nb = L->k;
+  const int d = L->d, nb = L->k;
   // Z = X BD1: 256-column tiles, each contracting with its own 256 input columns
   {
     CUtensorMap a, b, o;
@@ -309,7 +385,7 @@ dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, in
     p.elem_bytes = 2;
     p.a_split = p.m_tiles;
     p.a_batched0 = 1;
-    p.a_kdiag = 1;
+    p.a_kdiag = BN;
     p.b_split = p.k_chunks;
     p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
     set_pair(p, 2, 0);
@@ -325,42 +401,8 @@ dyra_status plan_monarch_front(const dyra_layer *L, const void *X, int batch, in
     plan.steps.push_back(st);
   }
   // L = X P into T[:, d:d+r]
-  {
-    CUtensorMap a, b, o;
-    const int BN = roundup(r, kPairMma ? 32 : 16);
-    DY_MAP(make_map(&a, X, 2, d, n, batch, d, (long long)n * d, 128));
-    DY_MAP(make_map(&b, L->w1, 2, d, r, 1, d, 0, BN / kBDiv));
-    TcGemmParams p = base_params();
-    p.m_tiles = (int)cdiv(n, 128);
-    p.n_tiles = 1;
-    p.batch = batch;
-    p.BN = BN;
-    p.k_chunks = (int)cdiv(d, 64);
-    p.elem_bytes = 2;
-    p.a_split = p.m_tiles;
-    p.a_batched0 = 1;
-    p.b_split = p.k_chunks;
-    p.idesc = p.idesc1 = tc_idesc(2, 0, 0, BN);
-    set_pair(p, 2, 0);
-    p.epi = EPI_ROW_BF16;
-    p.rows_valid = n;
-    p.cols_valid = r;
-    p.timeouts = status + 1;
-    if (BN % 32 == 0) {
-      DY_MAP(make_store_map(&o, T + d, r, n, batch, ldT, (long long)n * ldT));
-      p.tma_store = 1;
-      p.out_batched = 1;
-    } else {
-      o = a;
-      p.out = T + d;
-      p.out_bstride = (long long)n * ldT;
-      p.out_ld = ldT;
-    }
-    Step st = gemm_step(p, a, a, b, b);
-    st.out = o;
-    st.name = "xproj_L";
-    plan.steps.push_back(st);
-  }
+  const dyra_status ls = plan_l_projection(L, X, batch, n, T, ldT, d, status, plan);
+  if (ls != DYRA_OK) return ls;
   // the stride permutation between the two factors, in place
   {
     Step st;
@@ -679,6 +721,9 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
   if (L->kind == DYRA_STATIC_MONARCH) {
     const dyra_status fs = plan_monarch_front(L, X, batch, n, T, ldT, status, plan);
     if (fs != DYRA_OK) return fs;
+  } else if (L->kind == DYRA_STATIC_BLAST) {
+    const dyra_status fs = plan_blast_front(L, X, batch, n, T, ldT, status, plan);
+    if (fs != DYRA_OK) return fs;
   } else {
     // X and T are dense [batch * n] row blocks: the static and L columns of every token are
     // independent of its sample, so the GEMM tiles the flat rows (no per-sample tail tiles)
@@ -747,7 +792,7 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     p.elem_bytes = 2;
     p.a_split = p.m_tiles;
     p.a_batched0 = 1;
-    p.a_kdiag = 1;
+    p.a_kdiag = BN;
     p.a_k1 = kp;
     p.b_batched0 = 0;
     p.b_batched1 = 1;
@@ -914,6 +959,8 @@ std::vector<const char *> forward_kernel_names(const dyra_layer *L) {
   }
   if (L->kind == DYRA_STATIC_MONARCH)
     v.insert(v.end(), {"monarch_bd1", "xproj_L", "monarch_permute"});
+  else if (L->kind == DYRA_STATIC_BLAST)
+    v.insert(v.end(), {"blast_stage1", "xproj_L"});
   else
     v.push_back("xproj_static_L");
   auto solve = [&]() {
@@ -1059,6 +1106,95 @@ void monarch_dense(const std::vector<double> &B1, const std::vector<double> &B2,
       }
 }
 
+// BLAST with nb x nb blocks of rank t: U [nb][p][t], V [nb][q][t], S [nb][nb][t][t],
+// block (i, j) = U_i S_ij V_j^T. Fit (alternating exact minimisations of ||W - W_hat||_F with
+// orthonormal bases): U_i, V_j start as the top-t singular vectors of block row i / block
+// column j; each sweep sets U_i to the top-t left singular vectors of [W_i1 V_1 .. W_i,nb V_nb]
+// and then V_j to those of [W_1j^T U_1 .. W_nb,j^T U_nb]; finally S_ij = U_i^T W_ij V_j.
+constexpr int kBlastSweeps = 10;
+
+bool fit_blast(const std::vector<double> &W, int d, int m, int nb, int t, std::vector<double> &U,
+               std::vector<double> &V, std::vector<double> &S, int threads) {
+  const int p = d / nb, q = m / nb;
+  U.assign((size_t)nb * p * t, 0.0);
+  V.assign((size_t)nb * q * t, 0.0);
+  S.assign((size_t)nb * nb * t * t, 0.0);
+  auto block = [&](int i, int j, std::vector<double> &out) {   // W_ij [p x q]
+    out.resize((size_t)p * q);
+    for (int a = 0; a < p; ++a)
+      std::memcpy(&out[(size_t)a * q], &W[(size_t)(i * p + a) * m + (size_t)j * q],
+                  sizeof(double) * q);
+  };
+  std::vector<double> Uo, Sv, Vt, Wij, K, tmp;
+  // left singular vectors of a rows x cols matrix into dst [rows x t]
+  auto left = [&](int rows, int cols, const double *A, double *dst) {
+    Uo.resize((size_t)rows * t);
+    Sv.resize(t);
+    Vt.resize((size_t)t * cols);
+    if (!dyra::fit::top_svd(rows, cols, A, t, Uo.data(), Sv.data(), Vt.data(), threads)) return false;
+    std::copy(Uo.begin(), Uo.end(), dst);
+    return true;
+  };
+  for (int i = 0; i < nb; ++i)
+    if (!left(p, m, &W[(size_t)i * p * m], &U[(size_t)i * p * t])) return false;
+  for (int j = 0; j < nb; ++j) {   // column block j transposed: [q x d]
+    K.resize((size_t)q * d);
+    for (int c = 0; c < q; ++c)
+      for (int a = 0; a < d; ++a) K[(size_t)c * d + a] = W[(size_t)a * m + (size_t)j * q + c];
+    if (!left(q, d, K.data(), &V[(size_t)j * q * t])) return false;
+  }
+  for (int sw = 0; sw < kBlastSweeps; ++sw) {
+    for (int i = 0; i < nb; ++i) {   // K = [W_i1 V_1 .. W_i,nb V_nb], p x (nb t)
+      K.assign((size_t)p * nb * t, 0.0);
+      for (int j = 0; j < nb; ++j) {
+        block(i, j, Wij);
+        tmp.resize((size_t)p * t);
+        dyra::fit::gemm(p, t, q, Wij.data(), false, &V[(size_t)j * q * t], false, tmp.data(), 1);
+        for (int a = 0; a < p; ++a)
+          std::memcpy(&K[(size_t)a * nb * t + (size_t)j * t], &tmp[(size_t)a * t], sizeof(double) * t);
+      }
+      if (!left(p, nb * t, K.data(), &U[(size_t)i * p * t])) return false;
+    }
+    for (int j = 0; j < nb; ++j) {   // K = [W_1j^T U_1 .. W_nb,j^T U_nb], q x (nb t)
+      K.assign((size_t)q * nb * t, 0.0);
+      for (int i = 0; i < nb; ++i) {
+        block(i, j, Wij);
+        tmp.resize((size_t)q * t);
+        dyra::fit::gemm(q, t, p, Wij.data(), true, &U[(size_t)i * p * t], false, tmp.data(), 1);
+        for (int c = 0; c < q; ++c)
+          std::memcpy(&K[(size_t)c * nb * t + (size_t)i * t], &tmp[(size_t)c * t], sizeof(double) * t);
+      }
+      if (!left(q, nb * t, K.data(), &V[(size_t)j * q * t])) return false;
+    }
+  }
+  for (int i = 0; i < nb; ++i)
+    for (int j = 0; j < nb; ++j) {   // S_ij = U_i^T W_ij V_j
+      block(i, j, Wij);
+      tmp.resize((size_t)p * t);
+      dyra::fit::gemm(p, t, q, Wij.data(), false, &V[(size_t)j * q * t], false, tmp.data(), 1);
+      dyra::fit::gemm(t, t, p, &U[(size_t)i * p * t], true, tmp.data(), false,
+                      &S[((size_t)i * nb + j) * t * t], 1);
+    }
+  return true;
+}
+
+void blast_dense(const std::vector<double> &U, const std::vector<double> &V,
+                 const std::vector<double> &S, int d, int m, int nb, int t,
+                 std::vector<double> &Wh) {
+  const int p = d / nb, q = m / nb;
+  Wh.assign((size_t)d * m, 0.0);
+  std::vector<double> US((size_t)p * t), blk((size_t)p * q);
+  for (int i = 0; i < nb; ++i)
+    for (int j = 0; j < nb; ++j) {
+      dyra::fit::gemm(p, t, t, &U[(size_t)i * p * t], false, &S[((size_t)i * nb + j) * t * t],
+                      false, US.data(), 1);
+      dyra::fit::gemm(p, q, t, US.data(), false, &V[(size_t)j * q * t], true, blk.data(), 1);
+      for (int a = 0; a < p; ++a)
+        std::memcpy(&Wh[(size_t)(i * p + a) * m + (size_t)j * q], &blk[(size_t)a * q],
+                    sizeof(double) * q);
+    }
+}
+
 // Argument checks shared by dyra_fit and dyra_prepare.
 dyra_status validate(const dyra_prepare_args *a, dyra_solver *solver_out, int *ns_out,
                      bool device_checks) {
@@ -1085,6 +1221,10 @@ dyra_status validate(const dyra_prepare_args *a, dyra_solver *solver_out, int *n
   } else if (a->kind == DYRA_STATIC_MONARCH) {
     if (k <= 0 || d % k || m % k) return DYRA_ERR_INVALID_ARG;
     if (r > std::min(d, m)) return DYRA_ERR_INVALID_ARG;
+  } else if (a->kind == DYRA_STATIC_BLAST) {
+    if (k <= 0 || d % k || m % k) return DYRA_ERR_INVALID_ARG;
+    if (a->blast_t < 1 || a->blast_t > std::min(d / k, m / k)) return DYRA_ERR_INVALID_ARG;
+    if (r > std::min(d, m) || (a->F1 && !a->F3)) return DYRA_ERR_INVALID_ARG;
   } else {
     return DYRA_ERR_INVALID_ARG;
   }
@@ -1096,6 +1236,7 @@ dyra_status validate(const dyra_prepare_args *a, dyra_solver *solver_out, int *n
   if (!device_checks) return DYRA_OK;
   if (a->dtype == DYRA_F32) {
     if (r > 64) return DYRA_ERR_UNSUPPORTED;
+    if (a->kind == DYRA_STATIC_BLAST) return DYRA_ERR_UNSUPPORTED;
     if (a->activation != DYRA_ACT_NONE) return DYRA_ERR_UNSUPPORTED;
     if (a->als_t != 0.0 && a->als_t != 1.0) return DYRA_ERR_UNSUPPORTED;
     if (a->kind != DYRA_STATIC_LOWRANK) return DYRA_ERR_UNSUPPORTED;
@@ -1103,6 +1244,9 @@ dyra_status validate(const dyra_prepare_args *a, dyra_solver *solver_out, int *n
     if (r > 256 || r % 8 || d % 8 || m % 8) return DYRA_ERR_UNSUPPORTED;
     if (solver == DYRA_SOLVE_CHOLESKY && r > 64) return DYRA_ERR_UNSUPPORTED;
     if (a->kind == DYRA_STATIC_MONARCH && !dyra::monarch_supported(d, m, k, r))
+      return DYRA_ERR_UNSUPPORTED;
+    if (a->kind == DYRA_STATIC_BLAST &&
+        ((d / k) % 64 || a->blast_t % 32 || a->blast_t > 256))
       return DYRA_ERR_UNSUPPORTED;
   }
   return DYRA_OK;
@@ -1196,6 +1340,17 @@ dyra_status fit_host(const dyra_prepare_args *a, dyra_layer *L) {
     }
     L->W_hat.assign((size_t)d * m, 0.0);
     if (k > 0) dyra::fit::gemm(d, m, k, L->F1.data(), false, L->F2.data(), false, L->W_hat.data(), th);
+  } else if (a->kind == DYRA_STATIC_BLAST) {
+    const int nb = k, t = a->blast_t;
+    if (a->F1) {
+      L->F1.assign(a->F1, a->F1 + (size_t)d * t);
+      L->F2.assign(a->F2, a->F2 + (size_t)m * t);
+      L->F3.assign(a->F3, a->F3 + (size_t)nb * nb * t * t);
+    } else if (!fit_blast(W, d, m, nb, t, L->F1, L->F2, L->F3, th)) {
+      g_last_error = "eigen-decomposition did not converge";
+      return DYRA_ERR_INVALID_ARG;
+    }
+    blast_dense(L->F1, L->F2, L->F3, d, m, nb, t, L->W_hat);
   } else {
     const int nb = k;
     if (a->F1) {
@@ -1237,7 +1392,9 @@ dyra_layer *new_layer(const dyra_prepare_args *a, dyra_solver solver, int ns_ite
   dyra_layer *L = new (std::nothrow) dyra_layer();
   if (!L) return nullptr;
   L->d = a->d; L->m = a->m; L->k = a->k; L->r = a->r;
-  L->kp = (a->kind == DYRA_STATIC_LOWRANK) ? roundup(a->k, 64) : a->d;
+  L->kp = (a->kind == DYRA_STATIC_LOWRANK) ? roundup(a->k, 64)
+          : (a->kind == DYRA_STATIC_BLAST) ? roundup(a->k * a->blast_t, 64) : a->d;
+  L->blast_t = a->kind == DYRA_STATIC_BLAST ? a->blast_t : 0;
   L->kind = a->kind; L->dtype = a->dtype; L->solver = solver; L->ns_iters = ns_iters;
   L->ridge = a->ridge; L->device = a->device; L->activation = a->activation;
   L->als_half = a->als_t > 0.0 ? (int)std::lround(2.0 * a->als_t) : 2;
@@ -1278,6 +1435,41 @@ dyra_status upload_layer(const dyra_prepare_args *a, dyra_layer *L) {
     if (st == DYRA_OK) st = upload(&L->bd1, h);
     to_bf16(b2.data(), b2.size(), h);
     if (st == DYRA_OK) st = upload(&L->bd2, h);
+    to_bf16(wrt.data(), wrt.size(), h);
+    if (st == DYRA_OK) st = upload(&L->wres, h);
+  } else if (a->dtype == DYRA_BF16 && L->kind == DYRA_STATIC_BLAST) {
+    // w1 = P^T [r, d]; bd1 = the stage-1 factor [nb t, p]: row i t + x is column x of U_i;
+    // v = the output GEMM's static factor [m, kp]: v[j q + c][i t + x] = (S_ij V_j^T)[x][c]
+    const int nb = k, t = L->blast_t, pb = d / nb, qb = m / nb, kp = L->kp;
+    std::vector<double> pt((size_t)r * d), b1((size_t)nb * t * pb), vt((size_t)m * kp, 0.0),
+        wrt((size_t)m * d);
+    for (int j = 0; j < r; ++j)
+      for (int i = 0; i < d; ++i) pt[(size_t)j * d + i] = L->P[(size_t)i * r + j];
+    for (int i = 0; i < nb; ++i)
+      for (int x = 0; x < t; ++x)
+        for (int a_ = 0; a_ < pb; ++a_)
+          b1[((size_t)i * t + x) * pb + a_] = L->F1[((size_t)i * pb + a_) * t + x];
+    for (int i = 0; i < nb; ++i)
+      for (int j = 0; j < nb; ++j) {
+        const double *S = &L->F3[((size_t)i * nb + j) * t * t];
+        for (int c = 0; c < qb; ++c) {
+          const double *vr = &L->F2[((size_t)j * qb + c) * t];
+          for (int x = 0; x < t; ++x) {
+            double acc = 0.0;
+            for (int y = 0; y < t; ++y) acc += S[(size_t)x * t + y] * vr[y];
+            vt[((size_t)j * qb + c) * kp + (size_t)i * t + x] = acc;
+          }
+        }
+      }
+    for (int i = 0; i < d; ++i)
+      for (int j = 0; j < m; ++j) wrt[(size_t)j * d + i] = L->W_res[(size_t)i * m + j];
+    std::vector<__nv_bfloat16> h;
+    to_bf16(pt.data(), pt.size(), h);
+    if (st == DYRA_OK) st = upload(&L->w1, h);
+    to_bf16(b1.data(), b1.size(), h);
+    if (st == DYRA_OK) st = upload(&L->bd1, h);
+    to_bf16(vt.data(), vt.size(), h);
+    if (st == DYRA_OK) st = upload(&L->v, h);
     to_bf16(wrt.data(), wrt.size(), h);
     if (st == DYRA_OK) st = upload(&L->wres, h);
   } else if (a->dtype == DYRA_BF16) {

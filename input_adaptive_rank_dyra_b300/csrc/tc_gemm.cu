@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = phantom ? p.a_split * 128 : (a_second ? tc.m_tile - p.a_split : tc.m_tile) * 128;
         const CUtensorMap *ma = a_second ? &tmA1 : &tmA0;
         const int a_b = (a_second ? p.a_batched1 : p.a_batched0) ? tc.bz : 0;
-        const int a_k0 = p.a_kdiag ? tc.n_tile * p.BN : 0;
+        const int a_k0 = p.a_kdiag > 0 ? tc.n_tile * p.a_kdiag : 0;
         const int a_k1 = p.a_k1 >= 0 ? p.a_k1 : p.b_split * chunk;
         int s_lo;
         const int kct = tile_chunks(p, tc, crank, s_lo);

@@ -60,9 +60,9 @@ struct TcGemmParams {
   int b_split;       // k chunks >= b_split load from map B1 (K coordinate restarts at 0)
   int b_batched0, b_batched1;
   int b_major1;      // major of the chunks read from map B1
-  int a_kdiag;       // 1: K-major A chunks < b_split are read at K = n0 + kc * chunk, where n0
-                     // is the tile's first output column (block-diagonal B: an N tile only
-                     // contracts with the same range of K)
+  int a_kdiag;       // > 0: K-major A chunks < b_split are read at K = n_tile * a_kdiag +
+                     // kc * chunk (block-diagonal B: N tile j only contracts with its own
+                     // a_kdiag-wide range of K; Monarch: a_kdiag = BN)
   int a_k1;          // K coordinate of A (elements) read by chunk b_split; later chunks follow
                      // it. < 0: contiguous with the chunks before (b_split * chunk)
   int seg_n;         // > 0: flat M over `seg_count` segments (samples) of seg_n rows each.

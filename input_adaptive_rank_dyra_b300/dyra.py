@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libdyra_b300.so")
 DYRA_OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "OOM", 5: "NOT_SPD",
                 6: "TIMEOUT", 7: "WORKSPACE", 8: "NO_DEVICE"}
-KINDS = {"lowrank": 0, "monarch": 1}
+KINDS = {"lowrank": 0, "monarch": 1, "blast": 2}
 DTYPES = {"f32": 0, "bf16": 1}
 SOLVERS = {"auto": 0, "cholesky": 1, "newton_schulz": 2}
 INPUT_AWARE = {None: 0, "none": 0, "diag": 1, "cholesky": 2}
@@ -36,7 +36,7 @@ class PrepareArgs(ctypes.Structure):
         ("solver", ctypes.c_int), ("ns_iters", ctypes.c_int), ("dtype", ctypes.c_int),
         ("device", ctypes.c_int), ("fit_threads", ctypes.c_int), ("calib", _c_double_p),
         ("n_calib", ctypes.c_int), ("input_aware", ctypes.c_int), ("activation", ctypes.c_int),
-        ("als_t", ctypes.c_double),
+        ("als_t", ctypes.c_double), ("blast_t", ctypes.c_int), ("F3", _c_double_p),
     ]
 
 
@@ -202,18 +202,21 @@ class Layer:
                 for i in range(self.kernels_per_forward)]
 
 
-def _factor_arrays(kind, d, m, k):
+def _factor_arrays(kind, d, m, k, blast_t=0):
     if kind == "lowrank":
         return np.zeros((d, k)), np.zeros((k, m))
+    if kind == "blast":
+        return np.zeros((k, d // k, blast_t)), np.zeros((k, m // k, blast_t))
     return np.zeros((k, d // k, k)), np.zeros((k, k, m // k))
 
 
 def _args(W, b, kind, k, r, R0, F1, F2, ridge, solver, ns_iters, dtype, device, fit_threads,
-          calib=None, input_aware=None, activation=None, als_t=0.0):
+          calib=None, input_aware=None, activation=None, als_t=0.0, blast_t=0, F3=None):
     W = _f64(W)
     d, m = W.shape
     keep = dict(W=W, b=_f64(b, (m,)) if b is not None else None,
                 R0=_f64(R0, (r, m)) if R0 is not None else None, F1=_f64(F1), F2=_f64(F2),
+                F3=_f64(F3),
                 calib=_f64(calib) if calib is not None else None)
     if keep["calib"] is not None and (keep["calib"].ndim != 2 or keep["calib"].shape[1] != d):
         raise ValueError(f"calib must be [n_calib, {d}]")
@@ -224,20 +227,21 @@ def _args(W, b, kind, k, r, R0, F1, F2, ridge, solver, ns_iters, dtype, device, 
                        calib=_ptr(keep["calib"]),
                        n_calib=0 if keep["calib"] is None else keep["calib"].shape[0],
                        input_aware=INPUT_AWARE[input_aware], activation=ACTIVATIONS[activation],
-                       als_t=float(als_t))
+                       als_t=float(als_t), blast_t=int(blast_t), F3=_ptr(keep["F3"]))
     return args, keep
 
 
 def prepare(W, b=None, kind: str = "lowrank", k: int = 0, r: int = 8, R0=None, F1=None, F2=None,
             ridge: float = 0.0, solver: str = "auto", ns_iters: int = 0, dtype: str = "bf16",
             device: int = 0, fit_threads: int = 0, calib=None, input_aware=None,
-            activation=None, als_t: float = 0.0) -> Layer:
+            activation=None, als_t: float = 0.0, blast_t: int = 0, F3=None) -> Layer:
     """dyra_prepare: offline fit, residual, R0, P and upload (synchronous). input_aware
     ("diag" or "cholesky") fits the static branch on the calibration rows `calib` [N, d];
     activation="gelu" applies GELU to the layer's output; als_t (1, 1.5, 2, ...) sets the
-    number of ALS iterations of the correction."""
+    number of ALS iterations of the correction; kind="blast" takes k = blocks per side,
+    blast_t = the rank of every block's middle matrix and (optionally) F1/F2/F3 = U/V/S."""
     args, keep = _args(W, b, kind, k, r, R0, F1, F2, ridge, solver, ns_iters, dtype, device,
-                       fit_threads, calib, input_aware, activation, als_t)
+                       fit_threads, calib, input_aware, activation, als_t, blast_t, F3)
     h = ctypes.c_void_p()
     _check(load().dyra_prepare(ctypes.byref(args), ctypes.byref(h)), "dyra_prepare")
     del keep
@@ -245,14 +249,14 @@ def prepare(W, b=None, kind: str = "lowrank", k: int = 0, r: int = 8, R0=None, F
 
 
 def fit(W, b=None, kind: str = "lowrank", k: int = 0, r: int = 8, R0=None, F1=None, F2=None,
-        fit_threads: int = 0, calib=None, input_aware=None) -> dict:
+        fit_threads: int = 0, calib=None, input_aware=None, blast_t: int = 0, F3=None) -> dict:
     """dyra_fit: the offline step on the host only; returns float64 arrays."""
     args, keep = _args(W, b, kind, k, r, R0, F1, F2, 0.0, "auto", 0, "bf16", 0, fit_threads,
-                       calib, input_aware)
+                       calib, input_aware, None, 0.0, blast_t, F3)
     d, m = keep["W"].shape
     out = dict(W_hat=np.zeros((d, m)), W_res=np.zeros((d, m)), P=np.zeros((d, r)),
                R0=np.zeros((r, m)))
-    out["F1"], out["F2"] = _factor_arrays(kind, d, m, k)
+    out["F1"], out["F2"] = _factor_arrays(kind, d, m, k, blast_t)
     st = load().dyra_fit(ctypes.byref(args), *[out[key].ctypes.data for key in
                                                 ("W_hat", "W_res", "P", "R0", "F1", "F2")])
     _check(st, "dyra_fit")

@@ -34,6 +34,10 @@ Readings taken where the pages are silent (the same list is kept with the design
     V = sqrt(S_k) V_k^T (Y does not depend on the split);
   * Monarch with nb blocks: W_hat[(a,i),(c,j)] = B1[a][i,c] * B2[c][a,j]; each
     (a,c) block of W gets its best rank-1 approximation;
+  * BLAST with nb x nb blocks of rank t: block (i,j) = U[i] S[i,j] V[j]^T with a t x t middle
+    matrix per block (the pages' "small middle matrix"), fitted by alternating exact
+    minimisations from per-block-row and per-block-column truncated SVDs, a fixed number of
+    sweeps;
   * Newton-Schulz: Jacobi scaling G_hat = D G D with D = diag(G)^-1/2, X0 = I/||G_hat||_inf,
     X_{t+1} = X_t (2I - G_hat X_t), G^-1 ~ D X_T D;
   * input-aware decomposition, written for this build's row-vector convention y = x W:
@@ -49,7 +53,8 @@ import numpy as np
 import scipy.linalg as sla
 
 __all__ = [
-    "tsvd_factors", "lowrank_dense", "monarch_factors", "monarch_dense", "input_aware_scaling",
+    "tsvd_factors", "lowrank_dense", "monarch_factors", "monarch_dense", "blast_factors",
+    "blast_dense", "input_aware_scaling",
     "input_aware_factors", "residual",
     "top_right_singular", "projection", "prepare", "newton_schulz_inverse",
     "solve_right_factor", "forward", "als_factors", "forward_als", "gelu", "mlp_forward",
@@ -114,6 +119,51 @@ def monarch_dense(B1: np.ndarray, B2: np.ndarray) -> np.ndarray:
     return bd1 @ pi @ bd2
 
 
+def blast_dense(U: np.ndarray, V: np.ndarray, S: np.ndarray) -> np.ndarray:
+    """Dense W_hat of a BLAST matrix with nb x nb blocks ([S] Appendix B: row and column bases
+    shared across blocks; [B] structured-methods section: each block is a shared row basis,
+    a block-specific small middle matrix and a shared column basis). U [nb, p, t]: the basis
+    of block row i; V [nb, q, t]: the basis of block column j; S [nb, nb, t, t]: the middle
+    matrix of block (i, j). Block (i, j) = U[i] S[i, j] V[j]^T."""
+    nb, p, t = U.shape
+    q = V.shape[1]
+    W = np.zeros((nb * p, nb * q))
+    for i in range(nb):
+        for j in range(nb):
+            W[i * p:(i + 1) * p, j * q:(j + 1) * q] = U[i] @ S[i, j] @ V[j].T
+    return W
+
+
+def blast_factors(W: np.ndarray, nb: int, t: int, sweeps: int = 10):
+    """BLAST fit by minimising the reconstruction error ||W - W_hat||_F ([B] structured-methods
+    section), alternating exact minimisations with orthonormal bases:
+      start: U[i] = top-t left singular vectors of block row i, V[j] = top-t right singular
+             vectors of block column j;
+      middle matrices (bases fixed): S[i, j] = U[i]^T W_ij V[j] (the least-squares optimum);
+      row bases (column bases fixed, S optimal): U[i] = top-t left singular vectors of
+             [W_i1 V[1], ..., W_i,nb V[nb]] (maximises sum_j ||U[i]^T W_ij V[j]||^2);
+      column bases likewise from [W_1j^T U[1], ..., W_nb,j^T U[nb]];
+    `sweeps` rounds of (U, V), then S. Returns U [nb, p, t], V [nb, q, t], S [nb, nb, t, t]."""
+    d, m = W.shape
+    p, q = d // nb, m // nb
+    if p * nb != d or q * nb != m or t > min(p, q):
+        raise ValueError("BLAST needs nb | d, nb | m and t <= min(d, m) / nb")
+    blk = lambda i, j: W[i * p:(i + 1) * p, j * q:(j + 1) * q]
+    U = np.stack([np.linalg.svd(W[i * p:(i + 1) * p], full_matrices=False)[0][:, :t]
+                  for i in range(nb)])
+    V = np.stack([np.linalg.svd(W[:, j * q:(j + 1) * q], full_matrices=False)[2][:t].T
+                  for j in range(nb)])
+    for _ in range(sweeps):
+        for i in range(nb):
+            K = np.concatenate([blk(i, j) @ V[j] for j in range(nb)], axis=1)
+            U[i] = np.linalg.svd(K, full_matrices=False)[0][:, :t]
+        for j in range(nb):
+            K = np.concatenate([blk(i, j).T @ U[i] for i in range(nb)], axis=1)
+            V[j] = np.linalg.svd(K, full_matrices=False)[0][:, :t]
+    S = np.stack([np.stack([U[i].T @ blk(i, j) @ V[j] for j in range(nb)]) for i in range(nb)])
+    return U, V, S
+
+
 def input_aware_scaling(X_cal: np.ndarray, mode: str) -> np.ndarray:
     """The input-side transform S of an input-aware decomposition, from calibration
     activations X_cal [N, d] ([S] Appendix B: input-aware methods use an activation-based
@@ -175,14 +225,22 @@ def prepare(W: np.ndarray, b: np.ndarray, kind: str, k: int, r: int,
     elif kind == "monarch":
         U, V = factors if factors is not None else monarch_factors(W, k)
         W_hat = monarch_dense(U, V)
+    elif kind == "blast":   # k = (nb, t); factors = (U, V, S)
+        nb, t = k
+        U, V, S = factors if factors is not None else blast_factors(W, nb, t)
+        W_hat = blast_dense(U, V, S)
+        prep_extra = dict(F3=S)
     else:
         raise ValueError(kind)
     W_res = residual(W, W_hat)
     if R0 is None:
         R0 = top_right_singular(W_res, r)
     P = projection(W_res, R0)
-    return dict(kind=kind, k=k, r=r, W=W, b=np.asarray(b, dtype=np.float64), F1=U, F2=V,
-                W_hat=W_hat, W_res=W_res, R0=R0, P=P)
+    out = dict(kind=kind, k=k, r=r, W=W, b=np.asarray(b, dtype=np.float64), F1=U, F2=V,
+               W_hat=W_hat, W_res=W_res, R0=R0, P=P)
+    if kind == "blast":
+        out.update(prep_extra)
+    return out
 
 
 # ------------------------------------------------------------------------------------

@@ -23,7 +23,8 @@ def weights_and_prep(name: str):
     """(W, b, oracle preparation) of a named layer, computed once per test session."""
     cfg = WL.get_config(name)
     W, b = WL.make_weights(cfg)
-    prep = O.prepare(W, b, cfg.kind, cfg.k, cfg.r)
+    k = (cfg.k, cfg.blast_t) if cfg.kind == "blast" else cfg.k
+    prep = O.prepare(W, b, cfg.kind, k, cfg.r)
     return W, b, prep
 
 
@@ -43,6 +44,8 @@ def make_layer(cfg, prep, W, b, **kw):
     import input_adaptive_rank_dyra_b300 as dy
     args = dict(kind=cfg.kind, k=cfg.k, r=cfg.r, F1=prep["F1"], F2=prep["F2"], R0=prep["R0"],
                 dtype=cfg.dtype, device=0, solver=cfg.solver, ns_iters=cfg.ns_iters)
+    if cfg.kind == "blast":
+        args.update(blast_t=cfg.blast_t, F3=prep["F3"])
     args.update(kw)
     return dy.prepare(W, b, **args)
 

@@ -158,6 +158,23 @@ def test_fit_input_aware_rejects_bad_calibration():
         D.fit(W, kind="lowrank", k=3, r=2, input_aware="diag")
 
 
+def test_fit_blast_matches_oracle():
+    """The library's BLAST fit (host fp64, its own SVDs; 10 alternating sweeps from the same
+    start) against the oracle's on the BLAST workload's weights: the same W_hat (each step
+    depends only on the subspaces, not on their bases)."""
+    cfg = WL.get_config("c6")
+    W, b = WL.make_weights(cfg)
+    f = D.fit(W, kind="blast", k=cfg.k, r=cfg.r, blast_t=cfg.blast_t)
+    p = O.prepare(W, b, "blast", (cfg.k, cfg.blast_t), cfg.r)
+    scale = np.abs(W).max()
+    assert np.abs(f["W_hat"] - p["W_hat"]).max() < 1e-8 * scale
+    assert np.abs(f["P"] @ f["R0"] - p["P"] @ p["R0"]).max() < 1e-7 * scale
+    # and the structure is BLAST: every block row of W_hat has rank <= t
+    t, nb, pb = cfg.blast_t, cfg.k, cfg.d // cfg.k
+    for i in range(nb):
+        assert np.linalg.matrix_rank(f["W_hat"][i * pb:(i + 1) * pb], tol=1e-9 * scale) <= t
+
+
 def test_fit_rejects_rank_deficient_r0():
     W = np.random.default_rng(4).standard_normal((20, 30))
     R0 = np.zeros((3, 30))

@@ -53,7 +53,8 @@ def _check_forward(cfg, X, W, b, prep, layer, Y, ridge=0.0):
 # ---------------------------------------------------------------------------- reduced sizes
 
 REDUCED = [("c1", None, None), ("c2", 3, None), ("c2", 2, 61), ("c3_fc1", 2, None),
-           ("c3_fc2", 2, 300), ("c4", 2, None), ("c4", 3, 130), ("c5", 1, 1100)]
+           ("c3_fc2", 2, 300), ("c4", 2, None), ("c4", 3, 130), ("c5", 1, 1100),
+           ("c6", 2, None), ("c6", 3, 100)]
 
 
 @pytest.mark.parametrize("name,batch,n", REDUCED)
@@ -265,7 +266,7 @@ def test_library_fit_end_to_end():
 
 # ---------------------------------------------------------------------------- full sizes
 
-FULL = ["c2", "c3_fc1", "c3_fc2", "c4", "c5"]
+FULL = ["c2", "c3_fc1", "c3_fc2", "c4", "c5", "c6"]
 
 
 @pytest.mark.parametrize("name", FULL)

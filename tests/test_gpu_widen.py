@@ -8,7 +8,9 @@ approximation error E within 2% of the oracle's):
 * a transformer MLP block (fc1 -> GELU -> fc2) with both linear layers replaced (summary page
   Appendix D), on the DINOv3 ViT-L/16 shapes;
 * more ALS iterations, t = 1.5 (L, R, L) and t = 2 (summary page 3.3 / Figure 9), on the
-  Cholesky, Newton-Schulz and Monarch paths.
+  Cholesky, Newton-Schulz and Monarch paths;
+* the BLAST static branch (summary page Appendix B): its block-diagonal first stage and the
+  library's own BLAST fit.
 """
 import functools
 
@@ -132,3 +134,31 @@ def test_als_iterations_match_oracle(name, batch, n, t):
     # more iterations do not raise the error (ALS is monotone on ||X W_res - L R||)
     e1 = O.approximation_error(O.forward(X, prep), X, W, b)
     assert e_gpu <= e1 * 1.002
+
+
+def test_blast_stage_one_and_library_fit():
+    """BLAST's first stage lands in the static columns of T as X blockdiag(U_i) (each 64-wide
+    block of columns from its own 256 input columns), and a layer fitted by the library itself
+    matches the oracle run on its own fit (the fit's bases are gauge; W_hat is not)."""
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    from gpu_util import make_layer, weights_and_prep
+    cfg = WL.reduced(WL.get_config("c6"), batch=2, n=300)
+    W, b, prep = weights_and_prep("c6")
+    X = WL.make_inputs(cfg)
+    layer = make_layer(cfg, prep, W, b)
+    ws = dy.new_workspace(layer, cfg.batch, cfg.n)
+    Y = dy.linear_forward(layer, to_device(X, "bf16"), workspace=ws)
+    torch.cuda.synchronize()
+    nb, t, pb = cfg.k, cfg.blast_t, cfg.d // cfg.k
+    _, ldT = layer.workspace_tensor(cfg.batch, cfg.n, "T")
+    T = to_host(dy.workspace_view(layer, ws, cfg.batch, cfg.n, "T", (cfg.batch, cfg.n, ldT),
+                                  torch.bfloat16))
+    U = prep["F1"]
+    Z = np.concatenate([X[:, :, i * pb:(i + 1) * pb] @ U[i] for i in range(nb)], axis=2)
+    assert rel(T[:, :, :nb * t], Z) <= BF16_TOL
+    assert rel(to_host(Y), O.forward(X, prep)) <= BF16_TOL
+    own = dy.prepare(W, b, kind="blast", k=cfg.k, r=cfg.r, blast_t=t, dtype="bf16", device=0)
+    Y2 = dy.linear_forward(own, to_device(X, "bf16"))
+    torch.cuda.synchronize()
+    assert rel(to_host(Y2), O.forward(X, prep)) <= BF16_TOL

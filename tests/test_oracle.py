@@ -99,6 +99,76 @@ def test_monarch_fit_is_blockwise_optimal():
     assert np.isclose(err, tail, rtol=1e-10)
 
 
+# -------------------------------------------------------------------- BLAST fit
+
+def _planted_blast(rng, nb, p, q, t):
+    U = rng.standard_normal((nb, p, t))
+    V = rng.standard_normal((nb, q, t))
+    S = rng.standard_normal((nb, nb, t, t))
+    W = np.zeros((nb * p, nb * q))
+    for i in range(nb):                    # entry by entry: sum over the middle matrix
+        for j in range(nb):
+            for a in range(p):
+                for c in range(q):
+                    W[i * p + a, j * q + c] = sum(U[i, a, x] * S[i, j, x, y] * V[j, c, y]
+                                                  for x in range(t) for y in range(t))
+    return W, U, V, S
+
+
+def test_blast_dense_matches_index_form():
+    """Appendix B / blog structured-methods section: W_hat[(i,a),(j,c)] =
+    sum_{x,y} U[i][a,x] S[i,j][x,y] V[j][c,y]."""
+    rng = _rng(30)
+    W, U, V, S = _planted_blast(rng, 3, 4, 5, 2)
+    assert np.allclose(O.blast_dense(U, V, S), W, atol=1e-12)
+
+
+def test_blast_fit_recovers_planted_blast():
+    """A matrix that is exactly BLAST (nb = 3, t = 2) is reproduced: each block row has rank
+    t, so the SVD start spans the true bases and the middle matrices are exact."""
+    rng = _rng(31)
+    W, _, _, _ = _planted_blast(rng, 3, 6, 5, 2)
+    for sweeps in (0, 3):
+        U, V, S = O.blast_factors(W, 3, 2, sweeps=sweeps)
+        assert np.linalg.norm(W - O.blast_dense(U, V, S)) < 1e-10 * np.linalg.norm(W)
+
+
+def test_blast_fit_error_never_increases_and_middles_are_optimal():
+    """Each step is an exact minimiser, so the reconstruction error does not increase with
+    the sweeps; the middle matrices are the least-squares optimum for their bases (the block
+    residual is orthogonal to both bases), checked against lstsq on the vectorised block."""
+    rng = _rng(32)
+    W = rng.standard_normal((12, 16))
+    errs = [np.linalg.norm(W - O.blast_dense(*O.blast_factors(W, 4, 2, sweeps=s)))
+            for s in (0, 1, 2, 5, 20)]
+    assert all(errs[i + 1] <= errs[i] * (1 + 1e-12) for i in range(len(errs) - 1))
+    assert errs[-1] < errs[0]
+    U, V, S = O.blast_factors(W, 4, 2, sweeps=5)
+    p, q = 3, 4
+    for i in range(4):
+        for j in range(4):
+            Wij = W[i * p:(i + 1) * p, j * q:(j + 1) * q]
+            A = np.kron(U[i], V[j])          # vec(U S V^T) = (U kron V) vec(S), row-major vec
+            s_ls = np.linalg.lstsq(A, Wij.reshape(-1), rcond=None)[0]
+            assert np.allclose(S[i, j].reshape(-1), s_ls, atol=1e-10)
+
+
+def test_blast_forward_exact_when_residual_rank_at_most_r():
+    """BLAST branch end to end: W = BLAST + A R0 with rank(A) <= r and the planted factors gives
+    Y = X W + b."""
+    rng = _rng(33)
+    Wb, U, V, S = _planted_blast(rng, 2, 6, 5, 2)
+    r = 2
+    A = rng.standard_normal((12, r))
+    R0 = _orth(rng, 10, r).T
+    W = Wb + A @ R0
+    b = rng.standard_normal(10)
+    X = rng.standard_normal((2, 20, 12))
+    prep = O.prepare(W, b, "blast", (2, 2), r, R0=R0, factors=(U, V, S))
+    assert np.allclose(prep["W_res"], A @ R0, atol=1e-11)
+    assert np.allclose(O.forward(X, prep), X @ W + b, atol=1e-9 * np.abs(X @ W).max())
+
+
 # -------------------------------------------------------------------- input-aware fit
 
 def _correlated_calibration(rng, N, d):

@@ -47,6 +47,7 @@ class LayerConfig:
     solver: str = "auto"
     ns_iters: int = 8
     als_t: float = 1.0  # ALS iterations of the correction (1: the one-step form)
+    blast_t: int = 0    # BLAST: rank of every block's middle matrix (k = blocks per side)
     stream: int = 0     # distinguishes two layers that share a seed (fc1 / fc2)
 
     @property
@@ -70,6 +71,10 @@ CONFIGS = {
     # Attention projection 1024 -> 1024 with a Monarch static branch of 32 blocks of 32x32.
     "c4": LayerConfig("c4_monarch32_attn_proj", 16, 1029, 1024, 1024, "monarch", 32, 64, "bf16", 4,
                       "powerlaw", 0.7, "outliers"),
+    # BLAST static branch (4 x 4 blocks of 256 x 256, middle matrices of rank 64) plus the
+    # correction on the attention-projection shape of c4; W and X drawn as in config 2.
+    "c6": LayerConfig("c6_blast4x64_attn_proj", 16, 1029, 1024, 1024, "blast", 4, 64, "bf16", 6,
+                      "powerlaw", 0.7, "outliers", blast_t=64),
     # LLM prefill MLP up-projection 4096 -> 12288, k = 1024, r = 256, Newton-Schulz (8 steps).
     "c5": LayerConfig("c5_prefill_mlp_up", 4, 2048, 4096, 12288, "lowrank", 1024, 256, "bf16", 5,
                       "powerlaw", 0.5, "student_t", solver="newton_schulz", ns_iters=8),

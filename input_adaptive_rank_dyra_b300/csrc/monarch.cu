@@ -1,6 +1,7 @@
 // Monarch static branch of the bf16 DyRA forward: the stride permutation between the two
 // block-diagonal factors (the factors themselves run on the tcgen05 GEMM engine).
 #include "monarch.cuh"
+#include "ptx.cuh"
 
 namespace dyra {
 
@@ -15,6 +16,8 @@ __global__ void __launch_bounds__(256) monarch_permute_kernel(__nv_bfloat16 *T, 
   const int lane = threadIdx.x & 31;
   const long long warp = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  // T comes from the previous kernels of the stream: nothing is read before this wait
+  ptx::pdl_wait();
   for (long long row = warp; row < rows; row += nwarps) {
     __nv_bfloat16 *z = T + row * ldT;
     __nv_bfloat16 v[NB];
@@ -34,6 +37,7 @@ __global__ void __launch_bounds__(256) monarch_permute_kernel(__nv_bfloat16 *T, 
     }
     __syncwarp();
   }
+  ptx::pdl_launch_dependents();
 }
 
 }  // namespace
@@ -52,14 +56,22 @@ cudaError_t launch_monarch_permute(__nv_bfloat16 *T, long long rows, int ldT, in
   if (ldT % 8) return cudaErrorInvalidValue;
   long long blocks = (rows + 7) / 8;
   if (blocks > 148 * 16) blocks = 148 * 16;
-  const dim3 grid((unsigned)blocks);
+  // programmatic stream serialization: the kernel may start while the previous one finishes
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {};
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (nb) {
-    case 8: monarch_permute_kernel<8><<<grid, 256, 0, s>>>(T, rows, ldT); break;
-    case 16: monarch_permute_kernel<16><<<grid, 256, 0, s>>>(T, rows, ldT); break;
-    case 32: monarch_permute_kernel<32><<<grid, 256, 0, s>>>(T, rows, ldT); break;
+    case 8: return cudaLaunchKernelEx(&cfg, monarch_permute_kernel<8>, T, rows, ldT);
+    case 16: return cudaLaunchKernelEx(&cfg, monarch_permute_kernel<16>, T, rows, ldT);
+    case 32: return cudaLaunchKernelEx(&cfg, monarch_permute_kernel<32>, T, rows, ldT);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace dyra

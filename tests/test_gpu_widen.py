@@ -162,3 +162,33 @@ def test_blast_stage_one_and_library_fit():
     Y2 = dy.linear_forward(own, to_device(X, "bf16"))
     torch.cuda.synchronize()
     assert rel(to_host(Y2), O.forward(X, prep)) <= BF16_TOL
+
+
+def test_layers_back_to_back_with_programmatic_launch_on_every_edge():
+    """Several layers enqueued on one stream with no synchronisation between them: every
+    kernel of the chain is launched with programmatic stream serialization and reads its
+    inputs only after griddepcontrol.wait, so a layer never sees another one's half-written
+    intermediates. Order Monarch -> low rank -> Monarch -> BLAST -> Newton-Schulz -> Monarch,
+    each layer with its own workspace and fresh inputs; every output against the oracle."""
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    from gpu_util import make_layer, weights_and_prep
+    order = [("c4", 2, 300), ("c2", 2, None), ("c4", 3, 130), ("c6", 2, 200), ("c5", 1, 500),
+             ("c4", 2, 300)]
+    runs = []
+    for idx, (name, batch, n) in enumerate(order):
+        cfg = WL.reduced(WL.get_config(name), batch=batch, n=n)
+        W, b, prep = weights_and_prep(name)
+        X = WL.make_inputs(cfg) * (1.0 + 0.25 * idx)   # a different input for every run
+        X = WL.round_to_bf16(X)
+        layer = make_layer(cfg, prep, W, b)
+        ws = dy.new_workspace(layer, cfg.batch, cfg.n)
+        runs.append((layer, ws, to_device(X, "bf16"), X, prep, W, b))
+    torch.cuda.synchronize()
+    outs = [dy.linear_forward(layer, Xd, workspace=ws) for layer, ws, Xd, _, _, _, _ in runs]
+    torch.cuda.synchronize()
+    for (layer, ws, _, X, prep, W, b), Y in zip(runs, outs):
+        assert dy.workspace_status(layer, ws) == (0, 0)
+        solver = "cholesky" if layer.solver == "cholesky" else "newton_schulz"
+        Yo = O.forward(X, prep, solver=solver, ns_iters=layer.ns_iters)
+        assert rel(to_host(Y), Yo) <= BF16_TOL, layer.kind

@@ -19,6 +19,7 @@ same workload (rank 0 only) and prints the same line with "impl": "reference".
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import functools
 import hashlib
 import json
@@ -45,17 +46,16 @@ PER_CONFIG = ["c2", "c3_fc1", "c3_fc2", "c4", "c6", "c2_t2"]
 
 
 def bench_config(name):
-    import dataclasses
     if name == "c2_t2":
         return dataclasses.replace(WL.get_config("c2"), name="c2_vitb16_fc1_als_t2", als_t=2.0)
     return WL.get_config(name)
 _CSRC = "input_adaptive_rank_dyra_b300/csrc/"
 # the source files that define each kernel of the forward (a recorded DRAM-traffic figure is
 # used only while their hash matches the one recorded with it)
-GEMM_SOURCES = [_CSRC + "tc_gemm.cu", _CSRC + "tc_gemm.cuh", _CSRC + "ptx.cuh"]
-KERNEL_SOURCES = {"spd_invert": [_CSRC + "solve.cu", _CSRC + "kernels.cuh"],
+GEMM_SOURCES = [_CSRC + "tc_gemm.cu", _CSRC + "tc_gemm.cuh", _CSRC + "ptx.cuh",
+                _CSRC + "sweep.cuh"]
+KERNEL_SOURCES = {"spd_invert": [_CSRC + "solve.cu", _CSRC + "kernels.cuh", _CSRC + "sweep.cuh"],
                   "spd_apply_c": [_CSRC + "solve.cu", _CSRC + "kernels.cuh"],
-                  "ns_prep": [_CSRC + "solve.cu"],
                   "ns_iterate": [_CSRC + "ns.cu", _CSRC + "ptx.cuh", _CSRC + "kernels.cuh"],
                   "monarch_permute": [_CSRC + "monarch.cu", _CSRC + "monarch.cuh"]}
 
@@ -127,6 +127,10 @@ def kernel_work(cfg, name: str):
                     e * (B * n * (d + r) + m * k + B * r * m + B * n * m) + 4 * m)
     if name == "xproj_static_L":
         return 2.0 * B * n * d * (k + r), e * (B * n * d + (k + r) * d + B * n * (k + r))
+    if name == "cg_solve":      # cg_c_gram with the inversion and C~ = G^-1 C in its epilogue
+        return (2.0 * B * n * r * (d + r) + B * 2.0 * r ** 3 + B * 2.0 * r * r * d,
+                e * (B * n * d + B * n * r) + 4 * (B * r * d + B * r * r)
+                + (4 + e) * B * r * r + e * B * r * d)
     if name == "cg_c_gram":
         return 2.0 * B * n * r * (d + r), e * (B * n * d + B * n * r) + 4 * (B * r * d + B * r * r)
     if name == "spd_invert":    # r / 4 block sweeps: about r^3 FMA; G in, G^-1 out (fp32, bf16)
@@ -145,14 +149,12 @@ def kernel_work(cfg, name: str):
         return 2.0 * B * r * d * m, e * (B * r * d + d * m + B * r * m)
     if name == "fused_output":
         return 2.0 * B * n * (k + r) * m, e * (B * n * (k + r) + k * m + B * r * m + B * n * m) + 4 * m
-    if name == "ns_prep":       # G in, [E0 ; X0] out
-        return 3.0 * B * r * r, 4 * (B * r * r + 2 * B * r * r)
-    if name == "ns_iterate":    # [E ; X] E per iteration (the last one X E only), then
-        #                         G^-1 = D X D; the iterates stay in L2: [E0 ; X0] in,
-        #                         G^-1 out (fp32 and bf16)
+    if name == "ns_iterate":    # the start from G, [E ; X] E per iteration (the last one
+        #                         X E only), then G^-1 = D X D; the iterates stay in L2:
+        #                         G in, G^-1 out (fp32 and bf16)
         t = cfg.ns_iters
         return (B * (4.0 * (t - 1) + 2.0) * r ** 3,
-                4 * 2 * B * r * r + (4 + e) * B * r * r)
+                4 * B * r * r + (4 + e) * B * r * r)
     return 0.0, 0.0
 
 
@@ -853,10 +855,17 @@ def main(argv=None):
     ap.add_argument("--clock-warmup-s", type=float, default=1.0,
                     help="seconds of warm-up replays before the timed region (0: only W of "
                          "them, e.g. under a profiler)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="samples per step instead of the workload's own (smaller profiler "
+                         "captures; the line's config then names the reduced batch)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     cfg = WL.get_config(args.config)
+    if args.batch is not None:
+        if args.batch < 1:
+            ap.error("--batch must be >= 1")
+        cfg = dataclasses.replace(cfg, batch=args.batch, name=f"{cfg.name}_batch{args.batch}")
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

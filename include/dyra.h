@@ -229,10 +229,15 @@ dyra_status dyra_mlp_forward(const dyra_layer *fc1, const dyra_layer *fc2, const
                              int batch, int n, void *H, void *Y, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
-/* Same step (same passages as dyra_linear_forward) from HOST buffers: copies X_host -> X_dev, runs the forward, copies Y_dev ->
- * Y_host, all enqueued on `stream` (use page-locked host memory for asynchronous copies;
- * synchronise the stream before reading Y_host). X_dev / Y_dev are device staging buffers
- * owned by the caller. */
+/* Same step (same passages as dyra_linear_forward) from HOST buffers: copies X_host -> X_dev,
+ * runs the forward, copies Y_dev -> Y_host. The samples are independent (one least-squares
+ * system each), so a large batch is cut into up to 8 groups of whole samples whose copies in,
+ * forwards and copies out overlap: the copies run on two streams the layer owns, the forwards
+ * on `stream`, and `stream` waits for the last copy out, so work enqueued on `stream` after
+ * this call (or a synchronisation of `stream`) sees Y_host written. Use page-locked host
+ * memory (pageable memory makes the copies synchronous). X_dev / Y_dev are device staging
+ * buffers owned by the caller; the workspace's status words count every group. Calls on one
+ * layer from several host threads are serialised. */
 dyra_status dyra_linear_forward_host(const dyra_layer *layer, const void *X_host, int batch,
                                      int n, void *Y_host, void *X_dev, void *Y_dev,
                                      void *workspace, size_t workspace_bytes,

@@ -50,6 +50,10 @@ struct dyra_layer {
   float *bias_d = nullptr;
   mutable std::mutex mu;                 // plan cache
   mutable std::vector<std::pair<std::array<uintptr_t, 5>, std::shared_ptr<void>>> plans;
+  // the host-buffer forward's copy streams and events (created on first use)
+  mutable std::mutex host_mu;
+  mutable cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  mutable std::vector<cudaEvent_t> host_ev;
 };
 
 namespace {
@@ -85,10 +89,18 @@ struct DeviceGuard {
 // ------------------------------------------------------------------------ workspace
 
 struct WsLayout {
-  size_t T = 0, C = 0, G = 0, Ginv = 0, EX0 = 0, EX1 = 0, G32 = 0, dinv = 0, flags = 0,
-         B = 0, R = 0, Cs = 0, total = 0;
+  size_t T = 0, C = 0, G = 0, Ginv = 0, EX0 = 0, EX1 = 0, G32 = 0, B = 0, R = 0, Cs = 0,
+         total = 0;
+  size_t clear = 16;   // bytes at the start cleared before a forward (status and flags)
+  size_t ready = 0;    // [2][batch] ints: the fused Gram / solve kernel's per-sample flags
   int ldT = 0;
 };
+
+// The R-update's Gram GEMM takes the SPD solve into its epilogue (one kernel instead of
+// three) for the Cholesky branch.
+inline bool fused_gram_solve(const dyra_layer *L) {
+  return L->dtype == DYRA_BF16 && L->solver == DYRA_SOLVE_CHOLESKY && L->r <= 64 && L->r % 4 == 0;
+}
 
 WsLayout layout_of(const dyra_layer *L, int batch, int n) {
   WsLayout w;
@@ -100,6 +112,10 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
   };
   const size_t B = (size_t)batch, N = (size_t)n, d = L->d, m = L->m, r = L->r;
   if (L->dtype == DYRA_BF16) {
+    if (fused_gram_solve(L)) {   // right after the status words: one memset clears both
+      w.ready = take(B * 2 * 4);
+      w.clear = w.ready + B * 2 * 4;
+    }
     w.ldT = L->kp + L->r;
     w.T = take(B * N * (size_t)w.ldT * 2);
     w.C = take(B * d * r * 4);   // C^T, fp32
@@ -107,10 +123,8 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
     w.Ginv = take(B * r * r * 2);
     w.G32 = take(B * r * r * 4);         // fp32 G^-1, read by the apply step
     if (L->solver == DYRA_SOLVE_NEWTON_SCHULZ) {
-      w.EX0 = take(B * 3 * r * r * 4);   // [E ; X ; I + E] iterate, two buffers
-      w.EX1 = take(B * 3 * r * r * 4);
-      w.dinv = take(B * r * 4);
-      w.flags = take(B * 4);
+      w.EX0 = take(B * 2 * r * r * 4);   // [E ; X] iterate, two buffers
+      w.EX1 = take(B * 2 * r * r * 4);
     }
     w.Cs = take(B * r * d * 2);
     w.R = take(B * r * m * 2);
@@ -134,14 +148,13 @@ WsLayout layout_of(const dyra_layer *L, int batch, int n) {
 // same buffers, so a steady-state forward costs only its launches on the host.
 
 struct Step {
-  enum Kind { GEMM, SPD_INVERT, SPD_APPLY, NS_PREP, NS_FUSED, PERMUTE } kind = GEMM;
+  enum Kind { GEMM, SPD_INVERT, SPD_APPLY, NS_FUSED, PERMUTE } kind = GEMM;
   const char *name = nullptr;   // the kernel's name in dyra_kernel_name
   dyra::TcGemmParams p;
   CUtensorMap a0, a1, b0, b1, out;
-  CUtensorMap ns_maps[2][3];
+  CUtensorMap ns_maps[2][2];
   const float *G = nullptr;
-  float *X0 = nullptr, *X1 = nullptr, *dinv = nullptr;
-  int *flags = nullptr;
+  float *X0 = nullptr, *X1 = nullptr;
   __nv_bfloat16 *Ginv = nullptr;
   __nv_bfloat16 *T = nullptr;
   const float *Ct = nullptr;
@@ -155,6 +168,7 @@ struct Step {
 
 struct Plan {
   std::vector<Step> steps;
+  size_t clear = 16;   // bytes of the workspace cleared before a forward
 };
 
 // Records an event pair around each kernel, on the stream that kernel runs on. Under stream
@@ -460,10 +474,60 @@ dyra_status plan_gram_c(const dyra_layer *L, const void *X, int batch, int n,
   return DYRA_OK;
 }
 
+// The R-update's Gram GEMM with the solve in its epilogue (r <= 64, Cholesky branch): per
+// sample, the G tile [r, r] comes first in the walk and is inverted by its CTA's epilogue
+// warps, which publish (G + lambda I)^-1 (G32 fp32, Ginv bf16) and a flag; each 128-feature
+// C^T tile waits for its sample's flag and writes C~ = (G + lambda I)^-1 C (Cs, bf16
+// [batch, r, d]). C^T and G also go out (fp32) for checks of the intermediates.
+dyra_status plan_gram_solve(const dyra_layer *L, const void *X, int batch, int n,
+                            const __nv_bfloat16 *T, int ldT, float *Ct, float *G,
+                            __nv_bfloat16 *Cs, uint8_t *ws, const WsLayout &w, int *status,
+                            Plan &plan) {
+  using namespace dyra;
+  const int d = L->d, r = L->r, kp = L->kp;
+  CUtensorMap ax, al;
+  DY_MAP(make_map(&ax, X, 2, d, n, batch, d, (long long)n * d, 64));
+  DY_MAP(make_map(&al, T + kp, 2, r, n, batch, ldT, (long long)n * ldT, 64));
+  TcGemmParams p = base_params();
+  p.a_split = (int)cdiv(d, 128);
+  p.m_tiles = p.a_split + 1;
+  p.n_tiles = 1;
+  p.batch = batch;
+  p.BN = roundup(r, 64);
+  p.k_chunks = (int)cdiv(n, 64);
+  p.elem_bytes = 2;
+  p.a_major = 1;
+  p.b_major = 1;
+  p.a_batched0 = p.a_batched1 = 1;
+  p.b_split = p.k_chunks;
+  p.b_batched0 = 1;
+  p.idesc = tc_idesc(2, 1, 1, p.BN);
+  p.epi = EPI_CG_SOLVE;
+  p.g_first = 1;
+  p.solve_r = r;
+  p.ridge = (float)L->ridge;
+  p.ginv32 = reinterpret_cast<float *>(ws + w.G32);
+  p.ginv16 = reinterpret_cast<__nv_bfloat16 *>(ws + w.Ginv);
+  p.cs = Cs;
+  p.cs_d = d;
+  p.ready = reinterpret_cast<int *>(ws + w.ready);
+  p.nspd = status;
+  p.out = Ct;
+  p.out_bstride = (long long)d * r;
+  p.out_ld = r;
+  p.rows_valid = d;
+  p.cols_valid = r;
+  p.out2 = G;
+  p.timeouts = status + 1;
+  plan.steps.push_back(gemm_step(p, ax, al, al, al));
+  plan.steps.back().name = "cg_solve";
+  return DYRA_OK;
+}
+
 // Cs = (Gs + lambda I)^-1 Cs_src^T per sample: Gs [batch, r, r] fp32 (consumed), the operand
 // given as its transpose Ct [batch, d, r] fp32, the result bf16 [batch, r, d]; G^-1 also to
 // Ginv (bf16) and G32 (fp32). r <= 64 (Cholesky branch): one CTA per sample inverts G, then
-// a wide kernel applies the inverse; larger r: Newton-Schulz (ns_prep, ns_iterate), then a
+// a wide kernel applies the inverse; larger r: Newton-Schulz (ns_iterate), then a
 // tf32 GEMM applies the inverse.
 dyra_status plan_solve(const dyra_layer *L, int batch, float *G, float ridge, const float *Ct,
                        __nv_bfloat16 *Cs, uint8_t *ws, const WsLayout &w, int *status,
@@ -491,42 +555,27 @@ dyra_status plan_solve(const dyra_layer *L, int batch, float *G, float ridge, co
     st.name = "spd_apply_c";
     plan.steps.push_back(st);
   } else {
-    // Newton-Schulz in residual form: EX = [E ; X ; Y] per sample ([3r][r] fp32, Y = I + E,
-    // two buffers used in turn); each iteration forms X' = X Y, E' = E E and Y' = I + E'.
+    // Newton-Schulz in residual form, start to finish in one cluster kernel: EX = [E ; X]
+    // per sample ([2r][r] fp32, two buffers used in turn); each iteration forms
+    // X' = X + X E and E' = E E.
     float *EXa = reinterpret_cast<float *>(ws + w.EX0);
     float *EXb = reinterpret_cast<float *>(ws + w.EX1);
-    float *dinv = reinterpret_cast<float *>(ws + w.dinv);
-    int *flags = reinterpret_cast<int *>(ws + w.flags);
-    const long long ex_bs = 3LL * r * r;   // elements between samples of EX
+    const long long ex_bs = 2LL * r * r;   // elements between samples of EX
     {
-      Step st;
-      st.kind = Step::NS_PREP;
-      st.G = G;
-      st.batch = batch;
-      st.r = r;
-      st.ridge = ridge;
-      st.X0 = EXa;
-      st.dinv = dinv;
-      st.flags = flags;
-      st.name = "ns_prep";
-      plan.steps.push_back(st);
-    }
-    {
-      // every iteration and the finish (G^-1 = D X D) in one kernel
       Step st;
       st.kind = Step::NS_FUSED;
       float *bufs[2] = {EXa, EXb};
       for (int bi = 0; bi < 2; ++bi)
-        for (int blk = 0; blk < 3; ++blk)
+        for (int blk = 0; blk < 2; ++blk)
           DY_MAP(make_map(&st.ns_maps[bi][blk], bufs[bi] + (size_t)blk * r * r, 4, r, r, batch, r,
                           ex_bs, 128));
+      st.G = G;
+      st.ridge = ridge;
       st.X0 = EXa;
       st.X1 = EXb;
-      st.dinv = dinv;
       st.batch = batch;
       st.r = r;
       st.nb = L->ns_iters;
-      st.flags = flags;
       st.Ginv = Ginv;
       st.G32 = G32;
       st.status = status;
@@ -584,6 +633,7 @@ dyra_status plan_residual(const dyra_layer *L, int batch, const __nv_bfloat16 *C
     TcGemmParams p = base_params();
     p.m_tiles = (int)cdiv(rows, 128);
     p.n_tiles = (int)cdiv(m, BN);
+    p.m_fast = 1;   // W_res is the large operand: each column block read once from HBM
     p.batch = 1;
     p.BN = BN;
     p.k_chunks = (int)cdiv(d, 64);
@@ -756,20 +806,26 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
     plan.steps.push_back(st);
   }
   // 2-4. the R-update: [C^T ; G] = [X | L]^T L, C~ = (G + lambda I)^-1 C, R = C~ W_res
-  dyra_status st2 = plan_gram_c(L, X, batch, n, T, ldT, Ct, G, status, plan);
-  if (st2 == DYRA_OK) st2 = plan_solve(L, batch, G, (float)L->ridge, Ct, Cs, ws, w, status, plan);
-  if (st2 == DYRA_OK) st2 = plan_residual(L, batch, Cs, Rm, status, plan);
+  auto r_update = [&]() {
+    dyra_status e;
+    if (fused_gram_solve(L)) {
+      e = plan_gram_solve(L, X, batch, n, T, ldT, Ct, G, Cs, ws, w, status, plan);
+    } else {
+      e = plan_gram_c(L, X, batch, n, T, ldT, Ct, G, status, plan);
+      if (e == DYRA_OK) e = plan_solve(L, batch, G, (float)L->ridge, Ct, Cs, ws, w, status, plan);
+    }
+    if (e == DYRA_OK) e = plan_residual(L, batch, Cs, Rm, status, plan);
+    return e;
+  };
+  dyra_status st2 = r_update();
   if (st2 != DYRA_OK) return st2;
   // further ALS half-steps (t > 1): an L-update from the current R, then (t >= 2) another
   // R-update from the new L, and so on; the workspace buffers are reused
   for (int hs = 2; hs < L->als_half; ++hs) {
     if (hs % 2 == 0)
       st2 = plan_l_update(L, X, batch, n, T, ldT, Rm, G, Ct, Cs, ws, w, status, plan);
-    else {
-      st2 = plan_gram_c(L, X, batch, n, T, ldT, Ct, G, status, plan);
-      if (st2 == DYRA_OK) st2 = plan_solve(L, batch, G, (float)L->ridge, Ct, Cs, ws, w, status, plan);
-      if (st2 == DYRA_OK) st2 = plan_residual(L, batch, Cs, Rm, status, plan);
-    }
+    else
+      st2 = r_update();
     if (st2 != DYRA_OK) return st2;
   }
   // 5. Y = [X U | L] [V ; R] + b: K chunks of V^T (K-major, shared by all samples), then
@@ -871,7 +927,12 @@ dyra_status plan_bf16(const dyra_layer *L, const void *X, int batch, int n, void
 dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream_t s,
                      Recorder &rec, bool clear_status) {
   using namespace dyra;
-  if (clear_status) DY_CUDA(cudaMemsetAsync(ws, 0, 16, s));
+  // the fused Gram / solve kernel's flags are cleared even when the status words are kept
+  // (a chained layer's flags may share bytes with the previous layer's buffers)
+  if (clear_status)
+    DY_CUDA(cudaMemsetAsync(ws, 0, plan.clear, s));
+  else if (plan.clear > 16)
+    DY_CUDA(cudaMemsetAsync(static_cast<uint8_t *>(ws) + 16, 0, plan.clear - 16, s));
   for (const Step &st : plan.steps) {
     const cudaStream_t ks = s;
     switch (st.kind) {
@@ -885,15 +946,12 @@ dyra_status run_plan(const dyra_layer *L, const Plan &plan, void *ws, cudaStream
       case Step::SPD_APPLY:
         DY_TIMED(rec, ks, launch_spd_apply(st.G32, st.batch, st.r, st.Ct, st.d, st.Cs, ks));
         break;
-      case Step::NS_PREP:
-        DY_TIMED(rec, ks, launch_ns_prep(st.G, st.batch, st.r, st.ridge, st.X0, st.dinv, st.flags, ks));
-        break;
       case Step::PERMUTE:
         DY_TIMED(rec, ks, launch_monarch_permute(st.T, st.rows, st.ldT, st.nb, ks));
         break;
       case Step::NS_FUSED:
-        DY_TIMED(rec, ks, launch_ns_fused(st.ns_maps, st.batch, st.r, st.nb, st.X0, st.X1,
-                                          st.dinv, st.flags, st.G32, st.Ginv, st.status, ks));
+        DY_TIMED(rec, ks, launch_ns_fused(st.ns_maps, st.batch, st.r, st.nb, st.ridge, st.G, st.X0,
+                                          st.X1, st.G32, st.Ginv, st.status, ks));
         break;
       default:
         break;
@@ -967,11 +1025,15 @@ std::vector<const char *> forward_kernel_names(const dyra_layer *L) {
     if (L->solver == DYRA_SOLVE_CHOLESKY)
       v.insert(v.end(), {"spd_invert", "spd_apply_c"});
     else
-      v.insert(v.end(), {"ns_prep", "ns_iterate", "ginv_c"});
+      v.insert(v.end(), {"ns_iterate", "ginv_c"});
   };
   auto r_update = [&]() {
-    v.push_back("cg_c_gram");
-    solve();
+    if (fused_gram_solve(L)) {
+      v.push_back("cg_solve");
+    } else {
+      v.push_back("cg_c_gram");
+      solve();
+    }
     v.push_back("residual_product");
   };
   r_update();
@@ -1025,6 +1087,7 @@ dyra_status forward_impl(const dyra_layer *L, const void *X, int batch, int n, v
     plan = std::make_shared<Plan>();
     dyra_status ps = plan_bf16(L, X, batch, n, Y, ws, w, *plan);
     if (ps != DYRA_OK) return ps;
+    plan->clear = w.clear;
     if (plan->steps.size() != (size_t)kernels_per_forward(L)) {
       g_last_error = "internal: the launch plan does not match the kernel list";
       return DYRA_ERR_INVALID_ARG;
@@ -1651,6 +1714,9 @@ void dyra_layer_destroy(dyra_layer *layer) {
     DeviceGuard guard(layer->device);
     cudaDeviceSynchronize();   // no forward of this layer may still read its weights
     free_device(layer);
+    for (cudaEvent_t e : layer->host_ev) cudaEventDestroy(e);
+    if (layer->copy_in) cudaStreamDestroy(layer->copy_in);
+    if (layer->copy_out) cudaStreamDestroy(layer->copy_out);
   }
   delete layer;
 }
@@ -1734,11 +1800,55 @@ dyra_status dyra_linear_forward_host(const dyra_layer *L, const void *X_host, in
   const size_t xb = (size_t)batch * n * L->d * eb, yb = (size_t)batch * n * L->m * eb;
   if (workspace_bytes < layout_of(L, batch, n).total) return DYRA_ERR_WORKSPACE;
   DeviceGuard guard(L->device);
-  DY_CUDA(cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, stream));
   Recorder rec;
-  dyra_status st = forward_impl(L, X_dev, batch, n, Y_dev, workspace, workspace_bytes, stream, rec);
-  if (st != DYRA_OK) return st;
-  DY_CUDA(cudaMemcpyAsync(Y_host, Y_dev, yb, cudaMemcpyDeviceToHost, stream));
+  // groups of whole samples, each at least 8 MB of X and Y, at most 8 of them
+  const int groups = (int)std::min<size_t>({(size_t)batch, 8, std::max<size_t>(1, (xb + yb) >> 23)});
+  if (groups <= 1) {
+    DY_CUDA(cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, stream));
+    dyra_status st = forward_impl(L, X_dev, batch, n, Y_dev, workspace, workspace_bytes, stream, rec);
+    if (st != DYRA_OK) return st;
+    DY_CUDA(cudaMemcpyAsync(Y_host, Y_dev, yb, cudaMemcpyDeviceToHost, stream));
+    return DYRA_OK;
+  }
+  std::lock_guard<std::mutex> lock(L->host_mu);
+  if (!L->copy_in) DY_CUDA(cudaStreamCreateWithFlags(&L->copy_in, cudaStreamNonBlocking));
+  if (!L->copy_out) DY_CUDA(cudaStreamCreateWithFlags(&L->copy_out, cudaStreamNonBlocking));
+  const size_t need = 2 + 2 * (size_t)groups;
+  while (L->host_ev.size() < need) {
+    cudaEvent_t e;
+    DY_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    L->host_ev.push_back(e);
+  }
+  cudaEvent_t *ev = L->host_ev.data();
+  // the copies start after the work already on `stream` (earlier users of X_dev / Y_dev)
+  DY_CUDA(cudaEventRecord(ev[0], stream));
+  DY_CUDA(cudaStreamWaitEvent(L->copy_in, ev[0], 0));
+  DY_CUDA(cudaStreamWaitEvent(L->copy_out, ev[0], 0));
+  DY_CUDA(cudaMemsetAsync(workspace, 0, 16, stream));   // status words, counted over all groups
+  const size_t xs = xb / (size_t)batch, ys = yb / (size_t)batch;
+  for (int gi = 0; gi < groups; ++gi) {
+    const int b0 = (int)((long long)batch * gi / groups), b1 = (int)((long long)batch * (gi + 1) / groups);
+    const size_t xo = xs * (size_t)b0, yo = ys * (size_t)b0;
+    const size_t xn = xs * (size_t)(b1 - b0), yn = ys * (size_t)(b1 - b0);
+    cudaEvent_t in_done = ev[2 + 2 * gi], fwd_done = ev[3 + 2 * gi];
+    DY_CUDA(cudaMemcpyAsync(static_cast<uint8_t *>(X_dev) + xo,
+                            static_cast<const uint8_t *>(X_host) + xo, xn, cudaMemcpyHostToDevice,
+                            L->copy_in));
+    DY_CUDA(cudaEventRecord(in_done, L->copy_in));
+    DY_CUDA(cudaStreamWaitEvent(stream, in_done, 0));
+    dyra_status st = forward_impl(L, static_cast<const uint8_t *>(X_dev) + xo, b1 - b0, n,
+                                  static_cast<uint8_t *>(Y_dev) + yo, workspace, workspace_bytes,
+                                  stream, rec, false);
+    if (st != DYRA_OK) return st;
+    DY_CUDA(cudaEventRecord(fwd_done, stream));
+    DY_CUDA(cudaStreamWaitEvent(L->copy_out, fwd_done, 0));
+    DY_CUDA(cudaMemcpyAsync(static_cast<uint8_t *>(Y_host) + yo,
+                            static_cast<const uint8_t *>(Y_dev) + yo, yn, cudaMemcpyDeviceToHost,
+                            L->copy_out));
+  }
+  // `stream` completes after the last copy out
+  DY_CUDA(cudaEventRecord(ev[1], L->copy_out));
+  DY_CUDA(cudaStreamWaitEvent(stream, ev[1], 0));
   return DYRA_OK;
 }
 

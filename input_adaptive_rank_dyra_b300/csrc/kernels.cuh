@@ -16,18 +16,16 @@ cudaError_t launch_spd_invert(const float *G, int batch, int r, float ridge, flo
 // Cs [batch][r][d] bf16.
 cudaError_t launch_spd_apply(const float *Ginv32, int batch, int r, const float *Ct, int d,
                              __nv_bfloat16 *Cs, cudaStream_t s);
-// Newton-Schulz start (r <= 256): dinv = diag(G + ridge I)^-1/2, Gh = D (G + ridge I) D,
-// alpha = 1 / ||Gh||_inf, EX[b] = [I - alpha Gh ; alpha I ; 2I - alpha Gh] ([batch][3r][r]
-// fp32); flags[b] marks a sample whose diagonal is not positive and finite (its alpha is 0).
-cudaError_t launch_ns_prep(const float *G, int batch, int r, float ridge, float *EX, float *dinv,
-                           int *flags, cudaStream_t s);
-// All Newton-Schulz iterations and the finish in one kernel (ns.cu): from the iterate
-// EX = [E0 ; X0 ; Y0] that ns_prep leaves in ex0 ([batch][3r][r] fp32; ex1 the second
-// buffer), iters steps of X' = X Y, E' = E E, Y' = I + E', then G^-1 = D X D to G32 (fp32)
-// and Ginv (bf16). maps[i][0..2]: fp32 tensor maps of the E, X and Y blocks of buffer i
-// ([batch][r][r], row stride r, batch stride 3 r r, box {32, 128}). r <= 256, r % 8 == 0.
-cudaError_t launch_ns_fused(const CUtensorMap (&maps)[2][3], int batch, int r, int iters,
-                            float *ex0, float *ex1, const float *dinv, const int *flags, float *G32,
+// Newton-Schulz inverse of (G + ridge I) in one kernel (ns.cu), r <= 256, r % 8 == 0: the
+// start (D = diag(G + ridge I)^-1/2, G_hat = D (G + ridge I) D, alpha = 1 / ||G_hat||_inf,
+// E0 = I - alpha G_hat, X0 = alpha I, written to ex0), iters steps of X' = X + X E, E' = E E
+// with the iterates in ex0 / ex1 ([batch][2r][r] fp32, [E ; X]), then G^-1 = D X D to G32
+// (fp32) and Ginv (bf16). maps[i][0..1]: fp32 tensor maps of the E and X blocks of buffer i
+// ([batch][r][r], row stride r, batch stride 2 r r, box {32, 128}). A sample whose diagonal
+// is not positive and finite, or whose result is not finite, gets G^-1 = 0 and is counted in
+// status[0]; bounded waits that gave up are counted in status[1].
+cudaError_t launch_ns_fused(const CUtensorMap (&maps)[2][2], int batch, int r, int iters,
+                            float ridge, const float *G, float *ex0, float *ex1, float *G32,
                             __nv_bfloat16 *Ginv, int *status, cudaStream_t s);
 
 // failure-path self-test (probe.cu): one CTA whose bounded mbarrier wait, limited to

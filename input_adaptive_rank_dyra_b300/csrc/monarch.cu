@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(256) monarch_permute_kernel(__nv_bfloat16 *T, 
   const int lane = threadIdx.x & 31;
   const long long warp = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  // the next kernel may start launching (it waits for this grid to finish before reading)
+  ptx::pdl_launch_dependents();
   // T comes from the previous kernels of the stream: nothing is read before this wait
   ptx::pdl_wait();
   for (long long row = warp; row < rows; row += nwarps) {
@@ -24,7 +26,7 @@ __global__ void __launch_bounds__(256) monarch_permute_kernel(__nv_bfloat16 *T, 
     if (lane < NB) {
 #pragma unroll
       for (int c = 0; c < NB; c += 8) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(z + lane * NB + c);
+        const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(z + lane * NB + c));
         const __nv_bfloat16 *h = reinterpret_cast<const __nv_bfloat16 *>(&w);
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[c + j] = h[j];
@@ -37,7 +39,6 @@ __global__ void __launch_bounds__(256) monarch_permute_kernel(__nv_bfloat16 *T, 
     }
     __syncwarp();
   }
-  ptx::pdl_launch_dependents();
 }
 
 }  // namespace

@@ -1,28 +1,34 @@
 // Newton-Schulz inverse of the per-sample Gram matrix for larger r ("DyRA" summary page, 2.4:
-// Newton-Schulz for larger r, on tensor cores), all iterations in one kernel.
+// Newton-Schulz for larger r, on tensor cores): the start, every iteration and the finish in
+// one kernel.
 //
-// ns_prep (solve.cu) leaves, per sample, the iterate EX = [E0 ; X0 ; Y0] ([3r][r] fp32) with
-// E0 = I - alpha G_hat, X0 = alpha I and Y0 = I + E0. One iteration of X <- X (2I - G_hat X)
-// is, with E = I - G_hat X (E and X are polynomials in G_hat, hence symmetric and commuting)
-// and Y = I + E,
-//     X' = X (2I - G_hat X) = X Y,        E' = I - G_hat X' = E E,        Y' = I + E',
-// two products per iteration (the last iteration forms X' only). The kernel finishes with
-// G^-1 = D X_T D (D = diag(G + lambda I)^-1/2).
+// Start (Jacobi scaling): D = diag(G + lambda I)^-1/2, G_hat = D (G + lambda I) D,
+// alpha = 1 / max_i sum_j |G_hat_ij|, X0 = alpha I, E0 = I - alpha G_hat. One iteration of
+// X <- X (2I - G_hat X) is, with E = I - G_hat X (E and X are polynomials in G_hat, hence
+// symmetric and commuting),
+//     X' = X (2I - G_hat X) = X + X E,        E' = I - G_hat X' = E E,
+// two products per iteration (the last iteration forms X' only). X = Z + alpha I where Z
+// starts at 0 and collects the products X E: Z stays in the tensor memory accumulator of its
+// tile across iterations (fp32), the identity part is never rounded, and the iterate written
+// for the other tiles is Z + alpha I. The kernel finishes with G^-1 = D X_T D.
 //
 // A cluster of 2 rt^2 CTAs (rt = ceil(r / 128)) takes one sample: CTA c owns the 128 x 128
-// output tile (row block c / rt of [E ; X], column block c % rt). Per iteration it streams the
-// K chunks of its A rows (E or X) and of its B operand (rows of E for E tiles, of Y for X
-// tiles: both symmetric, so B^T = B) by TMA from the iterate in global memory (L2-resident)
-// into a ring of shared-memory stages and accumulates the tf32 products in TMEM (tcgen05.mma,
-// issued by one thread). The epilogue warps stage the tile, 32 columns at a time, in the idle
-// ring buffers (128-byte swizzle) and write it with TMA stores: E tiles write E' and Y', X
-// tiles write X'. The iterates alternate between two buffers. Between iterations the stores
-// complete and every thread of the cluster meets at a cluster barrier (release / acquire), so
-// the next iteration's loads see the whole new iterate; every thread executes every barrier,
-// whatever its role did, so a wait that gives up cannot leave a peer blocked.
+// output tile (row block c / rt of [E ; X], column block c % rt). At the start each CTA reads
+// the whole diagonal of G, the row sums of |G_hat| for every nc-th row (the maximum goes to
+// the cluster through distributed shared memory, in a fixed order) and writes its own tile of
+// E0 or X0. Per iteration it streams the K chunks of its A rows (E or X) and of its B operand
+// (rows of E: E is symmetric, so B^T = B) by TMA from the iterate in global memory
+// (L2-resident) into a ring of shared-memory stages and accumulates the tf32 products in TMEM
+// (tcgen05.mma, issued by one thread). The epilogue warps stage the tile, 32 columns at a
+// time, in the idle ring buffers (128-byte swizzle) and write it with TMA stores. The iterates
+// alternate between two buffers. Between iterations the stores complete and every thread of
+// the cluster meets at a cluster barrier (release / acquire), so the next iteration's loads
+// see the whole new iterate; every thread executes every barrier, whatever its role did, so a
+// wait that gives up cannot leave a peer blocked.
 //
 // Warps: 0 TMA producer (one lane), 1 TMEM allocation and MMA issue (one lane), 4..7 epilogue
-// (warp w reads TMEM lane quarter w % 4, i.e. rows 32 (w % 4) .. + 31 of the tile).
+// (warp w reads TMEM lane quarter w % 4, i.e. rows 32 (w % 4) .. + 31 of the tile); all eight
+// take part in the start.
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "tc_gemm.cuh"
@@ -39,22 +45,23 @@ constexpr int kNsfStages = 6;
 constexpr uint32_t kNsfStageBytes = 2 * 16384;   // A and B chunks: 128 rows x 128 bytes each
 constexpr uint32_t kNsfSmem = 1024 + kNsfStages * kNsfStageBytes + 256;
 constexpr int kEpiBarrier = 1;                    // named barrier of the 4 epilogue warps
+constexpr int kNsMaxR = 256;
 
 struct NsParams {
   int r, rt, iters;
-  float *ex0, *ex1;            // iterate buffers, [batch][3r][r] fp32 each ([E ; X ; Y])
-  const float *dinv;           // [batch][r]
-  const int *flags;            // [batch]: start flagged (diagonal not positive and finite)
+  float ridge;
+  const float *G;              // [batch][r][r] fp32 (without the ridge)
+  float *ex0, *ex1;            // iterate buffers, [batch][2r][r] fp32 each ([E ; X])
   float *G32;                  // [batch][r][r] fp32 G^-1
   __nv_bfloat16 *Ginv;         // [batch][r][r] bf16 G^-1
   int *status;                 // [0] samples set to 0, [1] bounded waits that gave up
   uint32_t idesc;
 };
 
-// The six tensor maps of the two iterate buffers: E, X and Y blocks of each ([batch][r][r],
+// The four tensor maps of the two iterate buffers: E and X blocks of each ([batch][r][r],
 // box {32, 128}, 128-byte swizzle), used for the TMA loads and for the TMA stores.
 struct NsMaps {
-  CUtensorMap m[2][3];
+  CUtensorMap m[2][2];
 };
 
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -70,14 +77,24 @@ __device__ __forceinline__ int ld_cluster_s32(const int *p, uint32_t rank) {
   return v;
 }
 
+__device__ __forceinline__ float ld_cluster_f32(const float *p, uint32_t rank) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];"
+               : "=f"(v)
+               : "r"(ptx::mapa_shared(ptx::smem_u32(p), rank))
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync %0, 128;" ::"n"(kEpiBarrier) : "memory");
 }
 
 // 32 fp32 values of row `row` (0..127) into a 128 x 32 staging tile with the 128-byte
-// swizzle TMA uses (16-byte chunk c of row i at chunk c ^ (i % 8)); `diag` >= 0 adds 1 to
-// column diag of the row (Y = I + E).
-__device__ __forceinline__ void stage_row32(uint32_t buf, int row, const uint32_t *v, int diag) {
+// swizzle TMA uses (16-byte chunk c of row i at chunk c ^ (i % 8)); `diag` >= 0 adds `add`
+// to column diag of the row.
+__device__ __forceinline__ void stage_row32(uint32_t buf, int row, const uint32_t *v, int diag,
+                                            float add) {
   const uint32_t dst = buf + (uint32_t)row * 128u;
   const uint32_t sw = (uint32_t)(row & 7);
 #pragma unroll
@@ -85,7 +102,7 @@ __device__ __forceinline__ void stage_row32(uint32_t buf, int row, const uint32_
     float w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      w[k] = __uint_as_float(v[4 * c + k]) + ((4 * c + k) == diag ? 1.f : 0.f);
+      w[k] = __uint_as_float(v[4 * c + k]) + ((4 * c + k) == diag ? add : 0.f);
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (((uint32_t)c ^ sw) << 4)),
                  "f"(w[0]), "f"(w[1]), "f"(w[2]), "f"(w[3])
                  : "memory");
@@ -95,6 +112,9 @@ __device__ __forceinline__ void stage_row32(uint32_t buf, int row, const uint32_
 __global__ void __launch_bounds__(kNsfThreads, 1)
     ns_fused_kernel(const __grid_constant__ NsMaps maps, const __grid_constant__ NsParams p) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ float sd[kNsMaxR];   // D
+  __shared__ float red[kNsfThreads / 32];
+  __shared__ float cmax, alpha_s;
   __shared__ int bad_cta;
   __shared__ int bad_all;
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -105,8 +125,8 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
   const uint32_t tmem_slot = tfull_bar + 8u;
   volatile uint32_t *tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t *>(smem_raw + (tmem_slot - raw_addr));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = (int)ptx::cluster_ctarank();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = (int)ptx::cluster_ctarank(), nc = (int)ptx::cluster_nctarank();
   const int b = blockIdx.y;
   const int r = p.r, rt = p.rt;
   const int rb = c / rt, cb = c % rt;            // row block of [E ; X], column block
@@ -124,7 +144,7 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
     ptx::mbar_init(tfull_bar, 1);
     ptx::mbar_init_fence();
     for (int i = 0; i < 2; ++i)
-      for (int j = 0; j < 3; ++j) ptx::tma_prefetch_desc(&maps.m[i][j]);
+      for (int j = 0; j < 2; ++j) ptx::tma_prefetch_desc(&maps.m[i][j]);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, 128);
@@ -134,8 +154,76 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
-  // the iterate and D come from the previous kernel (ns_prep)
+  // the apply GEMM may start launching now (it waits for this grid to finish before reading)
+  ptx::pdl_launch_dependents();
+  // G comes from the previous kernel of the stream: nothing is read before this wait
   ptx::pdl_wait();
+
+  // ------------------------------------------------------------ start
+  // D from the whole diagonal (every CTA reads it: the flag of a diagonal entry that is not
+  // positive and finite is the same in every CTA of the sample)
+  const float *g = p.G + (size_t)b * r * r;
+  bool bad = false;
+  if (tid < r) {
+    const float gii = __ldcg(g + (size_t)tid * r + tid) + p.ridge;
+    bad = !(gii > 0.f && gii < INFINITY);
+    sd[tid] = bad ? 0.f : rsqrtf(gii);
+  }
+  bad = __syncthreads_or(bad) != 0;
+  // row sums of |G_hat| of rows c, c + nc, ... (warp w takes every 8th of them)
+  float rmax = 0.f;
+  for (int i = c + nc * warp; i < r; i += nc * (kNsfThreads / 32)) {
+    const float *gr = g + (size_t)i * r;
+    float s = 0.f;
+    for (int j = lane; j < r; j += 32)
+      s += fabsf((__ldcg(gr + j) + (i == j ? p.ridge : 0.f)) * sd[i] * sd[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    rmax = fmaxf(rmax, s);
+  }
+  if (lane == 0) red[warp] = rmax;
+  __syncthreads();
+  if (tid == 0) {
+    float m = 0.f;
+    for (int k = 0; k < kNsfThreads / 32; ++k) m = fmaxf(m, red[k]);
+    cmax = m;
+  }
+  ptx::cluster_sync_all();   // every CTA's cmax is written
+  if (tid == 0) {
+    float m = 0.f;
+    for (int k = 0; k < nc; ++k) m = fmaxf(m, ld_cluster_f32(&cmax, (uint32_t)k));
+    // a flagged sample starts from E0 = I, X0 = 0: every iterate and its G^-1 stay 0
+    alpha_s = (bad || !(m > 0.f)) ? 0.f : 1.f / m;
+  }
+  __syncthreads();
+  const float alpha = alpha_s;
+  {
+    // this CTA's tile of the start: E0 = I - alpha G_hat (E tiles) or X0 = alpha I (X tiles)
+    float *dst = (x_tile ? p.ex0 + (size_t)r * r : p.ex0) + (size_t)b * 2 * r * r;
+    for (int e = tid; e < 128 * 32; e += kNsfThreads) {
+      const int i = row0 + e / 32, j = col0 + 4 * (e % 32);
+      if (i < r && j < r) {   // r % 8 == 0: a group of 4 columns is inside or outside
+        float v[4];
+        if (x_tile) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) v[k] = i == j + k ? alpha : 0.f;
+        } else {
+          const float4 gv = __ldcg(reinterpret_cast<const float4 *>(g + (size_t)i * r + j));
+          const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float gh = (gg[k] + (i == j + k ? p.ridge : 0.f)) * sd[i] * sd[j + k];
+            v[k] = (i == j + k ? 1.f : 0.f) - alpha * gh;
+          }
+        }
+        *reinterpret_cast<float4 *>(dst + (size_t)i * r + j) = make_float4(v[0], v[1], v[2], v[3]);
+      }
+    }
+  }
+  // the start is in global memory, visible to the TMA loads of every CTA of the cluster
+  fence_proxy_async_global();
+  ptx::cluster_sync_all();
+  fence_proxy_async_global();
 
   bool ok = true;                    // this thread's bounded waits all completed
   uint32_t ring = 0, ring_ph = 0;    // producer / MMA position in the stage ring
@@ -146,7 +234,7 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
     const bool active = !(last && !x_tile);      // the last iteration forms X' only
     const int src = t & 1;
     const CUtensorMap *mA = &maps.m[src][x_tile ? 1 : 0];
-    const CUtensorMap *mB = &maps.m[src][x_tile ? 2 : 0];
+    const CUtensorMap *mB = &maps.m[src][0];
     if (active && warp == 0 && lane == 0) {
       // ------------------------------------------------------------ TMA producer
       uint32_t s = ring, ph = ring_ph;
@@ -165,6 +253,8 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
       }
     } else if (active && warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issue
+      // E' = E E starts from 0; Z' = Z + X E accumulates onto Z (0 before the first iteration)
+      const uint32_t keep = (x_tile && t > 0) ? 1u : 0u;
       uint32_t s = ring, ph = ring_ph;
       const uint64_t a0 = ptx::sdesc_sw128(base, 16u, 1024u);
       const uint64_t b0 = ptx::sdesc_sw128(base + 16384u, 16u, 1024u);
@@ -177,7 +267,7 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
 #pragma unroll
           for (uint32_t ks = 0; ks < 4; ++ks)   // 4 MMAs of K = 8 (32 bytes) per chunk
             ptx::tc_mma_tf32(tmem, a0 + soff + 2 * ks, b0 + soff + 2 * ks, p.idesc,
-                             (kc | ks) ? 1u : 0u);
+                             (kc | ks) ? 1u : keep);
           ptx::tc_commit(empty_bar + 8u * s);
         }
         if (++s == kNsfStages) {
@@ -195,7 +285,7 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
       ptx::tc_fence_after();
       if (!last) {
         // every ring stage has been consumed by this iteration's MMAs: the ring holds the
-        // staging tiles (piece pc: E' or X' at stage pc, Y' in its second half)
+        // staging tiles (piece pc at stage pc); X tiles write Z' + alpha I
         const int row = 32 * q + lane;
         const int dst = src ^ 1;
         for (int pc = 0; pc < 4; ++pc) {
@@ -205,16 +295,12 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
           ptx::tmem_ld32(taddr + (uint32_t)(32 * pc), v);
           ptx::tmem_ld_wait();
           const uint32_t buf = base + (uint32_t)pc * kNsfStageBytes;
-          stage_row32(buf, row, v, -1);
-          if (!x_tile) {   // Y' = I + E': the diagonal is column row0 + row of this tile
-            const int dcol = row0 + row - j0;
-            stage_row32(buf + 16384u, row, v, (dcol >= 0 && dcol < 32) ? dcol : -1);
-          }
+          const int dcol = row0 + row - j0;
+          stage_row32(buf, row, v, (x_tile && dcol >= 0 && dcol < 32) ? dcol : -1, alpha);
           ptx::fence_proxy_async_smem();
           epi_sync();
           if (warp == 4 && lane == 0 && got) {
             ptx::tma_store_3d(&maps.m[dst][x_tile ? 1 : 0], buf, j0, row0, b);
-            if (!x_tile) ptx::tma_store_3d(&maps.m[dst][2], buf + 16384u, j0, row0, b);
             ptx::bulk_commit();
           }
         }
@@ -240,13 +326,12 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
   }
 
   // ------------------------------------------------------------ finish: G^-1 = D X_T D
-  // The X tiles' accumulators hold X_T = X_{T-1} Y_{T-1}. A sample whose start was flagged, or
+  // The X tiles' accumulators hold Z_T = X_T - alpha I. A sample whose start was flagged, or
   // whose result is not finite anywhere, gets G^-1 = 0 and is counted once.
-  const float *dv = p.dinv + (size_t)b * r;
   if (threadIdx.x == 0) bad_cta = 0;
   __syncthreads();
   const int i = row0 + 32 * q + lane;
-  bool bad = false;
+  bool nonfinite = false;
   if (x_tile && warp >= 4) {
     for (int pc = 0; pc < 4; ++pc) {
       const int j0 = col0 + 32 * pc;
@@ -256,23 +341,23 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
       ptx::tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (i < r && j0 + j < r) bad = bad || !(fabsf(__uint_as_float(v[j])) < INFINITY);
+        if (i < r && j0 + j < r) nonfinite = nonfinite || !(fabsf(__uint_as_float(v[j])) < INFINITY);
     }
-    if (!ok) bad = true;
+    if (!ok) nonfinite = true;
   }
-  if (bad) bad_cta = 1;
+  if (nonfinite) bad_cta = 1;
   // the cluster agrees on the sample's flag before anything is written
   ptx::cluster_sync_all();
   if (threadIdx.x == 0) {
-    int any = p.flags[b];
-    for (int k = 0; k < (int)ptx::cluster_nctarank(); ++k) any |= ld_cluster_s32(&bad_cta, (uint32_t)k);
+    int any = bad ? 1 : 0;
+    for (int k = 0; k < nc; ++k) any |= ld_cluster_s32(&bad_cta, (uint32_t)k);
     bad_all = any;
     if (any && c == 0) atomicAdd(p.status, 1);
   }
   ptx::cluster_sync_all();   // no CTA leaves while a peer may still read its flag
   if (x_tile && warp >= 4) {
     const bool zero = bad_all != 0;
-    const float di = i < r ? dv[i] : 0.f;
+    const float di = i < r ? sd[i] : 0.f;
     for (int pc = 0; pc < 4; ++pc) {
       const int j0 = col0 + 32 * pc;
       if (j0 >= r) break;
@@ -284,12 +369,16 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           if (j0 + j >= r) break;   // r % 8 == 0: whole groups of 4
-          float g[4];
+          float gv[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) g[k] = zero ? 0.f : di * __uint_as_float(v[j + k]) * dv[j0 + j + k];
-          *reinterpret_cast<float4 *>(p.G32 + o + j) = make_float4(g[0], g[1], g[2], g[3]);
-          __nv_bfloat162 h0 = __floats2bfloat162_rn(g[0], g[1]);
-          __nv_bfloat162 h1 = __floats2bfloat162_rn(g[2], g[3]);
+          for (int k = 0; k < 4; ++k) {
+            const int jj = j0 + j + k;
+            const float x = __uint_as_float(v[j + k]) + (i == jj ? alpha : 0.f);
+            gv[k] = zero ? 0.f : di * x * sd[jj];
+          }
+          *reinterpret_cast<float4 *>(p.G32 + o + j) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+          __nv_bfloat162 h0 = __floats2bfloat162_rn(gv[0], gv[1]);
+          __nv_bfloat162 h1 = __floats2bfloat162_rn(gv[2], gv[3]);
           uint2 hv;
           hv.x = *reinterpret_cast<uint32_t *>(&h0);
           hv.y = *reinterpret_cast<uint32_t *>(&h1);
@@ -304,16 +393,14 @@ __global__ void __launch_bounds__(kNsfThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 128);
   }
-  // the apply GEMM may launch now (it waits for this grid to complete before reading)
-  ptx::pdl_launch_dependents();
 }
 
 }  // namespace
 
-cudaError_t launch_ns_fused(const CUtensorMap (&maps)[2][3], int batch, int r, int iters,
-                            float *ex0, float *ex1, const float *dinv, const int *flags, float *G32,
+cudaError_t launch_ns_fused(const CUtensorMap (&maps)[2][2], int batch, int r, int iters,
+                            float ridge, const float *G, float *ex0, float *ex1, float *G32,
                             __nv_bfloat16 *Ginv, int *status, cudaStream_t s) {
-  if (r <= 0 || r > 256 || r % 8 || iters <= 0) return cudaErrorInvalidValue;
+  if (r <= 0 || r > kNsMaxR || r % 8 || iters <= 0) return cudaErrorInvalidValue;
   if (batch <= 0) return cudaSuccess;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -324,15 +411,15 @@ cudaError_t launch_ns_fused(const CUtensorMap (&maps)[2][3], int batch, int r, i
   if (attr_err != cudaSuccess) return attr_err;
   NsMaps m;
   for (int i = 0; i < 2; ++i)
-    for (int j = 0; j < 3; ++j) m.m[i][j] = maps[i][j];
+    for (int j = 0; j < 2; ++j) m.m[i][j] = maps[i][j];
   NsParams p;
   p.r = r;
   p.rt = (r + 127) / 128;
   p.iters = iters;
+  p.ridge = ridge;
+  p.G = G;
   p.ex0 = ex0;
   p.ex1 = ex1;
-  p.dinv = dinv;
-  p.flags = flags;
   p.G32 = G32;
   p.Ginv = Ginv;
   p.status = status;

@@ -241,6 +241,11 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
 // Wait until the grid this one depends on (the previous kernel of the stream, when this one
 // was launched with programmatic stream serialization) has completed and its writes are
 // visible. Returns at once for a kernel launched without that attribute.
+// Every kernel here is launched with programmatic stream serialization and may start while
+// the previous kernel of the stream is still running and writing. Data written by earlier
+// kernels is therefore read only after this wait, and only through TMA or ld.global.cg
+// (__ldcg, served by the coherent L2): the L1 and the read-only (non-coherent) path of an SM
+// may hold lines from before the writer finished.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Allow the next kernel of the stream to begin launching (its pdl_wait still waits for this

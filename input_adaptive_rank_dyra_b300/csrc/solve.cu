@@ -9,19 +9,19 @@
 //     (padded to R x R, R = 32 or 64, by the identity) in place by block sweeps on 4 x 4
 //     pivot blocks -- Gauss-Jordan without pivoting, whose scalar pivots on an SPD matrix are
 //     the squared diagonal of the Cholesky factor -- with the matrix spread over the CTA's
-//     registers, and stores G^-1 (fp32 and bf16). spd_apply then forms C~ = G^-1 C in fp32 FMA, one CTA per sample and
+//     registers, and stores G^-1 (fp32 and bf16). The R-update of the forward runs the same sweeps in the epilogue of
+//     its Gram GEMM; this kernel serves the L-update of further ALS iterations. spd_apply then forms C~ = G^-1 C in fp32 FMA, one CTA per sample and
 //     128 columns of C, each thread a 4 x 8 block of the result.
-//   * larger r: Newton-Schulz. ns_prep scales G symmetrically to unit diagonal and starts
-//     from X0 = I / ||G_hat||_inf. The iteration X <- X (2I - G_hat X) runs in residual
-//     form: with E = I - G_hat X (a polynomial in G_hat, like X), X (2I - G_hat X) = X (I + E)
-//     and the next residual is E^2; ns_iterate (ns.cu) runs every iteration on tf32 tensor
-//     cores and undoes the scaling in one kernel; a tf32 tensor-core GEMM then forms
-//     C~ = G^-1 C.
+//   * larger r: Newton-Schulz (ns.cu): one cluster kernel scales G symmetrically to unit
+//     diagonal, starts from X0 = I / ||G_hat||_inf and runs X <- X (2I - G_hat X) in
+//     residual form (E = I - G_hat X, X' = X + X E, E' = E E) on tf32 tensor cores, then
+//     undoes the scaling; a tf32 tensor-core GEMM then forms C~ = G^-1 C.
 // A sample with a pivot that is not positive (or not finite) is counted in status[0] and
 // gets G^-1 = 0 and C~ = 0, so its correction vanishes and its output is the static branch
 // plus bias.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "sweep.cuh"
 
 #include <cuda_bf16.h>
 #include <mutex>
@@ -32,62 +32,19 @@ namespace {
 
 constexpr int kSolveCols = 128;   // columns of C per spd_apply CTA
 
-// p = -(m^-1) of an SPD 4 x 4 block by four scalar sweeps; false if a pivot is not positive
-// and finite.
-__device__ __forceinline__ bool sweep4(const float (&m)[4][4], float (&p)[4][4]) {
-  float w[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) w[i][j] = m[i][j];
-  bool ok = true;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float dk = w[k][k];
-    ok = ok && dk > 0.f && dk < INFINITY;
-    const float di = 1.f / dk;
-    float c[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] = w[i][k];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w[i][j] = fmaf(-c[i] * di, c[j], w[i][j]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      w[k][i] = c[i] * di;
-      w[i][k] = c[i] * di;
-    }
-    w[k][k] = -di;
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) p[i][j] = w[i][j];
-  return ok;
-}
-
-// (G + ridge I)^-1 for one sample by in-place block sweeps on 4 x 4 pivot blocks (block
-// Gauss-Jordan without pivoting; on an SPD matrix the pivot blocks are SPD Schur complements,
-// whose scalar pivots are the squared diagonal of the Cholesky factor), one CTA per sample.
-// With K the pivot block, P = A_KK^-1 and S_i = A_iK P, one block sweep is
-//   A_ij -= S_i A_Kj  (i, j outside K),  A_iK = S_i,  A_Kj = P A_Kj,  A_KK = -P,
-// and after the sweeps over all blocks the matrix holds -(G + ridge I)^-1 (the identity
-// padding up to R x R is never swept). Each of (R/4)^2 threads keeps one 4 x 4 block in
-// registers. The pivot columns of the next step (rows of 4, = its pivot rows by symmetry) and
-// the inverse of its pivot block, which the owner of that block forms after its update, go
-// through double-buffered shared memory: one barrier per step, r / 4 steps. The inverse goes
-// to Ginv32 (fp32, read by spd_apply) and Ginv (bf16).
+// (G + ridge I)^-1 for one sample, one CTA of (R/4)^2 threads: the block sweeps of
+// sweep::invert_blocks with the matrix in registers, one barrier per 4 x 4 pivot block. The
+// inverse goes to Ginv32 (fp32, read by spd_apply) and Ginv (bf16).
 template <int R>
 __global__ void __launch_bounds__((R / 4) * (R / 4))
     spd_invert_kernel(const float *__restrict__ G, int r, float ridge,
                       float *__restrict__ Ginv32, __nv_bfloat16 *__restrict__ Ginv, int *status) {
-  constexpr int Q = R / 4;   // 4 x 4 blocks per side; one thread per block
-  __shared__ __align__(16) float colbuf[2][R][4];   // the step's pivot columns A_iK
-  __shared__ __align__(16) float pinv[2][4][4];     // P of the step
-  __shared__ int bad_s;
+  constexpr int Q = R / 4;
+  __shared__ sweep::Smem<R> sm;
   const int tid = threadIdx.x, b = blockIdx.x;
   const int i0 = (tid / Q) * 4, j0 = (tid % Q) * 4;
+  // the apply kernel may start launching (it waits for this grid to finish before reading)
+  ptx::pdl_launch_dependents();
   // G comes from the previous kernel of the stream: nothing is read before this wait
   ptx::pdl_wait();
   float a[4][4];
@@ -98,98 +55,11 @@ __global__ void __launch_bounds__((R / 4) * (R / 4))
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const int i = i0 + u, j = j0 + v;
-        a[u][v] = (i < r && j < r) ? g[i * r + j] + (i == j ? ridge : 0.f) : (i == j ? 1.f : 0.f);
+        a[u][v] = (i < r && j < r) ? __ldcg(g + (size_t)i * r + j) + (i == j ? ridge : 0.f)
+                                   : (i == j ? 1.f : 0.f);
       }
   }
-  if (tid == 0) bad_s = 0;
-  __syncthreads();
-  if (j0 == 0) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      *reinterpret_cast<float4 *>(colbuf[0][i0 + u]) = make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
-  }
-  if (tid == 0) {   // owner of the first pivot block
-    float p[4][4];
-    if (!sweep4(a, p)) bad_s = 1;
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int v = 0; v < 4; ++v) pinv[0][u][v] = -p[u][v];
-  }
-  __syncthreads();
-  const int steps = r / 4;
-  for (int kb = 0; kb < steps; ++kb) {
-    const int k0 = kb * 4, cur = kb & 1;
-    {
-      float P[4][4], crow[4][4], ccol[4][4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4 pp = *reinterpret_cast<const float4 *>(pinv[cur][u]);
-        const float4 cr = *reinterpret_cast<const float4 *>(colbuf[cur][i0 + u]);
-        const float4 cc = *reinterpret_cast<const float4 *>(colbuf[cur][j0 + u]);
-        P[u][0] = pp.x; P[u][1] = pp.y; P[u][2] = pp.z; P[u][3] = pp.w;
-        crow[u][0] = cr.x; crow[u][1] = cr.y; crow[u][2] = cr.z; crow[u][3] = cr.w;
-        ccol[u][0] = cc.x; ccol[u][1] = cc.y; ccol[u][2] = cc.z; ccol[u][3] = cc.w;
-      }
-      const bool rowsK = i0 == k0, colsK = j0 == k0;
-      if (rowsK && colsK) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) a[u][v] = -P[u][v];
-      } else if (rowsK) {   // A_Kj = P A_Kj = (A_jK P)^T
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float t = 0.f;
-#pragma unroll
-            for (int l = 0; l < 4; ++l) t = fmaf(ccol[v][l], P[l][u], t);
-            a[u][v] = t;
-          }
-      } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float S[4];   // S_i = A_iK P
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            float t = 0.f;
-#pragma unroll
-            for (int l = 0; l < 4; ++l) t = fmaf(crow[u][l], P[l][m], t);
-            S[m] = t;
-          }
-          if (colsK) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) a[u][v] = S[v];
-          } else {
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-#pragma unroll
-              for (int m = 0; m < 4; ++m) a[u][v] = fmaf(-S[m], ccol[v][m], a[u][v]);
-          }
-        }
-      }
-      const int kn = k0 + 4;   // the next pivot block, after this step
-      if (kn < r) {
-        if (j0 == kn) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<float4 *>(colbuf[cur ^ 1][i0 + u]) =
-                make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
-        }
-        if (i0 == kn && j0 == kn) {
-          float p[4][4];
-          if (!sweep4(a, p)) bad_s = 1;
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) pinv[cur ^ 1][u][v] = -p[u][v];
-        }
-      }
-    }
-    __syncthreads();
-  }
-  const bool bad = bad_s != 0;
+  const bool bad = !sweep::invert_blocks<R>(a, tid, r, sm, []() { __syncthreads(); });
   if (i0 < r && j0 < r) {   // r % 4 == 0: a block is inside r x r or outside it
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -204,8 +74,6 @@ __global__ void __launch_bounds__((R / 4) * (R / 4))
     }
   }
   if (tid == 0 && bad) atomicAdd(status, 1);
-  // the apply kernel may launch now (it waits for this grid to complete before reading)
-  ptx::pdl_launch_dependents();
 }
 
 // Threads of spd_apply for the padded size R: R / 4 row groups x 16 column groups.
@@ -235,6 +103,8 @@ __global__ void __launch_bounds__(apply_threads<R>())
   float *Ct_s = apply_sm + R * R;       // [R][LDC]: Ct_s[j][c] = C[j][col0 + c]
   const int tid = threadIdx.x, b = blockIdx.y;
   const int col0 = blockIdx.x * kSolveCols;
+  // the next kernel may start launching (it waits for this grid to finish before reading)
+  ptx::pdl_launch_dependents();
   // G^-1 and C come from earlier kernels of the stream: nothing is read before this wait
   ptx::pdl_wait();
   {
@@ -245,7 +115,7 @@ __global__ void __launch_bounds__(apply_threads<R>())
 #pragma unroll
     for (int k = 0; k < GN; ++k) {
       const int t = tid + k * NT, i = (4 * t) / R, j = (4 * t) % R;
-      gv[k] = (i < r && j < r) ? __ldg(reinterpret_cast<const float4 *>(gi + (size_t)i * r + j))
+      gv[k] = (i < r && j < r) ? __ldcg(reinterpret_cast<const float4 *>(gi + (size_t)i * r + j))
                                : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     // thread t takes column c = t % 128 and rows 4 (t / 128) .. + 3 of C, per pass
@@ -255,7 +125,7 @@ __global__ void __launch_bounds__(apply_threads<R>())
     for (int k = 0; k < CN; ++k) {
       const int t = tid + k * NT, cc = t % kSolveCols, j4 = 4 * (t / kSolveCols);
       const int col = col0 + cc;
-      cv[k] = (col < d && j4 < r) ? __ldg(reinterpret_cast<const float4 *>(cp + (size_t)col * r + j4))
+      cv[k] = (col < d && j4 < r) ? __ldcg(reinterpret_cast<const float4 *>(cp + (size_t)col * r + j4))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
@@ -273,7 +143,6 @@ __global__ void __launch_bounds__(apply_threads<R>())
     }
   }
   __syncthreads();
-  ptx::pdl_launch_dependents();
   const int ty = tid / 16, tx = tid % 16;
   float acc[4][8];
 #pragma unroll
@@ -312,96 +181,6 @@ __global__ void __launch_bounds__(apply_threads<R>())
         if (cbase + v < d) op[v] = __float2bfloat16_rn(acc[u][v]);
     }
   }
-}
-
-// Newton-Schulz start. A sample's r x r matrix is spread over a cluster of ceil(r / 32)
-// CTAs of 32 warps: warp w of CTA c owns row 32 c + w, lane l the columns l, l + 32, ...
-// (at most kNsPer values per thread, all loaded before any is used). The row-sum maximum
-// goes through each CTA's shared memory and is read by the whole cluster through
-// distributed shared memory.
-constexpr int kNsThreads = 1024;
-constexpr int kNsPer = 8;   // columns per lane: r <= 32 * kNsPer
-
-__device__ __forceinline__ float ld_cluster_f32(const float *p, uint32_t rank) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];"
-               : "=f"(v)
-               : "r"(ptx::mapa_shared(ptx::smem_u32(p), rank))
-               : "memory");
-  return v;
-}
-
-// Jacobi scaling and start of Newton-Schulz in residual form: dinv = diag(G + lambda I)^-1/2,
-// G_hat = D (G + lambda I) D, alpha = 1 / max_i sum_j |G_hat_ij| (the max taken over the
-// cluster in a fixed order, so alpha is deterministic), and the iterate
-// EX[b] = [E0 ; X0 ; Y0] = [I - alpha G_hat ; alpha I ; 2I - alpha G_hat] ([3r][r], fp32).
-// A sample whose diagonal is not positive and finite gets alpha = 0: E0 = I and X0 = 0, so
-// every iterate and its G^-1 stay 0.
-__global__ void __launch_bounds__(kNsThreads)
-    ns_prep_kernel(const float *__restrict__ G, int r, float ridge, float *__restrict__ EX,
-                   float *__restrict__ dinv, int *__restrict__ flags) {
-  __shared__ float sd[32 * kNsPer];
-  __shared__ float red[32];
-  __shared__ float cmax;
-  const int c = blockIdx.x, b = blockIdx.y, nc = gridDim.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = 32 * c + warp;   // this warp's row
-  const float *g = G + (size_t)b * r * r;
-  float v[kNsPer];
-#pragma unroll
-  for (int q = 0; q < kNsPer; ++q) {
-    const int j = lane + 32 * q;
-    v[q] = (i < r && j < r) ? __ldg(g + (size_t)i * r + j) : 0.f;
-  }
-  bool bad = false;
-  if (tid < r) {
-    const float gii = __ldg(g + (size_t)tid * r + tid) + ridge;
-    bad = !(gii > 0.f && gii < INFINITY);
-    sd[tid] = bad ? 0.f : rsqrtf(gii);
-  }
-  bad = __syncthreads_or(bad) != 0;   // every CTA of the sample sees the whole diagonal
-  float rs = 0.f;
-#pragma unroll
-  for (int q = 0; q < kNsPer; ++q) {
-    const int j = lane + 32 * q;
-    float x = 0.f;
-    if (i < r && j < r && !bad) x = (v[q] + (i == j ? ridge : 0.f)) * sd[i] * sd[j];
-    v[q] = x;
-    rs += fabsf(x);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
-  if (lane == 0) red[warp] = rs;
-  __syncthreads();
-  if (warp == 0) {
-    float m = red[lane];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) cmax = m;
-  }
-  ptx::cluster_sync_all();   // every CTA's cmax is written
-  if (tid == 0) {
-    float m = 0.f;
-    for (int k = 0; k < nc; ++k) m = fmaxf(m, ld_cluster_f32(&cmax, (uint32_t)k));
-    red[0] = m;
-  }
-  ptx::cluster_sync_all();   // no CTA leaves while a peer may still read its cmax
-  const float alpha = (bad || !(red[0] > 0.f)) ? 0.f : 1.f / red[0];
-  if (i < r) {
-    float *E = EX + (size_t)b * 3 * r * r, *X = E + (size_t)r * r, *Y = X + (size_t)r * r;
-#pragma unroll
-    for (int q = 0; q < kNsPer; ++q) {
-      const int j = lane + 32 * q;
-      if (j < r) {
-        const float e = (i == j ? 1.f : 0.f) - alpha * v[q];
-        E[(size_t)i * r + j] = e;
-        X[(size_t)i * r + j] = (i == j) ? alpha : 0.f;
-        Y[(size_t)i * r + j] = (i == j ? 1.f : 0.f) + e;
-      }
-    }
-  }
-  if (c == 0 && tid < r) dinv[(size_t)b * r + tid] = bad ? 0.f : sd[tid];
-  if (c == 0 && tid == 0) flags[b] = bad ? 1 : 0;
 }
 
 }  // namespace
@@ -461,35 +240,5 @@ cudaError_t launch_spd_apply(const float *Ginv32, int batch, int r, const float 
   return launch_pdl(spd_apply_kernel<64>, grid, dim3(apply_threads<64>()), apply_smem<64>(), s,
                     Ginv32, r, Ct, d, Cs);
 }
-
-namespace {
-
-// Launch configuration of the Newton-Schulz helpers: a cluster of ceil(r / 32) CTAs per sample.
-cudaLaunchConfig_t ns_config(int batch, int r, cudaStream_t s, cudaLaunchAttribute *attr) {
-  const unsigned nc = (unsigned)((r + 31) / 32);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nc, (unsigned)batch, 1);
-  cfg.blockDim = dim3(kNsThreads, 1, 1);
-  cfg.stream = s;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = nc;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
-}  // namespace
-
-cudaError_t launch_ns_prep(const float *G, int batch, int r, float ridge, float *EX, float *dinv,
-                           int *flags, cudaStream_t s) {
-  if (r <= 0 || r > 32 * kNsPer) return cudaErrorInvalidValue;
-  if (batch <= 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = ns_config(batch, r, s, attr);
-  return cudaLaunchKernelEx(&cfg, ns_prep_kernel, G, r, ridge, EX, dinv, flags);
-}
-
 
 }  // namespace dyra

@@ -2,6 +2,7 @@
 // forward. See tc_gemm.cuh for the roles of the warps and the epilogue modes.
 #include "tc_gemm.cuh"
 #include "ptx.cuh"
+#include "sweep.cuh"
 
 #include <cuda_bf16.h>
 #include <cstring>
@@ -28,12 +29,52 @@ struct TileCoord {
   int bz, m_tile, n_tile;
 };
 
+// Shared-memory scratch of the EPI_CG_SOLVE epilogue.
+struct alignas(16) SolveSmem {
+  int got, ok, pad[2];
+  float Gs[64][68];        // G of a G tile, or G^-1 for a C tile (row pitch 68 floats)
+  sweep::Smem<32> s32;
+  sweep::Smem<64> s64;
+};
+
+// Named barrier of the 8 epilogue warps.
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ void st_release_gpu(int *p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Unit u of the persistent walk (n fastest); with pair MMAs (cluster = 2) a unit is a pair
 // of M tiles and CTA rank `crank` of the cluster takes M tile 2 * pair + crank (possibly one
 // past the last M tile: then its loads read zeros and its epilogue stores nothing).
 __device__ __forceinline__ TileCoord decode_tile(int u, const TcGemmParams &p, int mp_tiles,
                                                  int crank) {
   TileCoord c;
+  if (p.g_first) {   // single CTAs, one N tile, m_tiles = a_split + 1: every G tile first
+    c.n_tile = 0;
+    if (u < p.batch) {
+      c.bz = u;
+      c.m_tile = p.a_split;
+    } else {
+      u -= p.batch;
+      c.m_tile = u % p.a_split;
+      c.bz = u / p.a_split;
+    }
+    return c;
+  }
+  if (p.m_fast) {
+    c.m_tile = (u % mp_tiles) * p.cluster + crank;
+    const int rest = u / mp_tiles;
+    c.n_tile = rest % p.n_tiles;
+    c.bz = rest / p.n_tiles;
+    return c;
+  }
   c.n_tile = u % p.n_tiles;
   const int rest = u / p.n_tiles;
   c.m_tile = (rest % mp_tiles) * p.cluster + crank;
@@ -126,11 +167,208 @@ __device__ __forceinline__ void stage_bits32(uint32_t buf, int lane, const uint3
   }
 }
 
-// Warp roles. Every issuing loop runs on one lane and is a short dependent instruction chain,
-// so A and B are issued by two warps in parallel.
 constexpr int kWarpLoadA = 0, kWarpMma = 1, kWarpLoadB = 2;
 constexpr int kEpiWarp0 = 4, kEpiWarps = 8;      // warps 4..11: two per TMEM lane quarter
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+
+// Rows i0 .. i0 + 3, columns j0 .. j0 + 3 of G^-1 (the block holds -G^-1; 0 for a sample that
+// is not positive definite) to ginv32 (fp32) and ginv16 (bf16).
+__device__ __forceinline__ void store_ginv_block(const TcGemmParams &p, int bz, int r, int i0,
+                                                 int j0, const float (&a)[4][4], bool bad) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const size_t o = ((size_t)bz * r + i0 + u) * r + j0;
+    const float4 x = bad ? make_float4(0.f, 0.f, 0.f, 0.f)
+                         : make_float4(-a[u][0], -a[u][1], -a[u][2], -a[u][3]);
+    *reinterpret_cast<float4 *>(p.ginv32 + o) = x;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y), h1 = __floats2bfloat162_rn(x.z, x.w);
+    uint2 hv;
+    hv.x = *reinterpret_cast<uint32_t *>(&h0);
+    hv.y = *reinterpret_cast<uint32_t *>(&h1);
+    *reinterpret_cast<uint2 *>(p.ginv16 + o) = hv;
+  }
+}
+
+// EPI_CG_SOLVE epilogue, run by the 8 epilogue warps together (every decision is taken by one
+// thread, handed out through shared memory and a named barrier, so all 8 warps meet the same
+// barriers whatever a bounded wait returned).
+//   G tile (rows 0..r-1 of the accumulator): G to shared memory, the accumulator released,
+//     (G + ridge I)^-1 by block sweeps (sweep::invert_blocks over the 256 epilogue threads),
+//     G^-1 to ginv32 / ginv16, then ready[b] = 1 (release, after a fence).
+//   C^T tile (128 rows = input features g, r columns): wait until ready[b] is set (acquire,
+//     bounded), stage G^-1 in shared memory, count the tile in ready[batch + b] (the last of
+//     the sample's tiles clears both words for the next launch), read the tile's rows from TMEM (each thread a full
+//     row), release the accumulator, write C^T (fp32) and C~[b][i][g] = sum_j G^-1[i][j] C[j][g]
+//     (bf16), the two warps of a lane quarter splitting the r output rows.
+__device__ __noinline__ void cg_solve_epilogue(const TcGemmParams &p, uint8_t *smem, uint32_t base,
+                                               uint32_t tmem_base, uint32_t tfull_bar,
+                                               uint32_t tempty_bar, int cid, int ncl, int total,
+                                               int mp_tiles, int e, int lane, int c_lo, int c_hi) {
+  SolveSmem &ss = *reinterpret_cast<SolveSmem *>(smem + p.solve_off);
+  const int et = e * 32 + lane;   // 0 .. 255 over the epilogue warps
+  const int q = (kEpiWarp0 + e) & 3;
+  const int r = p.solve_r, d = p.cs_d;
+  uint32_t i = 0;
+  for (int t = cid; t < total; t += ncl, ++i) {
+    const uint32_t acc = i & 1u;
+    const TileCoord tc = decode_tile(t, p, mp_tiles, 0);
+    if (et == 0) ss.got = ptx::mbar_wait(tfull_bar + 8u * acc, (i >> 1) & 1u, p.timeouts) ? 1 : 0;
+    epi_bar();
+    const bool got = ss.got != 0;
+    epi_bar();   // every warp has read ss.got before thread 0 may write it again
+    if (!got) break;
+    ptx::tc_fence_after();
+    const uint32_t taddr = tmem_base + acc * p.acc_cols + ((uint32_t)(q * 32) << 16);
+    const int bz = tc.bz;
+    if (tc.m_tile >= p.a_split) {
+      // ---------------------------------------------------------------- G tile
+      const int row = q * 32 + lane;
+      if (q * 32 < r) {   // uniform per warp: this lane quarter holds rows of G
+        for (int c0 = c_lo; c0 < c_hi && c0 < r; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (row < r && c0 + j < r) ss.Gs[row][c0 + j] = __uint_as_float(v[j]);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tempty_bar + 8u * acc);   // the accumulator is free
+      epi_bar();
+      if (p.out2) {   // G itself (without the ridge), kept for checks of the intermediates
+        float *go = reinterpret_cast<float *>(p.out2) + (size_t)bz * r * r;
+        for (int k = et; k < r * r; k += 256) go[k] = ss.Gs[k / r][k % r];
+      }
+      // (G + ridge I)^-1 by block sweeps over the epilogue threads (R = 32: the first 64)
+      bool bad;
+      float a[4][4];
+      if (r <= 32) {
+        const int i0 = (et / 8) * 4, j0 = (et % 8) * 4;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int ii = i0 + u, jj = j0 + w;
+            a[u][w] = (et < 64 && ii < r && jj < r) ? ss.Gs[ii][jj] + (ii == jj ? p.ridge : 0.f)
+                                                    : (ii == jj ? 1.f : 0.f);
+          }
+        bad = !sweep::invert_blocks<32>(a, et, r, ss.s32, []() { epi_bar(); });
+        if (et < 64 && i0 < r && j0 < r) store_ginv_block(p, bz, r, i0, j0, a, bad);
+      } else {
+        const int i0 = (et / 16) * 4, j0 = (et % 16) * 4;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int ii = i0 + u, jj = j0 + w;
+            a[u][w] = (ii < r && jj < r) ? ss.Gs[ii][jj] + (ii == jj ? p.ridge : 0.f)
+                                         : (ii == jj ? 1.f : 0.f);
+          }
+        bad = !sweep::invert_blocks<64>(a, et, r, ss.s64, []() { epi_bar(); });
+        if (i0 < r && j0 < r) store_ginv_block(p, bz, r, i0, j0, a, bad);
+      }
+      __threadfence();
+      epi_bar();   // every thread's G^-1 stores are fenced
+      if (et == 0) {   // thread 0 took part in the inversion and holds its flag
+        if (bad) atomicAdd(p.nspd, 1);
+        st_release_gpu(p.ready + bz, 1);
+      }
+    } else {
+      // ---------------------------------------------------------------- C^T tile
+      if (et == 0) {
+        int ok = 0;
+        if (ld_acquire_gpu(p.ready + bz) != 0) {
+          ok = 1;
+        } else {
+          const unsigned long long t0 = ptx::global_timer();
+          for (;;) {
+            __nanosleep(200);
+            if (ld_acquire_gpu(p.ready + bz) != 0) {
+              ok = 1;
+              break;
+            }
+            if (ptx::global_timer() - t0 > ptx::kWaitLimitNs) {
+              atomicAdd(p.timeouts, 1);
+              break;
+            }
+          }
+        }
+        ss.ok = ok;
+      }
+      epi_bar();
+      const bool ok = ss.ok != 0;
+      {   // G^-1 of the sample into shared memory (L2 reads: another CTA wrote it)
+        const float *gi = p.ginv32 + (size_t)bz * r * r;
+        for (int k4 = et; k4 < r * r / 4; k4 += 256) {
+          const int ii = (4 * k4) / r, jj = (4 * k4) % r;
+          const float4 v = ok ? __ldcg(reinterpret_cast<const float4 *>(gi) + k4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4 *>(&ss.Gs[ii][jj]) = v;
+        }
+      }
+      epi_bar();   // G^-1 is staged
+      if (et == 0) {   // the last of the sample's C tiles to read G^-1 resets its flag
+        if (atomicAdd(p.ready + p.batch + bz, 1) == p.a_split - 1) {
+          p.ready[p.batch + bz] = 0;
+          p.ready[bz] = 0;
+        }
+      }
+      // this thread's row of C^T (input feature g), all r columns
+      const int g = (tc.m_tile * 128) + q * 32 + lane;
+      float cv[64];
+      {
+        uint32_t v[32];
+        ptx::tmem_ld32(taddr, v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) cv[j] = __uint_as_float(v[j]);
+        if (r > 32) {
+          ptx::tmem_ld32(taddr + 32u, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) cv[32 + j] = __uint_as_float(v[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) cv[32 + j] = 0.f;
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tempty_bar + 8u * acc);   // the accumulator is free
+      if (p.out && e < 4 && g < d) {   // C^T row (fp32), kept for checks of the intermediates
+        float *dst = reinterpret_cast<float *>(p.out) + (size_t)bz * p.out_bstride + (size_t)g * p.out_ld;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4)
+          if (j < r) *reinterpret_cast<float4 *>(dst + j) = make_float4(cv[j], cv[j + 1], cv[j + 2], cv[j + 3]);
+      }
+      const int h = r / 2, i_lo = e < 4 ? 0 : h, i_hi = e < 4 ? h : r;
+      if (g < d) {
+        __nv_bfloat16 *op = p.cs + (size_t)bz * r * d + g;
+        for (int ii = i_lo; ii < i_hi; ++ii) {
+          const float4 *gr = reinterpret_cast<const float4 *>(&ss.Gs[ii][0]);
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) {
+            if (4 * j4 < r) {
+              const float4 w = gr[j4];
+              s0 = fmaf(w.x, cv[4 * j4], s0);
+              s1 = fmaf(w.y, cv[4 * j4 + 1], s1);
+              s2 = fmaf(w.z, cv[4 * j4 + 2], s2);
+              s3 = fmaf(w.w, cv[4 * j4 + 3], s3);
+            }
+          }
+          op[(size_t)ii * d] = __float2bfloat16_rn((s0 + s1) + (s2 + s3));
+        }
+      }
+      epi_bar();   // the next tile may restage ss.Gs
+    }
+  }
+}
+
+// Warp roles. Every issuing loop runs on one lane and is a short dependent instruction chain,
+// so A and B are issued by two warps in parallel.
 
 // PMMA: cta_group::2 pair MMAs. A kernel holding pair instructions may only be launched as a
 // cluster, so the single-CTA engine is a separate instantiation without them.
@@ -430,7 +668,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool add_bias = p.tma_store && p.bias;
     uint32_t buf_i = 0, i = 0;
     TileCoord tcn = decode_tile(cid < total ? cid : 0, p, mp_tiles, crank);
-    for (int t = cid; t < total; t += ncl, ++i) {
+    if (p.epi == EPI_CG_SOLVE) {
+      cg_solve_epilogue(p, smem, base, tmem_base, tfull_bar, tempty_bar, cid, ncl, total,
+                        mp_tiles, e, lane, c_lo, c_hi);
+    }
+    for (int t = p.epi == EPI_CG_SOLVE ? total : cid; t < total; t += ncl, ++i) {
       const uint32_t acc = i & 1u;
       const TileCoord tc = tcn;
       if (t + ncl < total) tcn = decode_tile(t + ncl, p, mp_tiles, crank);
@@ -716,13 +958,20 @@ cudaError_t tc_gemm_launch(TcGemmParams p, const CUtensorMap &a0, const CUtensor
   // epilogue then sets the pace and alternates pairs without waiting), one pair otherwise,
   // which leaves room for more pipeline stages to hide the operand loads' latency.
   if (p.epi_bufs != 1 && p.epi_bufs != 2) p.epi_bufs = p.k_chunks <= 6 ? 2 : 1;
-  const uint32_t staging = p.tma_store ? (uint32_t)kEpiWarps * (uint32_t)p.epi_bufs * kStagingPairBytes : 0u;
+  uint32_t staging = p.tma_store ? (uint32_t)kEpiWarps * (uint32_t)p.epi_bufs * kStagingPairBytes : 0u;
+  if (p.epi == EPI_CG_SOLVE) {
+    if (p.pair_mma || p.n_tiles != 1 || p.m_tiles != p.a_split + 1 || !p.g_first ||
+        p.solve_r <= 0 || p.solve_r > 64 || p.solve_r % 4 || p.BN < p.solve_r)
+      return cudaErrorInvalidValue;
+    staging = ((uint32_t)sizeof(SolveSmem) + 1023u) & ~1023u;
+  }
   const uint32_t fixed = 1024u + staging + 256u;   // alignment slack, staging, barriers
   int S = (int)((232448u - fixed) / stage);
   if (S > 8) S = 8;
   if (S < 2) return cudaErrorInvalidValue;
   p.stages = S;
   p.staging_off = (uint32_t)S * stage;
+  p.solve_off = p.staging_off;
   p.bar_off = p.staging_off + staging;   // barriers follow the staging buffers
   uint32_t smem = (uint32_t)S * stage + fixed;
   // one CTA per SM: the two accumulators may take all 512 TMEM columns

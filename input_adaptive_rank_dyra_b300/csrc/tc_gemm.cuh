@@ -31,6 +31,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 
 namespace dyra {
 
@@ -38,9 +39,14 @@ enum TcEpi : int {
   EPI_ROW_BF16 = 0,    // out[b][g][c] = bf16(acc + bias[c]); TMA store when tma_store is set
   EPI_CG = 2,          // m tiles < a_split: out[b*bs + g*ld + c] = acc     (C^T, fp32)
                        // m tiles >= a_split: out2[b*bs2 + g*ld2 + c] = acc  (G, fp32)
-  EPI_ROW_F32 = 3      // m tiles < a_split: out[b][g][c] = alpha*acc + beta*aux[b][g][c]
+  EPI_ROW_F32 = 3,     // m tiles < a_split: out[b][g][c] = alpha*acc + beta*aux[b][g][c]
                        // m tiles >= a_split: out2[b][g][c] = alpha*acc + beta*aux2[b][g][c]
                        // (fp32; aux / aux2 may be null; 16-byte vector accesses)
+  EPI_CG_SOLVE = 5     // the Gram GEMM [X | L]^T L with the r <= 64 SPD solve folded in: the
+                       // G tile of a sample (walked first) is inverted by the epilogue warps
+                       // (block sweeps, solve_r <= 64) and published (ginv32 / ginv16, then
+                       // ready[b] = 1); a C^T tile waits for its sample's G^-1 and
+                       // writes C^T (out, fp32) and C~ = G^-1 C (cs [b][r][d], bf16)
 };
 
 struct TcGemmParams {
@@ -96,6 +102,20 @@ struct TcGemmParams {
   long long aux_bstride, aux_ld, aux2_bstride, aux2_ld;
   float alpha, beta;
   int *timeouts;                  // device counter of bounded waits that gave up
+  int m_fast;                     // walk M tiles fastest (a large B shared by few M tiles:
+                                  // the units running together read the same B columns)
+  // EPI_CG_SOLVE
+  int g_first;                    // the walk takes every sample's G tile first
+  int solve_r;                    // r (<= 64, % 4 == 0)
+  float ridge;
+  float *ginv32;                  // [batch][r][r] fp32 (G + ridge I)^-1
+  __nv_bfloat16 *ginv16;          // [batch][r][r] bf16
+  __nv_bfloat16 *cs;              // [batch][r][d] bf16 C~
+  int cs_d;                       // d
+  int *ready;                     // [2][batch]: G^-1 of the sample published; C tiles that
+                                  // have read it (the last one sets both back to 0)
+  int *nspd;                      // counter of samples that are not positive definite
+  uint32_t solve_off;             // shared-memory offset of the solve scratch
 };
 
 struct TcOperand {

@@ -232,6 +232,28 @@ def test_deterministic_and_host_path_identical():
     assert torch.equal(Yh.view(torch.int16), Y1.cpu().view(torch.int16))
 
 
+def test_host_path_in_sample_groups_identical():
+    """A batch large enough (84 MB of X and Y) for the host-buffer entry point to cut it into
+    eight groups of one sample, whose copies and forwards overlap on three streams: the same
+    bits as the device-buffer forward of the whole batch, and the status words clean."""
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    cfg = WL.reduced(WL.get_config("c3_fc1"), batch=8)
+    W, b, prep = weights_and_prep("c3_fc1")
+    X = WL.make_inputs(cfg)
+    layer = make_layer(cfg, prep, W, b)
+    Y1, ws = _run(layer, X, cfg.dtype)
+    Xh = to_device(X, "bf16").cpu().pin_memory()
+    Yh = torch.full(Y1.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    Xs = torch.empty_like(Xh, device="cuda")
+    Ys = torch.empty(Y1.shape, dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):
+        dy.linear_forward_host(layer, Xh, Yh, Xs, Ys, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(Yh.view(torch.int16), Y1.cpu().view(torch.int16))
+        assert dy.workspace_status(layer, ws) == (0, 0)
+
+
 def test_profiled_forward_records_every_kernel():
     import torch
     import input_adaptive_rank_dyra_b300 as dy

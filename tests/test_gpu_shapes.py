@@ -177,3 +177,82 @@ def test_bounded_wait_runs_out_and_reports_timeout():
     assert int(words[1].item()) == 1 and int(words[0].item()) == 0
     cfg, W, b, prep = _variant("c2", 2, 64)
     _check(cfg, W, b, prep)                                  # the device still works
+
+
+def test_fused_gram_solve_more_samples_than_sms():
+    """The Cholesky branch folds the solve into the Gram GEMM: the kernel walks every sample's
+    G tile before any C^T tile. With 300 samples (more than the 148 persistent CTAs) each CTA
+    inverts two or three G tiles first, and most C^T tiles wait for a G^-1 that another CTA
+    published. r = 32 takes the 32-wide block sweep, r = 64 the 64-wide one; every sample's
+    G, G^-1 and C~ = G^-1 C against the oracle. 197 tokens per sample keep every G well
+    conditioned (condition number below 400; with 64 tokens and r = 64 it reaches 1e10 and
+    the fp32 sweep rightly reports samples that are not positive definite)."""
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    for r in (32, 64):
+        cfg, W, b, prep = _variant("c2", 300, 197, r=r)
+        X = WL.make_inputs(cfg)
+        layer = make_layer(cfg, prep, W, b)
+        assert layer.solver == "cholesky" and "cg_solve" in layer.kernel_names()
+        Y, ws = _forward(layer, X)
+        assert dy.workspace_status(layer, ws) == (0, 0)
+        Yo, inter = O.forward(X, prep, keep=True, solver="cholesky")
+        B_, d = cfg.batch, cfg.d
+        Go = np.stack(inter["G"])
+        G = to_host(dy.workspace_view(layer, ws, B_, cfg.n, "G", (B_, r, r), torch.float32))
+        Gi = to_host(dy.workspace_view(layer, ws, B_, cfg.n, "GINV", (B_, r, r), torch.bfloat16))
+        Cs = to_host(dy.workspace_view(layer, ws, B_, cfg.n, "CS", (B_, r, d), torch.bfloat16))
+        Gi_o = np.linalg.inv(Go)
+        Cs_o = Gi_o @ np.stack(inter["C"])
+        Yg = to_host(Y)
+        for s in range(B_):
+            assert rel(G[s], Go[s]) <= BF16_TOL, f"G, sample {s}"
+            assert rel(Gi[s], Gi_o[s]) <= BF16_TOL, f"G^-1, sample {s}"
+            assert rel(Cs[s], Cs_o[s]) <= BF16_TOL, f"C~, sample {s}"
+            assert rel(Yg[s], Yo[s]) <= BF16_TOL, f"Y, sample {s}"
+        layer.close()
+
+
+def test_fused_gram_solve_flags_clear_between_forwards():
+    """The fused kernel's per-sample flags: the last C^T tile of a sample clears them, and
+    every forward clears them first. Three forwards on one workspace give the same output
+    bit for bit, and in an MLP block whose fc1 (Newton-Schulz) lays its buffers over the
+    bytes of fc2's flags, fc2 still waits for its own G^-1."""
+    import torch
+    import input_adaptive_rank_dyra_b300 as dy
+    cfg, W, b, prep = _variant("c2", 5, 197)
+    X = WL.make_inputs(cfg)
+    layer = make_layer(cfg, prep, W, b)
+    Xd = to_device(X, "bf16")
+    ws = dy.new_workspace(layer, cfg.batch, cfg.n)
+    outs = []
+    for _ in range(3):
+        outs.append(dy.linear_forward(layer, Xd, workspace=ws))
+    torch.cuda.synchronize()
+    assert dy.workspace_status(layer, ws) == (0, 0)
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    assert rel(to_host(outs[0]), O.forward(X, prep)) <= BF16_TOL
+    layer.close()
+
+    c1, c2 = WL.get_config("c3_fc1"), WL.get_config("c3_fc2")
+    W1, b1 = WL.make_weights(c1)
+    W2, b2 = WL.make_weights(c2)
+    p1 = O.prepare(W1, b1, "lowrank", c1.k, c1.r)
+    p2 = O.prepare(W2, b2, "lowrank", c2.k, c2.r)
+    batch, n = 2, 300
+    Xm = WL.make_inputs(WL.reduced(c1, batch=batch, n=n))
+    fc1 = dy.prepare(W1, b1, kind="lowrank", k=c1.k, r=c1.r, F1=p1["F1"], F2=p1["F2"],
+                     R0=p1["R0"], dtype="bf16", device=0, activation="gelu",
+                     solver="newton_schulz")
+    fc2 = dy.prepare(W2, b2, kind="lowrank", k=c2.k, r=c2.r, F1=p2["F1"], F2=p2["F2"],
+                     R0=p2["R0"], dtype="bf16", device=0)
+    assert "cg_solve" not in fc1.kernel_names() and "cg_solve" in fc2.kernel_names()
+    wsm = torch.empty(max(fc1.workspace_size(batch, n), fc2.workspace_size(batch, n)),
+                      dtype=torch.uint8, device="cuda")
+    Ym = dy.mlp_forward(fc1, fc2, to_device(Xm, "bf16"), workspace=wsm)
+    torch.cuda.synchronize()
+    assert dy.workspace_status(fc2, wsm) == (0, 0)
+    H = O.gelu(O.forward(Xm, p1, solver="newton_schulz", ns_iters=fc1.ns_iters))
+    assert rel(to_host(Ym), O.forward(H, p2)) <= BF16_TOL
+    fc1.close()
+    fc2.close()

@@ -52,9 +52,9 @@ def bench_config(name):
 _CSRC = "input_adaptive_rank_dyra_b300/csrc/"
 # the source files that define each kernel of the forward (a recorded DRAM-traffic figure is
 # used only while their hash matches the one recorded with it)
-GEMM_SOURCES = [_CSRC + "tc_gemm.cu", _CSRC + "tc_gemm.cuh", _CSRC + "ptx.cuh",
-                _CSRC + "sweep.cuh"]
-KERNEL_SOURCES = {"spd_invert": [_CSRC + "solve.cu", _CSRC + "kernels.cuh", _CSRC + "sweep.cuh"],
+GEMM_SOURCES = [_CSRC + "tc_gemm.cu", _CSRC + "tc_gemm.cuh", _CSRC + "ptx.cuh"]
+KERNEL_SOURCES = {"cg_solve": GEMM_SOURCES + [_CSRC + "sweep.cuh"],   # the inversion in its epilogue
+                  "spd_invert": [_CSRC + "solve.cu", _CSRC + "kernels.cuh", _CSRC + "sweep.cuh"],
                   "spd_apply_c": [_CSRC + "solve.cu", _CSRC + "kernels.cuh"],
                   "ns_iterate": [_CSRC + "ns.cu", _CSRC + "ptx.cuh", _CSRC + "kernels.cuh"],
                   "monarch_permute": [_CSRC + "monarch.cu", _CSRC + "monarch.cuh"]}

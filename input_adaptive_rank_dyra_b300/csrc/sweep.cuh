@@ -19,10 +19,16 @@ namespace sweep {
 // Shared memory of one inversion.
 template <int R>
 struct alignas(16) Smem {
-  float colbuf[2][R][4];   // the step's pivot columns A_iK
+  float colbuf[2][R][4];   // the step's pivot columns A_iK, row i at cb_row<R>(i)
   float pinv[2][4][4];     // P of the step
   int bad;                 // a pivot was not positive and finite
 };
+
+// Position of row i of the pivot columns: rows with the same i % 4 are contiguous, so the 16-byte
+// reads of one warp (rows 4k + u for every block column k, u fixed) hit distinct banks; with
+// row i at position i the same reads were 8-way bank conflicts.
+template <int R>
+__device__ __forceinline__ int cb_row(int i) { return (i & 3) * (R / 4) + (i >> 2); }
 
 // p = -(m^-1) of an SPD 4 x 4 block by four scalar sweeps; false if a pivot is not positive
 // and finite. The four pivot reciprocals are the longest dependent chain of a step, so they
@@ -76,7 +82,8 @@ __device__ __forceinline__ bool invert_blocks(float (&a)[4][4], int tid, int r, 
   if (el && j0 == 0) {
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      *reinterpret_cast<float4 *>(sm.colbuf[0][i0 + u]) = make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
+      *reinterpret_cast<float4 *>(sm.colbuf[0][cb_row<R>(i0 + u)]) =
+          make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
   }
   if (tid == 0) {   // owner of the first pivot block
     float p[4][4];
@@ -95,8 +102,8 @@ __device__ __forceinline__ bool invert_blocks(float (&a)[4][4], int tid, int r, 
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const float4 pp = *reinterpret_cast<const float4 *>(sm.pinv[cur][u]);
-        const float4 cr = *reinterpret_cast<const float4 *>(sm.colbuf[cur][i0 + u]);
-        const float4 cc = *reinterpret_cast<const float4 *>(sm.colbuf[cur][j0 + u]);
+        const float4 cr = *reinterpret_cast<const float4 *>(sm.colbuf[cur][cb_row<R>(i0 + u)]);
+        const float4 cc = *reinterpret_cast<const float4 *>(sm.colbuf[cur][cb_row<R>(j0 + u)]);
         P[u][0] = pp.x; P[u][1] = pp.y; P[u][2] = pp.z; P[u][3] = pp.w;
         crow[u][0] = cr.x; crow[u][1] = cr.y; crow[u][2] = cr.z; crow[u][3] = cr.w;
         ccol[u][0] = cc.x; ccol[u][1] = cc.y; ccol[u][2] = cc.z; ccol[u][3] = cc.w;
@@ -144,7 +151,7 @@ __device__ __forceinline__ bool invert_blocks(float (&a)[4][4], int tid, int r, 
         if (j0 == kn) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<float4 *>(sm.colbuf[cur ^ 1][i0 + u]) =
+            *reinterpret_cast<float4 *>(sm.colbuf[cur ^ 1][cb_row<R>(i0 + u)]) =
                 make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
         }
         if (i0 == kn && j0 == kn) {

@@ -171,6 +171,41 @@ constexpr int kWarpLoadA = 0, kWarpMma = 1, kWarpLoadB = 2;
 constexpr int kEpiWarp0 = 4, kEpiWarps = 8;      // warps 4..11: two per TMEM lane quarter
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 
+// C~[i][g] = sum_j G^-1[i][j] C[j][g] for rows i_lo .. i_hi - 1 of one feature g (cv = the
+// feature's C column, zero past r; G^-1 rows in shared memory, zero-padded to RR columns past
+// r). Each row of G^-1 is read into registers before its FMAs (the reads of one row are
+// independent), and two rows go at once.
+template <int RR>
+__device__ __forceinline__ void apply_rows(const float (&Gs)[64][68], const float (&cv)[64],
+                                           int i_lo, int i_hi, int d, __nv_bfloat16 *op) {
+  constexpr int V = RR / 4;
+  for (int ii = i_lo; ii < i_hi; ii += 2) {
+    const bool two = ii + 1 < i_hi;
+    const float4 *g0 = reinterpret_cast<const float4 *>(&Gs[ii][0]);
+    const float4 *g1 = reinterpret_cast<const float4 *>(&Gs[two ? ii + 1 : ii][0]);
+    float4 w0[V], w1[V];
+#pragma unroll
+    for (int j4 = 0; j4 < V; ++j4) {
+      w0[j4] = g0[j4];
+      w1[j4] = g1[j4];
+    }
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+#pragma unroll
+    for (int j4 = 0; j4 < V; ++j4) {
+      s0 = fmaf(w0[j4].x, cv[4 * j4], s0);
+      s1 = fmaf(w0[j4].y, cv[4 * j4 + 1], s1);
+      s2 = fmaf(w0[j4].z, cv[4 * j4 + 2], s2);
+      s3 = fmaf(w0[j4].w, cv[4 * j4 + 3], s3);
+      t0 = fmaf(w1[j4].x, cv[4 * j4], t0);
+      t1 = fmaf(w1[j4].y, cv[4 * j4 + 1], t1);
+      t2 = fmaf(w1[j4].z, cv[4 * j4 + 2], t2);
+      t3 = fmaf(w1[j4].w, cv[4 * j4 + 3], t3);
+    }
+    op[(size_t)ii * d] = __float2bfloat16_rn((s0 + s1) + (s2 + s3));
+    if (two) op[(size_t)(ii + 1) * d] = __float2bfloat16_rn((t0 + t1) + (t2 + t3));
+  }
+}
+
 // Rows i0 .. i0 + 3, columns j0 .. j0 + 3 of G^-1 (the block holds -G^-1; 0 for a sample that
 // is not positive definite) to ginv32 (fp32) and ginv16 (bf16).
 __device__ __forceinline__ void store_ginv_block(const TcGemmParams &p, int bz, int r, int i0,
@@ -307,6 +342,9 @@ __device__ __noinline__ void cg_solve_epilogue(const TcGemmParams &p, uint8_t *s
                               : make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4 *>(&ss.Gs[ii][jj]) = v;
         }
+        // columns r .. RR - 1 of those rows (RR = 32 or 64, what the apply reads) are zero
+        const int pad = (r <= 32 ? 32 : 64) - r;
+        for (int k = et; k < r * pad; k += 256) ss.Gs[k / pad][r + k % pad] = 0.f;
       }
       epi_bar();   // G^-1 is staged
       if (et == 0) {   // the last of the sample's C tiles to read G^-1 resets its flag
@@ -346,21 +384,10 @@ __device__ __noinline__ void cg_solve_epilogue(const TcGemmParams &p, uint8_t *s
       const int h = r / 2, i_lo = e < 4 ? 0 : h, i_hi = e < 4 ? h : r;
       if (g < d) {
         __nv_bfloat16 *op = p.cs + (size_t)bz * r * d + g;
-        for (int ii = i_lo; ii < i_hi; ++ii) {
-          const float4 *gr = reinterpret_cast<const float4 *>(&ss.Gs[ii][0]);
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
-            if (4 * j4 < r) {
-              const float4 w = gr[j4];
-              s0 = fmaf(w.x, cv[4 * j4], s0);
-              s1 = fmaf(w.y, cv[4 * j4 + 1], s1);
-              s2 = fmaf(w.z, cv[4 * j4 + 2], s2);
-              s3 = fmaf(w.w, cv[4 * j4 + 3], s3);
-            }
-          }
-          op[(size_t)ii * d] = __float2bfloat16_rn((s0 + s1) + (s2 + s3));
-        }
+        if (r <= 32)
+          apply_rows<32>(ss.Gs, cv, i_lo, i_hi, d, op);
+        else
+          apply_rows<64>(ss.Gs, cv, i_lo, i_hi, d, op);
       }
       epi_bar();   // the next tile may restage ss.Gs
     }

@@ -232,9 +232,10 @@ __device__ __forceinline__ void store_ginv_block(const TcGemmParams &p, int bz, 
 //     G^-1 to ginv32 / ginv16, then ready[b] = 1 (release, after a fence).
 //   C^T tile (128 rows = input features g, r columns): wait until ready[b] is set (acquire,
 //     bounded), stage G^-1 in shared memory, count the tile in ready[batch + b] (the last of
-//     the sample's tiles clears both words for the next launch), read the tile's rows from TMEM (each thread a full
-//     row), release the accumulator, write C^T (fp32) and C~[b][i][g] = sum_j G^-1[i][j] C[j][g]
-//     (bf16), the two warps of a lane quarter splitting the r output rows.
+//     the sample's tiles clears both words for the next launch), read the tile's rows from
+//     TMEM (each thread a full row), release the accumulator, write C^T (fp32) and
+//     C~[b][i][g] = sum_j G^-1[i][j] C[j][g] (bf16), the two warps of a lane quarter splitting
+//     the r output rows.
 __device__ __noinline__ void cg_solve_epilogue(const TcGemmParams &p, uint8_t *smem, uint32_t base,
                                                uint32_t tmem_base, uint32_t tfull_bar,
                                                uint32_t tempty_bar, int cid, int ncl, int total,

@@ -550,3 +550,37 @@ def test_c1_dyra_beats_static_truncation():
     U2, V2 = O.tsvd_factors(W, cfg.k + cfg.r)
     e_static_kr = O.approximation_error(X @ (U2 @ V2) + b, X, W, b)
     assert e_dyra < e_static_kr < e_static
+
+
+def test_input_aware_scaling_hand_values():
+    """The input-side transform on a 2 x 2 calibration matrix worked out by hand:
+    X_cal = [[1, 2], [3, 4]] has channel mean squares 5 and 10, so diag gives
+    diag(sqrt 5, sqrt 10); its covariance X_cal^T X_cal / 2 = [[5, 7], [7, 10]] has the lower
+    Cholesky factor [[sqrt 5, 0], [7 / sqrt 5, sqrt(10 - 49 / 5)]]."""
+    X = np.array([[1.0, 2.0], [3.0, 4.0]])
+    S = O.input_aware_scaling(X, "diag")
+    assert np.allclose(S, np.diag([np.sqrt(5.0), np.sqrt(10.0)]), atol=1e-15)
+    L = O.input_aware_scaling(X, "cholesky")
+    expect = np.array([[np.sqrt(5.0), 0.0], [7.0 / np.sqrt(5.0), np.sqrt(10.0 - 49.0 / 5.0)]])
+    assert np.allclose(L, expect, atol=1e-14)
+    with pytest.raises(ValueError):
+        O.input_aware_scaling(X, "other")
+
+
+def test_top_right_singular_subspace_and_energy():
+    """R0 of a residual with a planted SVD: orthonormal rows spanning the top-r right singular
+    subspace, and W_res R0^T R0 keeps exactly the top-r singular values' energy
+    (Eckart-Young), whatever basis the SVD returns for that subspace."""
+    rng = _rng(31)
+    d, m, r = 12, 9, 3
+    Q1, _ = np.linalg.qr(rng.standard_normal((d, m)))
+    Q2, _ = np.linalg.qr(rng.standard_normal((m, m)))
+    sv = np.array([9.0, 7.0, 5.0, 1.0, 0.8, 0.5, 0.3, 0.2, 0.1])
+    W_res = Q1 @ np.diag(sv) @ Q2.T
+    R0 = O.top_right_singular(W_res, r)
+    assert R0.shape == (r, m)
+    assert np.allclose(R0 @ R0.T, np.eye(r), atol=1e-12)
+    top = Q2[:, :r]
+    assert np.allclose(R0.T @ R0, top @ top.T, atol=1e-12)
+    kept = np.linalg.norm(W_res @ R0.T @ R0) ** 2
+    assert np.isclose(kept, np.sum(sv[:r] ** 2), rtol=1e-12)

@@ -1839,7 +1839,12 @@ dyra_status dyra_linear_forward_host(const dyra_layer *L, const void *X_host, in
     dyra_status st = forward_impl(L, static_cast<const uint8_t *>(X_dev) + xo, b1 - b0, n,
                                   static_cast<uint8_t *>(Y_dev) + yo, workspace, workspace_bytes,
                                   stream, rec, false);
-    if (st != DYRA_OK) return st;
+    if (st != DYRA_OK) {   // `stream` still ends after the copies already enqueued
+      cudaEventRecord(ev[1], L->copy_out);
+      cudaStreamWaitEvent(stream, ev[1], 0);
+      cudaStreamWaitEvent(stream, in_done, 0);
+      return st;
+    }
     DY_CUDA(cudaEventRecord(fwd_done, stream));
     DY_CUDA(cudaStreamWaitEvent(L->copy_out, fwd_done, 0));
     DY_CUDA(cudaMemcpyAsync(static_cast<uint8_t *>(Y_host) + yo,

@@ -42,7 +42,7 @@ extern "C" {
 typedef enum dyra_status {
   DYRA_OK = 0,
   DYRA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shapes            */
-  DYRA_ERR_UNSUPPORTED = 2,   /* valid request that this build does not implement       */
+  DYRA_ERR_UNSUPPORTED = 2,   /* valid request that this library does not implement     */
   DYRA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (see dyra_last_error) */
   DYRA_ERR_OOM = 4,           /* device or host allocation failed in dyra_prepare       */
   DYRA_ERR_NOT_SPD = 5,       /* reported by dyra_workspace_status: some L^T L + lambda I

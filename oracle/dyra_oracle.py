@@ -40,7 +40,7 @@ Readings taken where the pages are silent (the same list is kept with the design
     sweeps;
   * Newton-Schulz: Jacobi scaling G_hat = D G D with D = diag(G)^-1/2, X0 = I/||G_hat||_inf,
     X_{t+1} = X_t (2I - G_hat X_t), G^-1 ~ D X_T D;
-  * input-aware decomposition, written for this build's row-vector convention y = x W:
+  * input-aware decomposition, written for the row-vector convention y = x W used here:
     W_hat = S^-T TSVD_k(S^T W), with S = diag(channel rms) or the lower Cholesky factor of the
     calibration covariance; R0 and P are then formed from W_res as for the plain fit;
   * one least-squares system per sample over all of its n tokens;
@@ -171,7 +171,7 @@ def input_aware_scaling(X_cal: np.ndarray, mode: str) -> np.ndarray:
     section: S built from calibration activations).
       "diag":     S = diag(rms of each input channel over the calibration rows);
       "cholesky": S = the lower Cholesky factor of the covariance X_cal^T X_cal / N.
-    In the row-vector convention y = x W of this build the output error over the calibration
+    In the row-vector convention y = x W used here the output error over the calibration
     rows is ||X_cal (W - W_hat)||_F, which equals ||S^T (W - W_hat)||_F for the Cholesky
     factor (X_cal^T X_cal / N = S S^T), up to the factor sqrt(N)."""
     N = X_cal.shape[0]
@@ -248,7 +248,7 @@ def prepare(W: np.ndarray, b: np.ndarray, kind: str, k: int, r: int,
 
 def newton_schulz_inverse(G: np.ndarray, iters: int) -> np.ndarray:
     """Approximate G^-1 of an SPD matrix by Newton-Schulz ([S] 2.4: Newton-Schulz for
-    larger r). Start and scaling are this build's reading (module docstring)."""
+    larger r). Start and scaling are a reading of the pages (module docstring)."""
     dinv = 1.0 / np.sqrt(np.diag(G))
     Gh = G * dinv[:, None] * dinv[None, :]
     alpha = 1.0 / np.max(np.sum(np.abs(Gh), axis=1))
